@@ -1,0 +1,391 @@
+#!/usr/bin/env python3
+"""Benchmark of the FORGE fused backward step on Llama-3.1-8B-shaped linears.
+
+One step = the backward of the seven linear layers of one decoder layer
+(down, up, gate, o, v, k, q; T = 16384 tokens): for each layer, dX = dY W from
+the pre-update weights, then the fused weight-gradient + AdamW step (bf16
+weights with stochastic rounding, fp32 moments).  Inputs are seeded synthetic
+tensors resident in HBM; each activation/gradient tensor is >= 134 MB, larger
+than the 129 MB L2, so no L2 flush is needed between steps.
+
+Printed: one JSON line (rank 0).  ``value`` = (2NKT for dW + 2NKT for dX,
+summed over the layers and ranks) / step time, in TFLOP/s.  ``roofline`` is the
+fused wgrad+optimizer kernel's own rate (CUDA events around its launches)
+against the measured dense-bf16 peak.  ``e2e`` repeats the step with the
+inputs copied from pinned host memory inside the timed region.  ``unfused``
+times the two-pass schedule (fp32 dW for every layer, then the optimizer).
+
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload instead (no GPU work).
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from optimizer_tcgen05_dw_gb300 import inputs  # noqa: E402
+
+METRIC = "fused wgrad+optimizer TFLOP/s and % of roofline at Llama-8B linear shapes"
+WORKLOAD_KEY = "llama8b_bf16_fp32state"
+# backward order through the decoder layer, and which activation feeds each linear
+ORDER = ["down_proj", "up_proj", "gate_proj", "o_proj", "v_proj", "k_proj", "q_proj"]
+ACT = {"q_proj": "x_attn", "k_proj": "x_attn", "v_proj": "x_attn", "o_proj": "x_o",
+       "gate_proj": "x_mlp", "up_proj": "x_mlp", "down_proj": "x_down"}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# Reference arm: the CPU oracle
+# ----------------------------------------------------------------------------
+
+def oracle_sample(layer="k_proj", T=16384, seed=7):
+    """One oracle step (dX + dW + AdamW, bf16 SR) on one Llama linear.  Returns
+    (seconds, flops counted like the GPU metric)."""
+    from oracle import linear_step as ls
+    from oracle import optimizers as opt
+    from oracle import rounding
+    w = inputs.WORKLOADS[WORKLOAD_KEY]
+    N, K = {n: (a, b) for n, a, b in inputs.LLAMA31_8B_LINEARS}[layer]
+    X = inputs.bf16_to_bits(inputs.normal((T, K), 1.0, seed))
+    dY = inputs.bf16_to_bits(inputs.normal((T, N), w.dy_std, seed + 1))
+    W = rounding.bf16_bits_rne(inputs.normal((N, K), 0.02, seed + 2, torch.float32).numpy())
+    st = {"W": W, "w_dtype": "bf16", "s_dtype": "fp32", "s1": np.zeros((N, K), np.float32),
+          "s2": np.zeros((N, K), np.float32)}
+    t0 = time.perf_counter()
+    ls.linear_bwd_step(X, dY, st, opt.ADAMW, opt.Hparams(**w.hparams), 1, seed, want_dx=True)
+    dt = time.perf_counter() - t0
+    return dt, 4.0 * N * K * T
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    for _ in range(args.warmup):
+        oracle_sample()
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, f = oracle_sample()
+        times.append(dt)
+        flops = f
+    tot = sum(times)
+    val = flops * len(times) / tot / 1e12
+    sample = ("one k_proj linear (1024x4096, T=16384) per step: dX + dW + AdamW with bf16 "
+              "stochastic rounding, numpy float64 GEMMs on all host cores")
+    print(json.dumps({
+        "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": inputs.WORKLOADS[WORKLOAD_KEY].name, "sample": "k_proj per step"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# Our arm
+# ----------------------------------------------------------------------------
+
+class Layer:
+    def __init__(self, name, N, K, T, dev, seed, host=False):
+        self.name, self.N, self.K, self.T = name, N, K, T
+        self.W = inputs.normal((N, K), 0.02, seed, torch.bfloat16, dev)
+        self.m = torch.zeros((N, K), dtype=torch.float32, device=dev)
+        self.v = torch.zeros((N, K), dtype=torch.float32, device=dev)
+        self.dY = inputs.normal((T, N), 1e-3, seed + 1, torch.bfloat16, dev)
+        self.dX = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+        self.seed = seed
+
+
+def build_workload(dev, T):
+    acts = {"x_attn": 4096, "x_o": 4096, "x_mlp": 4096, "x_down": 14336}
+    X = {a: inputs.normal((T, k), 1.0, 100 + i, torch.bfloat16, dev) for i, (a, k) in enumerate(acts.items())}
+    shapes = {n: (N, K) for n, N, K in inputs.LLAMA31_8B_LINEARS}
+    layers = [Layer(n, *shapes[n], T, dev, 1000 + 17 * i) for i, n in enumerate(ORDER)]
+    return X, layers
+
+
+def run_ours(args):
+    from optimizer_tcgen05_dw_gb300 import api
+    from optimizer_tcgen05_dw_gb300.build import build
+
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        dist_mod.init_process_group("nccl", device_id=torch.device("cuda", local))
+        dist = dist_mod
+    build()
+    api.lib()
+    dev = torch.device("cuda", local)
+    w = inputs.WORKLOADS[WORKLOAD_KEY]
+    T = w.T
+    hp = w.hparams
+    X, layers = build_workload(dev, T)
+    stream = torch.cuda.current_stream()
+    flops_dw = sum(2.0 * L.N * L.K * T for L in layers)
+    flops_step = 2.0 * flops_dw  # dW + dX
+
+    ev = {L.name: [] for L in layers}
+
+    def step(s, record=False):
+        for L in layers:
+            api.forge_linear_dgrad(L.dY, L.W, L.dX)
+            if record:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+            api.forge_linear_bwd_step(X[ACT[L.name]], L.dY, L.W, "adamw", hp, s, L.seed, L.m, L.v)
+            if record:
+                b.record(stream)
+                ev[L.name].append((a, b))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    s_no = 1
+    for _ in range(args.warmup):
+        step(s_no)
+        s_no += 1
+    api.forge_get_device_status()
+    barrier()
+    with ClockSampler(local) as clk:
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        barrier()
+        start.record(stream)
+        for _ in range(args.steps):
+            step(s_no, record=True)
+            s_no += 1
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    api.forge_get_device_status()
+    ms = start.elapsed_time(end) / args.steps
+    ms = max_over_ranks(ms)
+    fused_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev[L.name])
+    fused_launches = sum(len(v) for v in ev.values())
+    fused_tflops = flops_dw * args.steps / (fused_ms * 1e-3) / 1e12
+    hbm_gbs, peak_burst, peak_sust, peak_src = _peaks()
+    value = flops_step * world / (ms * 1e-3) / 1e12
+    per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev[L.name]]) * 1e-3) / 1e12, 1)
+                 for L in layers}
+    # algorithmic bytes of the fused kernel per step: X and dY once, W r/w (bf16), m and v r/w (fp32)
+    params = sum(L.N * L.K for L in layers)
+    bytes_fused = sum((L.T * L.K + L.T * L.N) * 2 for L in layers) + params * (4 + 16)
+
+    # ---- e2e: inputs from pinned host memory every step
+    hostX = {k: v.cpu().pin_memory() for k, v in X.items()}
+    hostdY = {L.name: L.dY.cpu().pin_memory() for L in layers}
+    h2d = sum(t.numel() * 2 for t in hostX.values()) + sum(t.numel() * 2 for t in hostdY.values())
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 4)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k in X:
+            X[k].copy_(hostX[k], non_blocking=True)
+        for L in layers:
+            L.dY.copy_(hostdY[L.name], non_blocking=True)
+            api.forge_linear_bwd_step(X[ACT[L.name]], L.dY, L.W, "adamw", hp, s_no, L.seed,
+                                      L.m, L.v, dX=L.dX)
+        s_no += 1
+        api.forge_get_device_status()  # device -> host read of the step's status word
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
+    del hostX, hostdY
+
+    # ---- unfused two-pass schedule on the same layers: all dW alive before the optimizer
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    dW = {L.name: torch.empty((L.N, L.K), dtype=torch.float32, device=dev) for L in layers}
+    unf_peak = torch.cuda.max_memory_allocated(dev)
+
+    def unfused_step(s):
+        for L in layers:
+            api.forge_linear_dgrad(L.dY, L.W, L.dX)
+            api.forge_unfused_wgrad(X[ACT[L.name]], L.dY, dW[L.name])
+        for L in layers:
+            api.forge_unfused_opt_step(dW[L.name], L.W, "adamw", hp, s, L.seed, L.m, L.v)
+
+    for _ in range(2):
+        unfused_step(s_no)
+        s_no += 1
+    barrier()
+    u0 = torch.cuda.Event(enable_timing=True)
+    u1 = torch.cuda.Event(enable_timing=True)
+    u_steps = max(3, args.steps // 4)
+    u0.record(stream)
+    for _ in range(u_steps):
+        unfused_step(s_no)
+        s_no += 1
+    u1.record(stream)
+    torch.cuda.synchronize()
+    api.forge_get_device_status()
+    unf_ms = max_over_ranks(u0.elapsed_time(u1) / u_steps)
+    del dW
+    torch.cuda.synchronize()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    ck = clk.summary()
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "layers": ORDER, "optimizer": "adamw",
+                   "hparams": hp, "weights": "bf16, stochastic rounding",
+                   "states": "fp32 m, v", "flops_per_step": flops_step,
+                   "flops_counted": "2NKT (dW) + 2NKT (dX) per linear",
+                   "l2": "no flush: every X/dY >= 134 MB and the states (1.7 GB) exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "kernel": "fused wgrad+optimizer (tc_kernel, FORGE epilogue)",
+                     "achieved": round(fused_tflops, 2),
+                     "peak": peak_sust, "unit": "TFLOP/s",
+                     "frac": round(fused_tflops / peak_sust, 4),
+                     "peak_kind": f"bf16 sustained, {peak_src}",
+                     "frac_of_burst_peak": round(fused_tflops / peak_burst, 4),
+                     "traffic": None,
+                     "algorithmic_bytes_per_step": bytes_fused,
+                     "launches_timed": fused_launches,
+                     "per_layer_tflops": per_layer},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": 4, "ms_per_step": round(e2e_ms, 4)},
+        "unfused": {"ms_per_step": round(unf_ms, 4),
+                    "value": round(flops_step * world / (unf_ms * 1e-3) / 1e12, 2),
+                    "speedup_fused_vs_unfused": round(unf_ms / ms, 3),
+                    "dW_pool_bytes": params * 4,
+                    "peak_alloc_bytes_fused": base_alloc,
+                    "peak_alloc_bytes_unfused": unf_peak},
+        "hbm_bytes_per_param_algorithmic": round(bytes_fused / params, 3),
+        "gpu_launches": 2 * len(layers) * args.steps,
+        "clocks": ck,
+    }
+    if not args.no_cpu_baseline:
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        dt, f = oracle_sample()
+        out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                               "kind": "oracle",
+                               "sample": "one k_proj linear (1024x4096, T=16384): dX + dW + AdamW "
+                                         "with bf16 stochastic rounding, one step"}
+    print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+"""ctypes binding of libforge (include/forge.h), same names as the C ABI.
+
+This module only marshals arguments: it checks that torch tensors have the
+dtype, shape, device and contiguity the C ABI documents, passes their data
+pointers and the current CUDA stream, and turns a non-OK status into
+ForgeError.  Every step of the computation runs in the library's kernels.
+Loading fails loudly if the library has not been built.
+"""
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+c_int32, c_int64, c_uint64, c_float, c_void_p = (ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64,
+                                                 ctypes.c_float, ctypes.c_void_p)
+
+OPT_KINDS = {"adamw": 0, "nadam": 1, "radam": 2, "lion": 3, "rmsprop": 4, "adagrad": 5,
+             "sgd": 6, "sgd_momentum": 7}
+W_FP32, W_BF16_SR = 0, 1
+STATE_FP32, STATE_INT8_B64 = 0, 1
+USES_S1 = {"adamw", "nadam", "radam", "lion", "sgd_momentum"}
+USES_S2 = {"adamw", "nadam", "radam", "rmsprop", "adagrad"}
+
+STATUS = {0: "FORGE_OK", 1: "FORGE_ERR_INVALID_ARG", 2: "FORGE_ERR_UNSUPPORTED",
+          3: "FORGE_ERR_CUDA", 4: "FORGE_ERR_TIMEOUT", 5: "FORGE_ERR_DEVICE"}
+
+
+class ForgeLinear(ctypes.Structure):
+    _fields_ = [("T", c_int64), ("N", c_int64), ("K", c_int64),
+                ("X", c_void_p), ("dY", c_void_p), ("dX", c_void_p)]
+
+
+class ForgeState(ctypes.Structure):
+    _fields_ = [("W", c_void_p), ("w_dtype", c_int32), ("s_dtype", c_int32),
+                ("s1", c_void_p), ("s2", c_void_p), ("s1_scale", c_void_p), ("s2_scale", c_void_p)]
+
+
+class ForgeHparams(ctypes.Structure):
+    _fields_ = [(n, c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay", "alpha",
+                                       "momentum")]
+
+
+HPARAM_DEFAULTS = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, alpha=0.99,
+                       momentum=0.0)
+
+
+class ForgeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+_SIGNATURES = {
+    "forge_linear_bwd_step": (c_int32, [ctypes.POINTER(ForgeLinear), ctypes.POINTER(ForgeState),
+                                        c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
+                                        c_void_p]),
+    "forge_linear_dgrad": (c_int32, [ctypes.POINTER(ForgeLinear), c_void_p, c_int32, c_void_p]),
+    "forge_unfused_wgrad": (c_int32, [ctypes.POINTER(ForgeLinear), c_void_p, c_void_p]),
+    "forge_unfused_opt_step": (c_int32, [c_void_p, ctypes.POINTER(ForgeState), c_int64, c_int64,
+                                         c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
+                                         c_void_p]),
+    "forge_quantize_state": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32,
+                                       c_void_p]),
+    "forge_dequantize_state": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32,
+                                         c_void_p]),
+    "forge_get_device_status": (c_int32, [c_void_p]),
+    "forge_set_wait_limit_ns": (c_int32, [c_uint64]),
+    "forge_debug_skip_loads": (c_int32, [c_int32]),
+    "forge_status_string": (ctypes.c_char_p, [c_int32]),
+    "forge_last_error_message": (ctypes.c_char_p, []),
+    "forge_abi_version": (c_int32, []),
+}
+
+
+def library_path() -> str:
+    return os.environ.get("FORGE_LIBRARY", _build.lib_path("libforge.so"))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libforge.  Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = library_path()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libforge is not built ({path} missing); run "
+                                   "optimizer_tcgen05_dw_gb300.build.build() first")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+        return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = lib().forge_last_error_message().decode(errors="replace")
+        raise ForgeError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t, name, dtype, shape):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def hparams(**kw) -> ForgeHparams:
+    h = dict(HPARAM_DEFAULTS)
+    for k, v in kw.items():
+        if k not in h:
+            raise KeyError(f"unknown hyper-parameter {k}")
+        h[k] = v
+    return ForgeHparams(**{k: float(v) for k, v in h.items()})
+
+
+def make_state(W, s1=None, s2=None, s1_scale=None, s2_scale=None) -> ForgeState:
+    """A forge_state_t for W (fp32 or bf16) and optional fp32 / INT8 states."""
+    N, K = W.shape
+    if W.dtype == torch.float32:
+        wdt = W_FP32
+    elif W.dtype == torch.bfloat16:
+        wdt = W_BF16_SR
+    else:
+        raise TypeError(f"W must be float32 or bfloat16, got {W.dtype}")
+    _need(W, "W", W.dtype, (N, K))
+    int8 = any(t is not None and t.dtype in (torch.int8, torch.uint8) for t in (s1, s2))
+    if int8:
+        if s1 is not None:
+            _need(s1, "s1", torch.int8, (N, K))
+            _need(s1_scale, "s1_scale", torch.float32, (N, K // 64))
+        if s2 is not None:
+            _need(s2, "s2", torch.uint8, (N, K))
+            _need(s2_scale, "s2_scale", torch.float32, (N, K // 64))
+    else:
+        for t, nm in ((s1, "s1"), (s2, "s2")):
+            if t is not None:
+                _need(t, nm, torch.float32, (N, K))
+    return ForgeState(_ptr(W), wdt, STATE_INT8_B64 if int8 else STATE_FP32, _ptr(s1), _ptr(s2),
+                      _ptr(s1_scale), _ptr(s2_scale))
+
+
+def forge_linear_bwd_step(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1=None, s2=None,
+                          s1_scale=None, s2_scale=None, dX=None, stream=None):
+    """The fused FORGE step on one linear layer (updates W and states in place;
+    writes dX from the pre-update W when dX is given)."""
+    T, K = X.shape
+    N = W.shape[0]
+    _need(X, "X", torch.bfloat16, (T, K))
+    _need(dY, "dY", torch.bfloat16, (T, N))
+    if dX is not None:
+        _need(dX, "dX", torch.bfloat16, (T, K))
+    st = make_state(W, s1, s2, s1_scale, s2_scale)
+    lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), _ptr(dX))
+    _check(lib().forge_linear_bwd_step(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
+                                       ctypes.byref(hparams(**hp)), int(step),
+                                       int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def forge_linear_dgrad(dY, W, dX, stream=None):
+    T, N = dY.shape
+    K = W.shape[1]
+    _need(dY, "dY", torch.bfloat16, (T, N))
+    _need(dX, "dX", torch.bfloat16, (T, K))
+    _need(W, "W", W.dtype, (N, K))
+    wdt = W_FP32 if W.dtype == torch.float32 else W_BF16_SR
+    lin = ForgeLinear(T, N, K, None, _ptr(dY), _ptr(dX))
+    _check(lib().forge_linear_dgrad(ctypes.byref(lin), _ptr(W), wdt, _stream(stream)))
+
+
+def forge_unfused_wgrad(X, dY, dW, stream=None):
+    T, K = X.shape
+    N = dY.shape[1]
+    _need(X, "X", torch.bfloat16, (T, K))
+    _need(dY, "dY", torch.bfloat16, (T, N))
+    _need(dW, "dW", torch.float32, (N, K))
+    lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), None)
+    _check(lib().forge_unfused_wgrad(ctypes.byref(lin), _ptr(dW), _stream(stream)))
+
+
+def forge_unfused_opt_step(dW, W, opt: str, hp: dict, step: int, seed: int, s1=None, s2=None,
+                           s1_scale=None, s2_scale=None, stream=None):
+    N, K = W.shape
+    if dW is not None:
+        _need(dW, "dW", torch.float32, (N, K))
+    st = make_state(W, s1, s2, s1_scale, s2_scale)
+    _check(lib().forge_unfused_opt_step(_ptr(dW), ctypes.byref(st), N, K, OPT_KINDS[opt],
+                                        ctypes.byref(hparams(**hp)), int(step),
+                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def forge_quantize_state(x, codes, absmax, is_signed: bool, stream=None):
+    rows, cols = x.shape
+    _need(x, "x", torch.float32, (rows, cols))
+    _need(codes, "codes", torch.int8 if is_signed else torch.uint8, (rows, cols))
+    _need(absmax, "absmax", torch.float32, (rows, cols // 64))
+    _check(lib().forge_quantize_state(_ptr(x), _ptr(codes), _ptr(absmax), rows, cols,
+                                      1 if is_signed else 0, _stream(stream)))
+
+
+def forge_dequantize_state(codes, absmax, x, is_signed: bool, stream=None):
+    rows, cols = x.shape
+    _need(x, "x", torch.float32, (rows, cols))
+    _need(codes, "codes", torch.int8 if is_signed else torch.uint8, (rows, cols))
+    _need(absmax, "absmax", torch.float32, (rows, cols // 64))
+    _check(lib().forge_dequantize_state(_ptr(codes), _ptr(absmax), _ptr(x), rows, cols,
+                                        1 if is_signed else 0, _stream(stream)))
+
+
+def forge_get_device_status(stream=None):
+    """Synchronises the stream; raises ForgeError if a kernel reported an error."""
+    _check(lib().forge_get_device_status(_stream(stream)))
+
+
+def forge_set_wait_limit_ns(ns: int):
+    _check(lib().forge_set_wait_limit_ns(int(ns)))
+
+
+def forge_debug_skip_loads(enable: bool):
+    _check(lib().forge_debug_skip_loads(1 if enable else 0))
+
+
+def forge_abi_version() -> int:
+    return int(lib().forge_abi_version())

@@ -1,0 +1,516 @@
+// The C ABI of libforge (declared in include/forge.h): argument checks,
+// per-step optimizer scalars, TMA tensor maps, and kernel launches.
+//
+// Nothing here allocates device memory: every buffer is the caller's.  The
+// library's only device state is one status word per device (below).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/forge.h"
+#include "common.h"
+#include "launch.h"
+
+namespace forge {
+
+// Device-side status word: 0 = OK, otherwise the first error a kernel saw.
+__device__ uint32_t g_device_status;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+forge_status_t fail(forge_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+forge_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(FORGE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+std::atomic<int32_t> g_skip_loads{0};
+
+// ---------------------------------------------------------------- per device
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int num_sms = 0;
+  uint32_t* status = nullptr;
+  int cc_major = 0, cc_minor = 0;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {};
+
+forge_status_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FORGE_ERR_UNSUPPORTED, "device %d", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d;
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    void* sym = nullptr;
+    if ((e = cudaGetSymbolAddress(&sym, g_device_status)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    d.status = static_cast<uint32_t*>(sym);
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  *out = g_dev[dev];
+  return FORGE_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+forge_status_t encode_fn(EncodeFn* fn) {
+  static std::once_flag once;
+  static EncodeFn cached = nullptr;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) cached = reinterpret_cast<EncodeFn>(p);
+  });
+  if (cached == nullptr) {
+    return err != cudaSuccess ? cuda_fail(err, "cuTensorMapEncodeTiled lookup")
+                              : fail(FORGE_ERR_CUDA, "cuTensorMapEncodeTiled not available");
+  }
+  *fn = cached;
+  return FORGE_OK;
+}
+
+// A 2-D bf16 row-major tensor [outer x inner] and a box of box_outer rows of
+// box_inner (64) elements, 128-byte swizzled; out-of-range elements read 0.
+forge_status_t bf16_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer,
+                        uint32_t box_inner, uint32_t box_outer) {
+  EncodeFn fn;
+  forge_status_t st = encode_fn(&fn);
+  if (st != FORGE_OK) return st;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FORGE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld]", static_cast<int>(r),
+                static_cast<long long>(outer), static_cast<long long>(inner));
+  return FORGE_OK;
+}
+
+// ---------------------------------------------------------------- scalars
+
+// Per-step scalars of each rule, in double from the float hyper-parameters,
+// rounded once to float (the formulas of the published methods; see optim.cuh
+// for the per-element order).
+OptScalars make_scalars(int kind, const forge_hparams_t& hp, int64_t step) {
+  OptScalars s;
+  std::memset(&s, 0, sizeof(s));
+  s.kind = kind;
+  const double lr = hp.lr, b1 = hp.beta1, b2 = hp.beta2, eps = hp.eps, wd = hp.weight_decay;
+  const double t = static_cast<double>(step);
+  s.l2 = static_cast<float>(wd);
+  s.lr = static_cast<float>(lr);
+  s.eps = static_cast<float>(eps);
+  s.b1 = static_cast<float>(b1);
+  s.b2 = static_cast<float>(b2);
+  s.omb1 = static_cast<float>(1.0 - b1);
+  s.omb2 = static_cast<float>(1.0 - b2);
+  switch (kind) {
+    case kAdamW: {
+      const double c1 = 1.0 - std::pow(b1, t), c2 = 1.0 - std::pow(b2, t);
+      s.decay = static_cast<float>(1.0 - lr * wd);
+      s.step_size = static_cast<float>(lr / c1);
+      s.sqrt_c2 = static_cast<float>(std::sqrt(c2));
+      break;
+    }
+    case kNAdam: {
+      // mu_i = b1 (1 - 0.5 * 0.96^(0.004 i)); product of mu_1..mu_t
+      const double c2 = 1.0 - std::pow(b2, t);
+      auto mu = [&](int64_t i) { return b1 * (1.0 - 0.5 * std::pow(0.96, static_cast<double>(i) * 0.004)); };
+      double prod = 1.0;
+      for (int64_t i = 1; i <= step; ++i) prod *= mu(i);
+      const double mu_t = mu(step), mu_next = mu(step + 1);
+      const double prod_next = prod * mu_next;
+      s.c2 = static_cast<float>(c2);
+      s.coef_g = static_cast<float>(lr * (1.0 - mu_t) / (1.0 - prod));
+      s.coef_m = static_cast<float>(lr * mu_next / (1.0 - prod_next));
+      break;
+    }
+    case kRAdam: {
+      const double c1 = 1.0 - std::pow(b1, t), c2 = 1.0 - std::pow(b2, t);
+      const double rho_inf = 2.0 / (1.0 - b2) - 1.0;
+      const double rho_t = rho_inf - 2.0 * t * std::pow(b2, t) / c2;
+      s.sqrt_c2 = static_cast<float>(std::sqrt(c2));
+      if (rho_t > 5.0) {
+        const double r = std::sqrt((rho_t - 4.0) * (rho_t - 2.0) * rho_inf /
+                                   ((rho_inf - 4.0) * (rho_inf - 2.0) * rho_t));
+        s.rectified = 1;
+        s.step_size = static_cast<float>(lr * r / c1);
+      } else {
+        s.rectified = 0;
+        s.step_size = static_cast<float>(lr / c1);
+      }
+      break;
+    }
+    case kLion:
+      s.decay = static_cast<float>(1.0 - lr * wd);
+      break;
+    case kRMSprop:
+      s.alpha = hp.alpha;
+      s.oma = static_cast<float>(1.0 - static_cast<double>(hp.alpha));
+      break;
+    case kSGDMomentum:
+      s.mom = hp.momentum;
+      break;
+    default:
+      break;
+  }
+  return s;
+}
+
+// ---------------------------------------------------------------- checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+forge_status_t check_state(const forge_state_t* st, int kind, int64_t N, int64_t K) {
+  if (st == nullptr) return fail(FORGE_ERR_INVALID_ARG, "state is NULL");
+  if (st->w_dtype != FORGE_W_FP32 && st->w_dtype != FORGE_W_BF16_SR)
+    return fail(FORGE_ERR_INVALID_ARG, "w_dtype %d", st->w_dtype);
+  if (st->s_dtype != FORGE_STATE_FP32 && st->s_dtype != FORGE_STATE_INT8_B64)
+    return fail(FORGE_ERR_INVALID_ARG, "s_dtype %d", st->s_dtype);
+  if (N * K > 0 && (st->W == nullptr || !aligned16(st->W)))
+    return fail(FORGE_ERR_INVALID_ARG, "W must be a non-NULL 16-byte aligned device pointer");
+  const bool int8 = st->s_dtype == FORGE_STATE_INT8_B64;
+  if (int8 && K % 64 != 0) return fail(FORGE_ERR_INVALID_ARG, "INT8 states need K %% 64 == 0 (K=%lld)", (long long)K);
+  if (N * K == 0) return FORGE_OK;
+  if (uses_s1(kind)) {
+    if (st->s1 == nullptr || !aligned16(st->s1))
+      return fail(FORGE_ERR_INVALID_ARG, "rule %d needs s1 (16-byte aligned)", kind);
+    if (int8 && st->s1_scale == nullptr) return fail(FORGE_ERR_INVALID_ARG, "INT8 s1 needs s1_scale");
+  }
+  if (uses_s2(kind)) {
+    if (st->s2 == nullptr || !aligned16(st->s2))
+      return fail(FORGE_ERR_INVALID_ARG, "rule %d needs s2 (16-byte aligned)", kind);
+    if (int8 && st->s2_scale == nullptr) return fail(FORGE_ERR_INVALID_ARG, "INT8 s2 needs s2_scale");
+  }
+  return FORGE_OK;
+}
+
+forge_status_t check_linear(const forge_linear_t* lin, bool need_x) {
+  if (lin == nullptr) return fail(FORGE_ERR_INVALID_ARG, "lin is NULL");
+  if (lin->T < 0 || lin->N < 0 || lin->K < 0)
+    return fail(FORGE_ERR_INVALID_ARG, "negative shape T=%lld N=%lld K=%lld", (long long)lin->T,
+                (long long)lin->N, (long long)lin->K);
+  if (lin->N % 8 != 0 || lin->K % 8 != 0)
+    return fail(FORGE_ERR_INVALID_ARG, "N and K must be multiples of 8 (N=%lld K=%lld)",
+                (long long)lin->N, (long long)lin->K);
+  if (lin->T > (int64_t{1} << 31) - 1 || lin->N > (int64_t{1} << 31) - 1 || lin->K > (int64_t{1} << 31) - 1)
+    return fail(FORGE_ERR_UNSUPPORTED, "dimensions must fit in 31 bits");
+  if (lin->T > 0 && lin->N > 0) {
+    if (lin->dY == nullptr || !aligned16(lin->dY)) return fail(FORGE_ERR_INVALID_ARG, "dY must be 16-byte aligned");
+    if (need_x && lin->K > 0 && (lin->X == nullptr || !aligned16(lin->X)))
+      return fail(FORGE_ERR_INVALID_ARG, "X must be 16-byte aligned");
+  }
+  if (lin->dX != nullptr && !aligned16(lin->dX)) return fail(FORGE_ERR_INVALID_ARG, "dX must be 16-byte aligned");
+  return FORGE_OK;
+}
+
+forge_status_t check_hp(int32_t kind, const forge_hparams_t* hp, int64_t step) {
+  if (kind < FORGE_ADAMW || kind > FORGE_SGD_MOMENTUM) return fail(FORGE_ERR_INVALID_ARG, "opt_kind %d", kind);
+  if (hp == nullptr) return fail(FORGE_ERR_INVALID_ARG, "hparams is NULL");
+  if (step < 1) return fail(FORGE_ERR_INVALID_ARG, "step must be >= 1 (got %lld)", (long long)step);
+  return FORGE_OK;
+}
+
+void fill_tiles(GemmParams& p, int64_t M, int64_t Ncols, int64_t red) {
+  p.M = static_cast<int32_t>(M);
+  p.Ncols = static_cast<int32_t>(Ncols);
+  p.num_kb = static_cast<int32_t>((red + kBlockK - 1) / kBlockK);
+  p.tiles_m = static_cast<int32_t>((M + kTileM - 1) / kTileM);
+  p.tiles_n = static_cast<int32_t>((Ncols + kTileN - 1) / kTileN);
+  p.num_tiles = p.tiles_m * p.tiles_n;
+}
+
+int grid_for(const GemmParams& p, const DeviceInfo& d) {
+  return p.num_tiles < d.num_sms ? p.num_tiles : d.num_sms;
+}
+
+forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype, cudaStream_t s,
+                            const DeviceInfo& d) {
+  const int64_t T = lin->T, N = lin->N, K = lin->K;
+  if (T == 0 || K == 0) return FORGE_OK;
+  cudaError_t e;
+  if (N == 0) {  // empty reduction: dX = 0
+    if ((e = cudaMemsetAsync(lin->dX, 0, static_cast<size_t>(T * K * 2), s)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync(dX)");
+    return FORGE_OK;
+  }
+  if (w_dtype == FORGE_W_FP32) {
+    if ((e = launch_dgrad_fp32w(lin->dY, static_cast<const float*>(W), lin->dX, T, N, K, s)) != cudaSuccess)
+      return cuda_fail(e, "dX (fp32 weights) launch");
+    return FORGE_OK;
+  }
+  CUtensorMap ma, mb;
+  forge_status_t st;
+  if ((st = bf16_map(&ma, lin->dY, N, T, 64, kTileM)) != FORGE_OK) return st;
+  if ((st = bf16_map(&mb, W, K, N, 64, kBlockK)) != FORGE_OK) return st;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  fill_tiles(p, T, K, N);
+  p.out = lin->dX;
+  p.status = d.status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.skip_loads = g_skip_loads.load();
+  if ((e = launch_tc_plain(kModeDgrad, ma, mb, p, grid_for(p, d), s)) != cudaSuccess)
+    return cuda_fail(e, "dX launch");
+  return FORGE_OK;
+}
+
+forge_status_t check_device(const DeviceInfo& d) {
+  if (d.cc_major != 10 || d.cc_minor != 3)
+    return fail(FORGE_ERR_UNSUPPORTED, "libforge is built for sm_103a; device is sm_%d%d", d.cc_major, d.cc_minor);
+  return FORGE_OK;
+}
+
+}  // namespace
+}  // namespace forge
+
+using namespace forge;
+
+extern "C" {
+
+forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_state_t* state,
+                                     int32_t opt_kind, const forge_hparams_t* hp, int64_t step,
+                                     uint64_t seed, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if ((st = check_linear(lin, true)) != FORGE_OK) return st;
+  if ((st = check_hp(opt_kind, hp, step)) != FORGE_OK) return st;
+  if ((st = check_state(state, opt_kind, lin->N, lin->K)) != FORGE_OK) return st;
+  if (lin->N == 0 || lin->K == 0) return FORGE_OK;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  if ((st = check_device(d)) != FORGE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 1. dX from the pre-update weights, enqueued first on the same stream.
+  if (lin->dX != nullptr && (st = launch_dgrad(lin, state->W, state->w_dtype, s, d)) != FORGE_OK) return st;
+  const OptScalars sc = make_scalars(opt_kind, *hp, step);
+  cudaError_t e;
+  if (lin->T == 0) {
+    // No tokens: the gradient is exactly zero; apply the rule to it.
+    ElemParams ep;
+    std::memset(&ep, 0, sizeof(ep));
+    ep.W = state->W; ep.s1 = state->s1; ep.s2 = state->s2;
+    ep.s1_scale = state->s1_scale; ep.s2_scale = state->s2_scale;
+    ep.N = lin->N; ep.K = lin->K; ep.sc = sc; ep.seed = seed; ep.step = static_cast<uint64_t>(step);
+    if ((e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "optimizer launch (T = 0)");
+    return FORGE_OK;
+  }
+  // 2. the fused weight-gradient + optimizer pass.
+  CUtensorMap ma, mb;
+  if ((st = bf16_map(&ma, lin->dY, lin->N, lin->T, 64, kBlockK)) != FORGE_OK) return st;
+  if ((st = bf16_map(&mb, lin->X, lin->K, lin->T, 64, kBlockK)) != FORGE_OK) return st;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  fill_tiles(p, lin->N, lin->K, lin->T);
+  p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
+  p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
+  p.sc = sc;
+  p.seed = seed;
+  p.step = static_cast<uint64_t>(step);
+  p.status = d.status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.skip_loads = g_skip_loads.load();
+  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, p, grid_for(p, d), s)) != cudaSuccess)
+    return cuda_fail(e, "fused step launch");
+  return FORGE_OK;
+}
+
+forge_status_t forge_linear_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if ((st = check_linear(lin, false)) != FORGE_OK) return st;
+  if (w_dtype != FORGE_W_FP32 && w_dtype != FORGE_W_BF16_SR) return fail(FORGE_ERR_INVALID_ARG, "w_dtype %d", w_dtype);
+  if (lin->T == 0 || lin->K == 0) return FORGE_OK;
+  if (lin->dX == nullptr) return fail(FORGE_ERR_INVALID_ARG, "dX is NULL");
+  if (lin->N > 0 && (W == nullptr || !aligned16(W))) return fail(FORGE_ERR_INVALID_ARG, "W must be 16-byte aligned");
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  if ((st = check_device(d)) != FORGE_OK) return st;
+  return launch_dgrad(lin, W, w_dtype, static_cast<cudaStream_t>(stream), d);
+}
+
+forge_status_t forge_unfused_wgrad(const forge_linear_t* lin, float* dW, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if ((st = check_linear(lin, true)) != FORGE_OK) return st;
+  if (lin->N == 0 || lin->K == 0) return FORGE_OK;
+  if (dW == nullptr || !aligned16(dW)) return fail(FORGE_ERR_INVALID_ARG, "dW must be a 16-byte aligned device pointer");
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  if ((st = check_device(d)) != FORGE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (lin->T == 0) {
+    if ((e = cudaMemsetAsync(dW, 0, static_cast<size_t>(lin->N * lin->K * 4), s)) != cudaSuccess)
+      return cuda_fail(e, "cudaMemsetAsync(dW)");
+    return FORGE_OK;
+  }
+  CUtensorMap ma, mb;
+  if ((st = bf16_map(&ma, lin->dY, lin->N, lin->T, 64, kBlockK)) != FORGE_OK) return st;
+  if ((st = bf16_map(&mb, lin->X, lin->K, lin->T, 64, kBlockK)) != FORGE_OK) return st;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  fill_tiles(p, lin->N, lin->K, lin->T);
+  p.out = dW;
+  p.status = d.status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.skip_loads = g_skip_loads.load();
+  if ((e = launch_tc_plain(kModeWgradStore, ma, mb, p, grid_for(p, d), s)) != cudaSuccess)
+    return cuda_fail(e, "wgrad launch");
+  return FORGE_OK;
+}
+
+forge_status_t forge_unfused_opt_step(const float* dW, const forge_state_t* state, int64_t N, int64_t K,
+                                      int32_t opt_kind, const forge_hparams_t* hp, int64_t step,
+                                      uint64_t seed, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if (N < 0 || K < 0 || K % 8 != 0) return fail(FORGE_ERR_INVALID_ARG, "need N >= 0 and K %% 8 == 0");
+  if ((st = check_hp(opt_kind, hp, step)) != FORGE_OK) return st;
+  if ((st = check_state(state, opt_kind, N, K)) != FORGE_OK) return st;
+  if (N == 0 || K == 0) return FORGE_OK;
+  if (dW != nullptr && !aligned16(dW)) return fail(FORGE_ERR_INVALID_ARG, "dW must be 16-byte aligned");
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  ElemParams ep;
+  std::memset(&ep, 0, sizeof(ep));
+  ep.dW = dW;
+  ep.W = state->W; ep.s1 = state->s1; ep.s2 = state->s2;
+  ep.s1_scale = state->s1_scale; ep.s2_scale = state->s2_scale;
+  ep.N = N; ep.K = K;
+  ep.sc = make_scalars(opt_kind, *hp, step);
+  ep.seed = seed;
+  ep.step = static_cast<uint64_t>(step);
+  cudaError_t e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "optimizer launch");
+  return FORGE_OK;
+}
+
+static forge_status_t quant_common(const void* a, const void* b, const float* absmax, int64_t rows,
+                                   int64_t cols) {
+  if (rows < 0 || cols < 0 || cols % 64 != 0) return fail(FORGE_ERR_INVALID_ARG, "need cols %% 64 == 0");
+  if (rows * cols == 0) return FORGE_OK;
+  if (a == nullptr || b == nullptr || absmax == nullptr || !aligned16(a) || !aligned16(b))
+    return fail(FORGE_ERR_INVALID_ARG, "NULL or misaligned pointer");
+  return FORGE_OK;
+}
+
+forge_status_t forge_quantize_state(const float* x, void* codes, float* absmax, int64_t rows, int64_t cols,
+                                    int32_t is_signed, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if ((st = quant_common(x, codes, absmax, rows, cols)) != FORGE_OK) return st;
+  if (rows * cols == 0) return FORGE_OK;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  ElemParams ep;
+  std::memset(&ep, 0, sizeof(ep));
+  ep.dW = x; ep.s1 = codes; ep.s1_scale = absmax; ep.N = rows; ep.K = cols; ep.is_signed = is_signed ? 1 : 0;
+  cudaError_t e = launch_quantize(ep, d.num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
+  return FORGE_OK;
+}
+
+forge_status_t forge_dequantize_state(const void* codes, const float* absmax, float* x, int64_t rows,
+                                      int64_t cols, int32_t is_signed, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if ((st = quant_common(x, codes, absmax, rows, cols)) != FORGE_OK) return st;
+  if (rows * cols == 0) return FORGE_OK;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  ElemParams ep;
+  std::memset(&ep, 0, sizeof(ep));
+  ep.W = x; ep.s1 = const_cast<void*>(codes); ep.s1_scale = const_cast<float*>(absmax);
+  ep.N = rows; ep.K = cols; ep.is_signed = is_signed ? 1 : 0;
+  cudaError_t e = launch_dequantize(ep, d.num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
+  return FORGE_OK;
+}
+
+forge_status_t forge_get_device_status(void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t word = 0;
+  if ((e = cudaMemcpy(&word, d.status, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return cuda_fail(e, "read status word");
+  if (word != 0) {
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpy(d.status, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "clear status word");
+    if (word == kStatusTimeout) return fail(FORGE_ERR_TIMEOUT, "a pipeline wait in a kernel expired");
+    return fail(FORGE_ERR_DEVICE, "device status %u", word);
+  }
+  return FORGE_OK;
+}
+
+forge_status_t forge_set_wait_limit_ns(uint64_t ns) {
+  g_wait_limit_ns.store(ns == 0 ? 2000000000ull : ns);
+  return FORGE_OK;
+}
+
+forge_status_t forge_debug_skip_loads(int32_t enable) {
+  g_skip_loads.store(enable ? 1 : 0);
+  return FORGE_OK;
+}
+
+const char* forge_status_string(forge_status_t status) {
+  switch (status) {
+    case FORGE_OK: return "FORGE_OK";
+    case FORGE_ERR_INVALID_ARG: return "FORGE_ERR_INVALID_ARG: invalid argument";
+    case FORGE_ERR_UNSUPPORTED: return "FORGE_ERR_UNSUPPORTED: unsupported request";
+    case FORGE_ERR_CUDA: return "FORGE_ERR_CUDA: CUDA runtime error";
+    case FORGE_ERR_TIMEOUT: return "FORGE_ERR_TIMEOUT: device-side wait expired";
+    case FORGE_ERR_DEVICE: return "FORGE_ERR_DEVICE: device-side error";
+  }
+  return "unknown forge_status_t";
+}
+
+const char* forge_last_error_message(void) { return g_msg; }
+
+int32_t forge_abi_version(void) { return FORGE_ABI_VERSION; }
+
+}  // extern "C"

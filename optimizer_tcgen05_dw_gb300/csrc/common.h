@@ -1,0 +1,85 @@
+// Definitions shared by the host API and the kernels of libforge.
+#pragma once
+
+#include <cstdint>
+
+namespace forge {
+
+// Rule identifiers (values match forge_opt_kind_t).
+enum OptKind : int32_t {
+  kAdamW = 0, kNAdam = 1, kRAdam = 2, kLion = 3,
+  kRMSprop = 4, kAdaGrad = 5, kSGD = 6, kSGDMomentum = 7
+};
+enum WDtype : int32_t { kWFp32 = 0, kWBf16 = 1 };
+enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1 };
+
+// Device-side status codes (values match forge_status_t).
+enum DeviceStatus : uint32_t { kStatusOk = 0, kStatusTimeout = 4 };
+
+// Per-step scalars of a rule, formed on the host in double from the float
+// hyper-parameters and the step number and rounded once to float.  Field use
+// per rule (everything else is zero):
+//   AdamW   decay b1 omb1 b2 omb2 step_size sqrt_c2 eps
+//   NAdam   l2 b1 omb1 b2 omb2 c2 eps coef_g coef_m
+//   RAdam   l2 b1 omb1 b2 omb2 eps; rectified ? (step_size, sqrt_c2) : step_size
+//   Lion    decay lr b1 omb1 b2 omb2
+//   RMSprop l2 alpha oma lr eps
+//   AdaGrad l2 lr eps
+//   SGD     l2 lr
+//   SGD-m   l2 lr mom
+struct OptScalars {
+  int32_t kind;
+  int32_t rectified;
+  float l2, decay, lr, b1, omb1, b2, omb2, eps;
+  float step_size, sqrt_c2, c2, coef_g, coef_m, alpha, oma, mom;
+};
+
+// Which state buffers a rule keeps.
+inline constexpr bool uses_s1(int k) {
+  return k == kAdamW || k == kNAdam || k == kRAdam || k == kLion || k == kSGDMomentum;
+}
+inline constexpr bool uses_s2(int k) {
+  return k == kAdamW || k == kNAdam || k == kRAdam || k == kRMSprop || k == kAdaGrad;
+}
+
+// Tensor-core GEMM geometry: a 128 x 256 output tile (two 128 x 128 optimizer
+// tiles side by side), 64-deep reduction blocks, a 4-stage shared-memory ring.
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kBlockK = 64;
+constexpr int kStages = 4;
+constexpr int kABytes = kTileM * kBlockK * 2;            // 16 KiB
+constexpr int kBBytes = kTileN * kBlockK * 2;            // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;           // 48 KiB
+constexpr int kNumEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kNumEpiWarps);        // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kTmemCols = 2 * kTileN;                    // double-buffered fp32 accumulator
+constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
+
+enum GemmMode : int32_t {
+  kModeFusedOpt = 0,   // dW tile -> optimizer epilogue (the FORGE step)
+  kModeWgradStore = 1, // dW tile -> fp32 store (unfused pass 1)
+  kModeDgrad = 2       // dX tile -> bf16 store
+};
+
+// Parameters of one tensor-core launch.  Output tile space is M x Ncols
+// (wgrad: M = N_out rows of W, Ncols = K; dgrad: M = T, Ncols = K).
+struct GemmParams {
+  int32_t M, Ncols;
+  int32_t num_kb;            // reduction blocks of 64
+  int32_t tiles_m, tiles_n, num_tiles;
+  void* out;                 // wgrad store: fp32 [M x Ncols]; dgrad: bf16 [M x Ncols]
+  void* W;                   // fused: [M x Ncols] fp32 or bf16
+  void* s1;
+  void* s2;
+  float* s1_scale;
+  float* s2_scale;
+  OptScalars sc;
+  uint64_t seed;
+  uint64_t step;
+  uint64_t wait_limit_ns;
+  uint32_t* status;          // device status word (first error wins)
+  int32_t skip_loads;
+};
+
+}  // namespace forge

@@ -1,0 +1,280 @@
+// Elementwise kernels: the standalone optimizer step of the unfused schedule,
+// the INT8 state quantiser/dequantiser, and dX for fp32 master weights.
+//
+// The optimizer step runs exactly the per-element arithmetic of the fused
+// epilogue (optim.cuh) on a gradient read from global memory -- the
+// "separate optimizer kernel launch" the FORGE explainer's Technical Summary
+// §4 ("Throughput") names as the cost the fused step removes.
+//
+// Layout of work: each thread owns 8 consecutive elements of a row (one
+// Philox call, 16/32-byte vector accesses; consecutive threads own
+// consecutive groups, so a warp touches 256 contiguous elements).  For INT8
+// states the 8 threads of a block of 64 share the block's absmax through
+// warp shuffles.
+#include <cuda_bf16.h>
+
+#include "launch.h"
+#include "optim.cuh"
+
+namespace forge {
+
+namespace {
+
+constexpr int kElemThreads = 256;
+
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Max over the 8 lanes of an aligned lane group (all 32 lanes call it).
+__device__ __forceinline__ float group8_max(float a) {
+  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+  return a;
+}
+
+template <bool SIGNED>
+__device__ __forceinline__ void load_codes8(const void* base, int64_t e0, float a, float (&v)[8]) {
+  const uint2 c = *reinterpret_cast<const uint2*>(static_cast<const uint8_t*>(base) + e0);
+  const uint32_t w[2] = {c.x, c.y};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t b = (w[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+    const int code = SIGNED ? static_cast<int>(static_cast<int8_t>(b)) : static_cast<int>(b);
+    v[j] = dev::dequant<SIGNED>(code, a);
+  }
+}
+
+template <bool SIGNED>
+__device__ __forceinline__ void store_codes8(void* base, int64_t e0, float a, const float (&v)[8]) {
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    w[j >> 2] |= (static_cast<uint32_t>(dev::quant<SIGNED>(v[j], a)) & 0xFFu) << (8 * (j & 3));
+  *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + e0) = make_uint2(w[0], w[1]);
+}
+
+template <int KIND, int WDT, int SDT>
+__device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemParams& p) {
+  const int64_t e0 = gid * 8;
+  float g[8], w[8], s1[8], s2[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { g[j] = 0.f; w[j] = 0.f; s1[j] = 0.f; s2[j] = 0.f; }
+  const int64_t sidx = e0 / 64;  // block index (rows hold K/64 whole blocks)
+  if (active) {
+    if (p.dW != nullptr) load8(p.dW + e0, g);
+    if (WDT == kWBf16) {
+      const uint4 wb = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0);
+      const uint32_t wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        w[2 * j] = dev::bf16_to_f32(wv[j] & 0xFFFFu);
+        w[2 * j + 1] = dev::bf16_to_f32(wv[j] >> 16);
+      }
+    } else {
+      load8(static_cast<const float*>(p.W) + e0, w);
+    }
+    if (SDT == kSInt8) {
+      if (uses_s1(KIND)) load_codes8<true>(p.s1, e0, p.s1_scale[sidx], s1);
+      if (uses_s2(KIND)) load_codes8<false>(p.s2, e0, p.s2_scale[sidx], s2);
+    } else {
+      if (uses_s1(KIND)) load8(static_cast<const float*>(p.s1) + e0, s1);
+      if (uses_s2(KIND)) load8(static_cast<const float*>(p.s2) + e0, s2);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+    if (WDT == kWBf16) {
+      const uint4 r = dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step);
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(r, 2 * j)) |
+               (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(r, 2 * j + 1)) << 16);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.W) + e0) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+      store8(static_cast<float*>(p.W) + e0, w);
+    }
+    if (SDT == kSFp32) {
+      if (uses_s1(KIND)) store8(static_cast<float*>(p.s1) + e0, s1);
+      if (uses_s2(KIND)) store8(static_cast<float*>(p.s2) + e0, s2);
+    }
+  }
+  if (SDT == kSInt8) {
+    // new block absmax over the 8 threads of this block (inactive threads
+    // belong to inactive blocks and contribute nothing)
+    float n1 = 0.f, n2 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      n1 = dev::absmax_acc(n1, s1[j]);
+      n2 = dev::absmax_acc(n2, s2[j]);
+    }
+    if (uses_s1(KIND)) n1 = group8_max(n1);
+    if (uses_s2(KIND)) n2 = group8_max(n2);
+    if (active) {
+      const bool leader = (gid & 7) == 0;
+      if (uses_s1(KIND)) {
+        store_codes8<true>(p.s1, e0, n1, s1);
+        if (leader) p.s1_scale[sidx] = n1;
+      }
+      if (uses_s2(KIND)) {
+        store_codes8<false>(p.s2, e0, n2, s2);
+        if (leader) p.s2_scale[sidx] = n2;
+      }
+    }
+  }
+}
+
+template <int WDT, int SDT>
+__global__ void __launch_bounds__(kElemThreads) opt_step_kernel(const ElemParams p) {
+  const int64_t groups = p.N * p.K / 8;
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x - lane;
+       base < groups; base += stride) {
+    const int64_t gid = base + lane;
+    const bool active = gid < groups;
+    switch (p.sc.kind) {
+      case kAdamW: opt_group<kAdamW, WDT, SDT>(gid, active, p); break;
+      case kNAdam: opt_group<kNAdam, WDT, SDT>(gid, active, p); break;
+      case kRAdam: opt_group<kRAdam, WDT, SDT>(gid, active, p); break;
+      case kLion: opt_group<kLion, WDT, SDT>(gid, active, p); break;
+      case kRMSprop: opt_group<kRMSprop, WDT, SDT>(gid, active, p); break;
+      case kAdaGrad: opt_group<kAdaGrad, WDT, SDT>(gid, active, p); break;
+      case kSGD: opt_group<kSGD, WDT, SDT>(gid, active, p); break;
+      default: opt_group<kSGDMomentum, WDT, SDT>(gid, active, p); break;
+    }
+  }
+}
+
+template <bool SIGNED>
+__global__ void __launch_bounds__(kElemThreads) quantize_kernel(const ElemParams p) {
+  const int64_t groups = p.N * p.K / 8;
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x - lane;
+       base < groups; base += stride) {
+    const int64_t gid = base + lane;
+    const bool active = gid < groups;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    if (active) load8(p.dW + gid * 8, v);
+    float a = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a = dev::absmax_acc(a, v[j]);
+    a = group8_max(a);
+    if (active) {
+      store_codes8<SIGNED>(p.s1, gid * 8, a, v);
+      if ((gid & 7) == 0) p.s1_scale[gid / 8] = a;
+    }
+  }
+}
+
+template <bool SIGNED>
+__global__ void __launch_bounds__(kElemThreads) dequantize_kernel(const ElemParams p) {
+  const int64_t groups = p.N * p.K / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gid < groups;
+       gid += stride) {
+    float v[8];
+    load_codes8<SIGNED>(p.s1, gid * 8, p.s1_scale[gid / 8], v);
+    store8(static_cast<float*>(p.W) + gid * 8, v);
+  }
+}
+
+// dX[t, k] = sum_n dY[t, n] * bf16(W[n, k]) with fp32 accumulation; a 64 x 64
+// output tile per block, 4 x 4 per thread, 32-deep shared-memory slices.
+__global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* __restrict__ dY,
+                                                          const float* __restrict__ W,
+                                                          __nv_bfloat16* __restrict__ dX,
+                                                          int64_t T, int64_t N, int64_t K) {
+  __shared__ float sA[32][64 + 1];  // [n][t]
+  __shared__ float sB[32][64 + 1];  // [n][k]
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * 64, k0 = static_cast<int64_t>(blockIdx.x) * 64;
+  float acc[4][4] = {};
+  for (int64_t n0 = 0; n0 < N; n0 += 32) {
+    for (int i = threadIdx.x; i < 32 * 64; i += 256) {
+      const int nn = i & 31, tt = i >> 5;
+      const int64_t t = t0 + tt, n = n0 + nn;
+      sA[nn][tt] = (t < T && n < N) ? __bfloat162float(dY[t * N + n]) : 0.f;
+      const int kk = i & 63, nr = i >> 6;
+      const int64_t k = k0 + kk, n2 = n0 + nr;
+      sB[nr][kk] = (k < K && n2 < N) ? __bfloat162float(__float2bfloat16_rn(W[n2 * K + k])) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int nn = 0; nn < 32; ++nn) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = sA[nn][ty * 4 + i]; b[i] = sB[nn][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t k = k0 + tx * 4 + j;
+      if (k < K) dX[t * K + k] = __float2bfloat16_rn(acc[i][j]);
+    }
+  }
+}
+
+int elem_grid(int64_t groups, int num_sms) {
+  const int64_t want = (groups + kElemThreads - 1) / kElemThreads;
+  const int64_t cap = static_cast<int64_t>(num_sms) * 8;
+  return static_cast<int>(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+}  // namespace
+
+cudaError_t launch_opt_step(int wdt, int sdt, const ElemParams& p, int num_sms, cudaStream_t s) {
+  const int grid = elem_grid(p.N * p.K / 8, num_sms);
+  if (wdt == kWBf16) {
+    if (sdt == kSInt8) opt_step_kernel<kWBf16, kSInt8><<<grid, kElemThreads, 0, s>>>(p);
+    else opt_step_kernel<kWBf16, kSFp32><<<grid, kElemThreads, 0, s>>>(p);
+  } else {
+    if (sdt == kSInt8) opt_step_kernel<kWFp32, kSInt8><<<grid, kElemThreads, 0, s>>>(p);
+    else opt_step_kernel<kWFp32, kSFp32><<<grid, kElemThreads, 0, s>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(const ElemParams& p, int num_sms, cudaStream_t s) {
+  const int grid = elem_grid(p.N * p.K / 8, num_sms);
+  if (p.is_signed) quantize_kernel<true><<<grid, kElemThreads, 0, s>>>(p);
+  else quantize_kernel<false><<<grid, kElemThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const ElemParams& p, int num_sms, cudaStream_t s) {
+  const int grid = elem_grid(p.N * p.K / 8, num_sms);
+  if (p.is_signed) dequantize_kernel<true><<<grid, kElemThreads, 0, s>>>(p);
+  else dequantize_kernel<false><<<grid, kElemThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dgrad_fp32w(const void* dY, const float* W, void* dX, int64_t T, int64_t N,
+                               int64_t K, cudaStream_t s) {
+  const dim3 grid(static_cast<unsigned>((K + 63) / 64), static_cast<unsigned>((T + 63) / 64));
+  dgrad_fp32w_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dY), W,
+                                          static_cast<__nv_bfloat16*>(dX), T, N, K);
+  return cudaGetLastError();
+}
+
+}  // namespace forge

@@ -1,0 +1,40 @@
+// Host-side launchers of the kernels, one per translation unit, called by the
+// C ABI in api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace forge {
+
+// Parameters of the elementwise (non-tensor-core) kernels.
+struct ElemParams {
+  const float* dW;   // optimizer step: fp32 gradient (nullptr = zero); quantise: input
+  void* W;
+  void* s1;
+  void* s2;
+  float* s1_scale;
+  float* s2_scale;
+  int64_t N, K;      // rows, columns
+  OptScalars sc;
+  uint64_t seed, step;
+  int32_t is_signed; // quantise / dequantise
+};
+
+// tc_fused.cu: the FORGE step (mode kModeFusedOpt) for one (W dtype, state dtype).
+cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t s);
+// tc_plain.cu: unfused pass 1 (kModeWgradStore) or dX (kModeDgrad).
+cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t s);
+// elementwise.cu
+cudaError_t launch_opt_step(int wdt, int sdt, const ElemParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_quantize(const ElemParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_dequantize(const ElemParams& p, int num_sms, cudaStream_t s);
+// dX = dY * bf16(W) for fp32 master weights (CUDA cores).
+cudaError_t launch_dgrad_fp32w(const void* dY, const float* W, void* dX, int64_t T, int64_t N,
+                               int64_t K, cudaStream_t s);
+
+}  // namespace forge

@@ -1,0 +1,27 @@
+// Instantiations of the tensor-core kernel for the fused FORGE step.
+#include "launch.h"
+#include "tc_kernel.cuh"
+
+namespace forge {
+
+template <int WDT, int SDT>
+static cudaError_t run_fused(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
+                             int grid, cudaStream_t s) {
+  auto* k = tc_kernel<kModeFusedOpt, WDT, SDT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, kSmemBytes, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
+                            const GemmParams& p, int grid, cudaStream_t s) {
+  if (wdt == kWBf16) {
+    return sdt == kSInt8 ? run_fused<kWBf16, kSInt8>(a, b, p, grid, s)
+                         : run_fused<kWBf16, kSFp32>(a, b, p, grid, s);
+  }
+  return sdt == kSInt8 ? run_fused<kWFp32, kSInt8>(a, b, p, grid, s)
+                       : run_fused<kWFp32, kSFp32>(a, b, p, grid, s);
+}
+
+}  // namespace forge

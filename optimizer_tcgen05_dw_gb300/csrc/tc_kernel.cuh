@@ -1,0 +1,535 @@
+// The tensor-core kernel behind the fused step, the unfused wgrad pass and dX.
+//
+// FORGE (gist.science explainer), Technical Summary §2 "Core Mechanism": for
+// each tile of W the partial products of dY and X are accumulated in FP32,
+// the optimizer is applied to the finished tile at once, the gradient tile is
+// discarded, and only the updated weights and moments are written back.
+//
+// GB300 design (one CTA per SM, persistent over output tiles):
+//   warp 0      one lane issues TMA tile loads of the two operands into a
+//               kStages-deep shared-memory ring (128-byte swizzle), each stage
+//               guarded by a "full" (bytes landed) and "empty" (MMAs done)
+//               mbarrier;
+//   warp 1      allocates 512 tensor-memory columns; one lane issues
+//               tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of two
+//               TMEM accumulators, so the MMAs of tile i+1 overlap the
+//               epilogue of tile i;
+//   warps 2..9  the epilogue: tcgen05.ld pulls the finished fp32 tile into
+//               registers (one TMEM lane = one output row per thread, two
+//               warps per 32-lane quarter splitting the 256 columns), then
+//               either runs the optimizer on it (FORGE), stores it as fp32
+//               (unfused pass 1) or as bf16 (dX).
+// Operand layouts (all 128-byte swizzled atoms of 8 rows x 128 bytes):
+//   wgrad  A = dY^T tile [128 n x 64 t]: dY is [T x N] with n contiguous, so A
+//          is MN-major: two 64-wide column atoms 8 KiB apart (LBO), 8-row
+//          token groups 1 KiB apart (SBO).  B = X tile [256 k x 64 t], MN-major,
+//          four 64-wide atoms.
+//   dgrad  A = dY tile [128 t x 64 n], K-major (n contiguous); B = W tile
+//          [256 k x 64 n], MN-major.
+// Every wait is bounded (GemmParams::wait_limit_ns): on expiry the CTA records
+// a timeout in the status word, all roles stop, in-flight copies and MMAs are
+// drained (again bounded), tensor memory is released and the CTA returns.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "optim.cuh"
+#include "ptx.cuh"
+
+namespace forge {
+
+struct SharedState {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t tmem_full[2];
+  uint64_t tmem_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int32_t abort;
+};
+
+// Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
+// or the wait expired (the first expiry records the timeout).
+__device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, const GemmParams& p,
+                                             SharedState* ss, bool honour_abort = true) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (honour_abort && *reinterpret_cast<volatile int32_t*>(&ss->abort)) return false;
+    if (ptx::global_timer_ns() - t0 > p.wait_limit_ns) {
+      *reinterpret_cast<volatile int32_t*>(&ss->abort) = 1;
+      atomicCAS(p.status, 0u, static_cast<uint32_t>(kStatusTimeout));
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& tm, int& tn) {
+  tm = tile / p.tiles_n;
+  tn = tile - tm * p.tiles_n;
+}
+
+// ------------------------------------------------------------------ roles
+
+template <int MODE>
+__device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, const GemmParams& p,
+                              uint8_t* smA, uint8_t* smB, SharedState* ss) {
+  uint32_t it = 0;
+  uint32_t issued_mask = 0;
+  uint32_t last_parity = 0;  // bit s: parity of the last phase armed on full[s]
+  if (!p.skip_loads) {
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int tm, tn;
+      tile_coords(tile, p, tm, tn);
+      const int m0 = tm * kTileM, n0 = tn * kTileN;
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = (it / kStages) & 1u;
+        if (!bounded_wait(&ss->empty[s], ph ^ 1u, p, ss)) goto drain;
+        ptx::mbar_arrive_expect_tx(&ss->full[s], kStageBytes);
+        uint8_t* a = smA + s * kABytes;
+        uint8_t* b = smB + s * kBBytes;
+        if (MODE == kModeDgrad) {
+          ptx::tma_load_2d(mA, &ss->full[s], a, kb * kBlockK, m0);
+        } else {
+          ptx::tma_load_2d(mA, &ss->full[s], a, m0, kb * kBlockK);
+          ptx::tma_load_2d(mA, &ss->full[s], a + 8192, m0 + 64, kb * kBlockK);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          ptx::tma_load_2d(mB, &ss->full[s], b + j * 8192, n0 + 64 * j, kb * kBlockK);
+        issued_mask |= 1u << s;
+        last_parity = (last_parity & ~(1u << s)) | (ph << s);
+      }
+    }
+  }
+drain:
+  // Every issued copy lands before the CTA can exit (already true unless a
+  // consumer gave up early).
+  for (int s = 0; s < kStages; ++s)
+    if (issued_mask & (1u << s)) bounded_wait(&ss->full[s], (last_parity >> s) & 1u, p, ss, false);
+}
+
+template <int MODE>
+__device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, SharedState* ss) {
+  constexpr uint32_t kIdesc =
+      ptx::idesc_bf16_f32(kTileM, kTileN, /*a_mn=*/MODE != kModeDgrad, /*b_mn=*/true);
+  uint32_t it = 0;
+  int local = 0;
+  for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+    const int acc = local & 1;
+    const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+    if (!bounded_wait(&ss->tmem_empty[acc], aph ^ 1u, p, ss)) goto done;
+    ptx::tc_fence_after();
+    {
+      const uint32_t d_tmem = ss->tmem_base + static_cast<uint32_t>(acc * kTileN);
+      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+        const int s = static_cast<int>(it % kStages);
+        const uint32_t ph = (it / kStages) & 1u;
+        if (!bounded_wait(&ss->full[s], ph, p, ss)) goto done;
+        ptx::tc_fence_after();
+        const uint32_t a0 = ptx::smem_addr(smA + s * kABytes);
+        const uint32_t b0 = ptx::smem_addr(smB + s * kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBlockK / 16; ++kk) {
+          // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB.
+          // K-major: 16 bf16 = 32 B inside the 128-byte swizzle row.
+          const uint64_t adesc = (MODE == kModeDgrad)
+                                     ? ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024)
+                                     : ptx::smem_desc_sw128(a0 + kk * 2048, 8192, 1024);
+          const uint64_t bdesc = ptx::smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+          ptx::mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(&ss->empty[s]);  // frees the stage once these MMAs finish
+      }
+      ptx::mma_commit(&ss->tmem_full[acc]);  // accumulator complete
+    }
+  }
+done:
+  // Tensor memory may be released only after every issued MMA has finished.
+  ptx::mma_commit(&ss->mma_done);
+  bounded_wait(&ss->mma_done, 0u, p, ss, false);
+}
+
+// ------------------------------------------------------------------ epilogues
+
+// 8 consecutive elements e0..e0+7 of one row of W (e0 % 8 == 0), fp32 or no
+// state: load, apply the rule, round, store.
+template <int KIND, int WDT>
+__device__ __forceinline__ void group8_fp32state(const float* g, int64_t e0, const GemmParams& p) {
+  float w[8], s1[8], s2[8];
+  if (WDT == kWBf16) {
+    const uint4 wb = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0);
+    const uint32_t wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w[2 * j] = dev::bf16_to_f32(wv[j] & 0xFFFFu);
+      w[2 * j + 1] = dev::bf16_to_f32(wv[j] >> 16);
+    }
+  } else {
+    const float4* wp = reinterpret_cast<const float4*>(static_cast<const float*>(p.W) + e0);
+    const float4 a = wp[0], b = wp[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+  if (uses_s1(KIND)) {
+    const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(p.s1) + e0);
+    const float4 a = sp[0], b = sp[1];
+    s1[0] = a.x; s1[1] = a.y; s1[2] = a.z; s1[3] = a.w;
+    s1[4] = b.x; s1[5] = b.y; s1[6] = b.z; s1[7] = b.w;
+  }
+  if (uses_s2(KIND)) {
+    const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(p.s2) + e0);
+    const float4 a = sp[0], b = sp[1];
+    s2[0] = a.x; s2[1] = a.y; s2[2] = a.z; s2[3] = a.w;
+    s2[4] = b.x; s2[5] = b.y; s2[6] = b.z; s2[7] = b.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+  if (WDT == kWBf16) {
+    const uint4 r = dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step);
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(r, 2 * j)) |
+             (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(r, 2 * j + 1)) << 16);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.W) + e0) = make_uint4(o[0], o[1], o[2], o[3]);
+  } else {
+    float4* wp = reinterpret_cast<float4*>(static_cast<float*>(p.W) + e0);
+    wp[0] = make_float4(w[0], w[1], w[2], w[3]);
+    wp[1] = make_float4(w[4], w[5], w[6], w[7]);
+  }
+  if (uses_s1(KIND)) {
+    float4* sp = reinterpret_cast<float4*>(static_cast<float*>(p.s1) + e0);
+    sp[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
+    sp[1] = make_float4(s1[4], s1[5], s1[6], s1[7]);
+  }
+  if (uses_s2(KIND)) {
+    float4* sp = reinterpret_cast<float4*>(static_cast<float*>(p.s2) + e0);
+    sp[0] = make_float4(s2[0], s2[1], s2[2], s2[3]);
+    sp[1] = make_float4(s2[4], s2[5], s2[6], s2[7]);
+  }
+}
+
+template <int KIND, int WDT>
+__device__ __forceinline__ void epi_fused_fp32state(uint32_t tbase, int64_t row, int colbase,
+                                                    bool row_ok, const GemmParams& p) {
+  const int64_t K = p.Ncols;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float g[32];
+    ptx::tmem_ld_32x32b_x32(tbase + c * 32, g);
+    if (!row_ok) continue;
+    const int col0 = colbase + c * 32;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (col0 + q * 8 < K) group8_fp32state<KIND, WDT>(g + q * 8, row * K + col0 + q * 8, p);
+    }
+  }
+}
+
+// Byte j of a 64-byte code block held in 16 words.
+__device__ __forceinline__ int code_at(const uint32_t (&c)[16], int j, bool is_signed) {
+  const uint32_t b = (c[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+  return is_signed ? static_cast<int>(static_cast<int8_t>(b)) : static_cast<int>(b);
+}
+
+// One INT8 block of 64 elements of one row (the thread owns the whole block):
+// pass 1 finds the new absmax of each state, pass 2 recomputes the same
+// element results, writes W, and quantises the states with the new absmax.
+template <int KIND, int WDT>
+__device__ __forceinline__ void epi_fused_int8_block(uint32_t tblock, int64_t row, int col0,
+                                                     bool ok, const GemmParams& p) {
+  const int64_t K = p.Ncols;
+  const int64_t e_blk = row * K + col0;
+  const int64_t sidx = row * (K / 64) + col0 / 64;
+  uint32_t c1[16], c2[16];
+  float a1 = 0.f, a2 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) { c1[i] = 0u; c2[i] = 0u; }
+  if (ok) {
+    if (uses_s1(KIND)) {
+      const uint4* q = reinterpret_cast<const uint4*>(static_cast<const int8_t*>(p.s1) + e_blk);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = q[i];
+        c1[4 * i] = v.x; c1[4 * i + 1] = v.y; c1[4 * i + 2] = v.z; c1[4 * i + 3] = v.w;
+      }
+      a1 = p.s1_scale[sidx];
+    }
+    if (uses_s2(KIND)) {
+      const uint4* q = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.s2) + e_blk);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 v = q[i];
+        c2[4 * i] = v.x; c2[4 * i + 1] = v.y; c2[4 * i + 2] = v.z; c2[4 * i + 3] = v.w;
+      }
+      a2 = p.s2_scale[sidx];
+    }
+  }
+  const bool need_w_for_state = (KIND != kAdamW && KIND != kLion) && p.sc.l2 != 0.f;
+  float n1 = 0.f, n2 = 0.f;  // new absmax
+  // ---- pass 1: new states, absmax only
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float g[32];
+    ptx::tmem_ld_32x32b_x32(tblock + half * 32, g);
+    if (!ok) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float w[8];
+      const int64_t e0 = e_blk + half * 32 + q * 8;
+      if (need_w_for_state) {
+        if (WDT == kWBf16) {
+          const uint4 wb = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0);
+          const uint32_t wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            w[2 * j] = dev::bf16_to_f32(wv[j] & 0xFFFFu);
+            w[2 * j + 1] = dev::bf16_to_f32(wv[j] >> 16);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) w[j] = static_cast<const float*>(p.W)[e0 + j];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) w[j] = 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int jj = half * 32 + q * 8 + j;
+        float s1 = uses_s1(KIND) ? dev::dequant<true>(code_at(c1, jj, true), a1) : 0.f;
+        float s2 = uses_s2(KIND) ? dev::dequant<false>(code_at(c2, jj, false), a2) : 0.f;
+        float wj = w[j];
+        dev::rule<KIND>(wj, g[q * 8 + j], s1, s2, p.sc);
+        if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, s1);
+        if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, s2);
+      }
+    }
+  }
+  // ---- pass 2: recompute, write W, quantise states
+  uint32_t o1[16], o2[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) { o1[i] = 0u; o2[i] = 0u; }
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float g[32];
+    ptx::tmem_ld_32x32b_x32(tblock + half * 32, g);
+    if (!ok) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float w[8];
+      const int64_t e0 = e_blk + half * 32 + q * 8;
+      if (WDT == kWBf16) {
+        const uint4 wb = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0);
+        const uint32_t wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          w[2 * j] = dev::bf16_to_f32(wv[j] & 0xFFFFu);
+          w[2 * j + 1] = dev::bf16_to_f32(wv[j] >> 16);
+        }
+      } else {
+        const float4* wp = reinterpret_cast<const float4*>(static_cast<const float*>(p.W) + e0);
+        const float4 a = wp[0], b = wp[1];
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int jj = half * 32 + q * 8 + j;
+        float s1 = uses_s1(KIND) ? dev::dequant<true>(code_at(c1, jj, true), a1) : 0.f;
+        float s2 = uses_s2(KIND) ? dev::dequant<false>(code_at(c2, jj, false), a2) : 0.f;
+        dev::rule<KIND>(w[j], g[q * 8 + j], s1, s2, p.sc);
+        if (uses_s1(KIND))
+          o1[jj >> 2] |= (static_cast<uint32_t>(dev::quant<true>(s1, n1)) & 0xFFu) << (8 * (jj & 3));
+        if (uses_s2(KIND))
+          o2[jj >> 2] |= (static_cast<uint32_t>(dev::quant<false>(s2, n2)) & 0xFFu) << (8 * (jj & 3));
+      }
+      if (WDT == kWBf16) {
+        const uint4 r = dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step);
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(r, 2 * j)) |
+                 (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(r, 2 * j + 1)) << 16);
+        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.W) + e0) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+        float4* wp = reinterpret_cast<float4*>(static_cast<float*>(p.W) + e0);
+        wp[0] = make_float4(w[0], w[1], w[2], w[3]);
+        wp[1] = make_float4(w[4], w[5], w[6], w[7]);
+      }
+    }
+  }
+  if (!ok) return;
+  if (uses_s1(KIND)) {
+    uint4* q = reinterpret_cast<uint4*>(static_cast<int8_t*>(p.s1) + e_blk);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = make_uint4(o1[4 * i], o1[4 * i + 1], o1[4 * i + 2], o1[4 * i + 3]);
+    p.s1_scale[sidx] = n1;
+  }
+  if (uses_s2(KIND)) {
+    uint4* q = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.s2) + e_blk);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = make_uint4(o2[4 * i], o2[4 * i + 1], o2[4 * i + 2], o2[4 * i + 3]);
+    p.s2_scale[sidx] = n2;
+  }
+}
+
+template <int KIND, int WDT, int SDT>
+__device__ __forceinline__ void epi_fused(uint32_t tbase, int64_t row, int colbase, bool row_ok,
+                                          const GemmParams& p) {
+  if (SDT == kSInt8) {
+#pragma unroll 1
+    for (int blk = 0; blk < 2; ++blk) {
+      const int col0 = colbase + blk * 64;
+      epi_fused_int8_block<KIND, WDT>(tbase + blk * 64, row, col0, row_ok && col0 < p.Ncols, p);
+    }
+  } else {
+    epi_fused_fp32state<KIND, WDT>(tbase, row, colbase, row_ok, p);
+  }
+}
+
+template <int WDT, int SDT>
+__device__ __forceinline__ void epi_fused_dispatch(uint32_t tbase, int64_t row, int colbase,
+                                                   bool row_ok, const GemmParams& p) {
+  switch (p.sc.kind) {
+    case kAdamW: epi_fused<kAdamW, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    case kNAdam: epi_fused<kNAdam, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    case kRAdam: epi_fused<kRAdam, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    case kLion: epi_fused<kLion, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    case kRMSprop: epi_fused<kRMSprop, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    case kAdaGrad: epi_fused<kAdaGrad, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    case kSGD: epi_fused<kSGD, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+    default: epi_fused<kSGDMomentum, WDT, SDT>(tbase, row, colbase, row_ok, p); break;
+  }
+}
+
+// fp32 store of the accumulator (unfused pass 1) or bf16 store (dX).
+template <int MODE>
+__device__ __forceinline__ void epi_store(uint32_t tbase, int64_t row, int colbase, bool row_ok,
+                                          const GemmParams& p) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    float g[32];
+    ptx::tmem_ld_32x32b_x32(tbase + c * 32, g);
+    if (!row_ok) continue;
+    const int col0 = colbase + c * 32;
+    if (MODE == kModeWgradStore) {
+      float* out = static_cast<float*>(p.out) + row * static_cast<int64_t>(p.Ncols);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (col0 + q * 4 < p.Ncols)
+          *reinterpret_cast<float4*>(out + col0 + q * 4) =
+              make_float4(g[4 * q], g[4 * q + 1], g[4 * q + 2], g[4 * q + 3]);
+    } else {
+      uint16_t* out = static_cast<uint16_t*>(p.out) + row * static_cast<int64_t>(p.Ncols);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (col0 + q * 8 >= p.Ncols) continue;
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(g[8 * q + 2 * j], g[8 * q + 2 * j + 1]);
+          o[j] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(out + col0 + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+    }
+  }
+}
+
+template <int MODE, int WDT, int SDT>
+__device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, int lane) {
+  const int quarter = warp & 3;           // TMEM lanes this warp may access
+  const int half = (warp - 2) >> 2;       // which 128 of the 256 columns
+  const int r = quarter * 32 + lane;
+  int local = 0;
+  for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+    const int acc = local & 1;
+    const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+    // One lane waits and the verdict is broadcast, so the warp stays
+    // converged for the .sync.aligned tensor-memory loads that follow.
+    int ok = 0;
+    if (lane == 0) ok = bounded_wait(&ss->tmem_full[acc], aph, p, ss) ? 1 : 0;
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    if (!ok) break;
+    ptx::tc_fence_after();
+    int tm, tn;
+    tile_coords(tile, p, tm, tn);
+    const int64_t row = static_cast<int64_t>(tm) * kTileM + r;
+    const int colbase = tn * kTileN + half * 128;
+    const bool row_ok = row < p.M;
+    const uint32_t tbase = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(acc * kTileN + half * 128);
+    if (MODE == kModeFusedOpt)
+      epi_fused_dispatch<WDT, SDT>(tbase, row, colbase, row_ok, p);
+    else
+      epi_store<MODE>(tbase, row, colbase, row_ok, p);
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ss->tmem_empty[acc]);
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int MODE, int WDT, int SDT>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+              const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + kStages * kABytes;
+  SharedState* ss = reinterpret_cast<SharedState*>(smB + kStages * kBBytes);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&ss->full[s], 1);
+      ptx::mbar_init(&ss->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&ss->tmem_full[a], 1);
+      ptx::mbar_init(&ss->tmem_empty[a], kNumEpiWarps);
+    }
+    ptx::mbar_init(&ss->mma_done, 1);
+    ss->abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&mapA);
+    ptx::prefetch_tensormap(&mapB);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tmem_alloc(&ss->tmem_base, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+
+  if (warp == 0) {
+    if (lane == 0) producer_role<MODE>(&mapA, &mapB, p, smA, smB, ss);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role<MODE>(p, smA, smB, ss);
+  } else {
+    epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(ss->tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace forge

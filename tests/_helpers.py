@@ -1,0 +1,212 @@
+"""Shared test utilities: input construction, oracle/GPU adapters, tolerance checks.
+
+Tolerances ("Tolerances"):
+* quantities with an exact FP32 input (integer-grid data, oracle-supplied
+  gradients): bit-exact;
+* FP32 weights and moments from realistic data: |gpu - ref| <= 1e-7 + 1e-5 |ref|;
+* BF16 weights: <= 1 ULP on >= 99.9 % of elements and <= 2 ULP on every
+  element whose result is decided by the FP32 gradient, i.e. outside the set
+  where the oracle's gradient is within the FP32 summation error of a sign
+  change (the explainer's §2 "Exactness": the summation order is the only
+  difference, and near a sign change it decides the update);
+* INT8 codes: within one step; scales rtol 1e-5 (bit-exact when inputs agree);
+* dX (bf16): |gpu - exact| <= 1 bf16 ULP of the exact value plus the FP32
+  summation bound 2^-20 * sum_n |dY W|.
+"""
+
+import numpy as np
+import torch
+
+from oracle import linear_step as ls
+from oracle import optimizers as opt
+from oracle import quant, rounding
+from optimizer_tcgen05_dw_gb300 import inputs
+
+NAME_TO_KIND = {n: i for i, n in enumerate(opt.NAMES)}
+SUM_ERR = 2.0 ** -20  # relative FP32 summation bound used for exclusions
+
+
+def oracle_hparams(hp: dict) -> opt.Hparams:
+    return opt.Hparams(**hp)
+
+
+def to_bits(t):
+    return inputs.bf16_to_bits(t)
+
+
+class Problem:
+    """One layer: inputs per step, initial state, and both trajectories."""
+
+    def __init__(self, T, N, K, w_dtype, s_dtype, opt_name, hp, seed=1, grid=False,
+                 x_std=1.0, dy_std=1e-3, w_std=0.02, m_std=1e-4, v_std=1e-6, steps=2,
+                 device_inputs=False):
+        self.T, self.N, self.K = T, N, K
+        self.w_dtype, self.s_dtype, self.opt, self.hp = w_dtype, s_dtype, opt_name, hp
+        self.kind = NAME_TO_KIND[opt_name]
+        self.seed = seed
+        self.steps = steps
+        gen_dev = "cuda" if device_inputs else "cpu"
+        self.X, self.dY = [], []
+        for s in range(steps):
+            if grid:
+                X = inputs.integer_grid((T, K), -4, 4, 0, inputs.layer_seed(seed, 0, s, 1), device=gen_dev)
+                dY = inputs.integer_grid((T, N), -4, 4, -12, inputs.layer_seed(seed, 0, s, 2), device=gen_dev)
+            else:
+                X = inputs.normal((T, K), x_std, inputs.layer_seed(seed, 0, s, 1), device=gen_dev)
+                dY = inputs.normal((T, N), dy_std, inputs.layer_seed(seed, 0, s, 2), device=gen_dev)
+            self.X.append(X)
+            self.dY.append(dY)
+        W = inputs.normal((N, K), w_std, inputs.layer_seed(seed, 0, 0, 3), torch.float32)
+        m = inputs.normal((N, K), m_std, inputs.layer_seed(seed, 0, 0, 4), torch.float32)
+        v = inputs.abs_normal((N, K), v_std, inputs.layer_seed(seed, 0, 0, 5))
+        st = {"w_dtype": w_dtype, "s_dtype": s_dtype,
+              "W": W.numpy() if w_dtype == "fp32" else rounding.bf16_bits_rne(W.numpy())}
+        if opt.USES_S1[self.kind]:
+            if s_dtype == "int8":
+                st["s1"], st["s1_scale"] = quant.quantize_blocks(m.numpy(), signed=True)
+            else:
+                st["s1"] = m.numpy()
+        if opt.USES_S2[self.kind]:
+            if s_dtype == "int8":
+                st["s2"], st["s2_scale"] = quant.quantize_blocks(v.numpy(), signed=False)
+            else:
+                st["s2"] = v.numpy()
+        self.state0 = st
+
+    # ---- GPU side
+    def gpu_state(self):
+        st = self.state0
+        dev = "cuda"
+        W = (torch.from_numpy(st["W"].copy()) if self.w_dtype == "fp32"
+             else inputs.bits_to_bf16(st["W"])).to(dev)
+        out = {"W": W}
+        for k in ("s1", "s2", "s1_scale", "s2_scale"):
+            if st.get(k) is not None:
+                out[k] = torch.from_numpy(np.ascontiguousarray(st[k])).to(dev)
+        return out
+
+    def run_gpu(self, fused=True, want_dx=False, state=None):
+        from optimizer_tcgen05_dw_gb300 import api
+        g = self.gpu_state() if state is None else state
+        dxs = []
+        for s in range(self.steps):
+            X, dY = self.X[s].cuda(), self.dY[s].cuda()
+            dX = torch.empty((self.T, self.K), dtype=torch.bfloat16, device="cuda") if want_dx else None
+            if fused:
+                api.forge_linear_bwd_step(X, dY, g["W"], self.opt, self.hp, s + 1, self.seed,
+                                          g.get("s1"), g.get("s2"), g.get("s1_scale"),
+                                          g.get("s2_scale"), dX=dX)
+            else:
+                if want_dx:
+                    api.forge_linear_dgrad(dY, g["W"], dX)
+                dW = torch.empty((self.N, self.K), dtype=torch.float32, device="cuda")
+                api.forge_unfused_wgrad(X, dY, dW)
+                api.forge_unfused_opt_step(dW, g["W"], self.opt, self.hp, s + 1, self.seed,
+                                           g.get("s1"), g.get("s2"), g.get("s1_scale"),
+                                           g.get("s2_scale"))
+            dxs.append(dX)
+        api.forge_get_device_status()
+        torch.cuda.synchronize()
+        return g, dxs
+
+    # ---- oracle side
+    def run_oracle(self, want_dx=False):
+        st = {k: (None if v is None else (v.copy() if isinstance(v, np.ndarray) else v))
+              for k, v in self.state0.items()}
+        hp = oracle_hparams(self.hp)
+        dxs, sens = [], np.zeros((self.N, self.K), dtype=bool)
+        for s in range(self.steps):
+            Xb, dYb = to_bits(self.X[s]), to_bits(self.dY[s])
+            sens |= self.sensitive(Xb, dYb, st)
+            out = ls.linear_bwd_step(Xb, dYb, st, self.kind, hp, s + 1, self.seed, want_dx=want_dx)
+            dxs.append(out.get("dX"))
+            st.update({k: out[k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale")})
+        return st, dxs, sens
+
+    def sensitive(self, Xb, dYb, st):
+        """Elements whose update flips within the FP32 summation error of g."""
+        X = rounding.bf16_bits_to_f32(Xb).astype(np.float64)
+        dY = rounding.bf16_bits_to_f32(dYb).astype(np.float64)
+        g = dY.T @ X
+        bound = SUM_ERR * (np.abs(dY).T @ np.abs(X)) + 1e-30
+        mask = np.abs(g) <= bound
+        if self.kind == opt.LION and st.get("s1") is not None:
+            m = st["s1"] if self.s_dtype == "fp32" else quant.dequantize_blocks(
+                st["s1"], st["s1_scale"], True)
+            b1 = np.float32(self.hp.get("beta1", 0.9))
+            c = b1 * m.astype(np.float64) + (1 - b1) * g
+            mask |= np.abs(c) <= bound
+        return mask
+
+
+def gpu_np(t):
+    if t.dtype == torch.bfloat16:
+        return to_bits(t)
+    return t.detach().cpu().numpy()
+
+
+def assert_bitexact(gpu, ref, what):
+    a, b = gpu_np(gpu), np.asarray(ref)
+    if a.dtype == np.float32:
+        same = (a == b) | (np.isnan(a) & np.isnan(b))
+    else:
+        same = a == b
+    bad = np.argwhere(~same)
+    assert bad.size == 0, f"{what}: {len(bad)} of {a.size} differ; first at {bad[:3].tolist()}: " \
+        f"gpu={a[tuple(bad[0])]} ref={b[tuple(bad[0])]}"
+
+
+def assert_fp32_close(gpu, ref, what, exclude=None, rtol=1e-5, atol=1e-7):
+    a = gpu_np(gpu).astype(np.float64)
+    b = np.asarray(ref, dtype=np.float64)
+    ok = np.abs(a - b) <= atol + rtol * np.abs(b)
+    if exclude is not None:
+        ok |= exclude
+    bad = np.argwhere(~ok)
+    assert bad.size == 0, f"{what}: {len(bad)} of {a.size} outside tolerance; first " \
+        f"{bad[:3].tolist()}: gpu={a[tuple(bad[0])]} ref={b[tuple(bad[0])]}"
+
+
+def assert_bf16_close(gpu, ref_bits, what, exclude=None):
+    d = rounding.bf16_ulp_distance(gpu_np(gpu), ref_bits)
+    frac1 = float((d <= 1).mean())
+    assert frac1 >= 0.999, f"{what}: only {frac1:.5f} of elements within 1 ULP"
+    far = d > 2
+    if exclude is not None:
+        far &= ~exclude
+    bad = np.argwhere(far)
+    assert bad.size == 0, f"{what}: {len(bad)} elements beyond 2 ULP; first {bad[:3].tolist()} " \
+        f"({d[tuple(bad[0])]} ULP)"
+
+
+def block_mask(mask):
+    """Element mask -> the same mask widened to whole 64-element blocks."""
+    N, K = mask.shape
+    b = mask.reshape(N, K // 64, 64).any(axis=2)
+    return np.repeat(b, 64, axis=1), b
+
+
+def assert_int8_close(gpu_codes, gpu_scale, ref_codes, ref_scale, what, exclude=None):
+    a = gpu_np(gpu_codes).astype(np.int64)
+    b = np.asarray(ref_codes).astype(np.int64)
+    ex_el, ex_blk = (None, None) if exclude is None else block_mask(exclude)
+    diff = np.abs(a - b) > 1
+    if ex_el is not None:
+        diff &= ~ex_el
+    bad = np.argwhere(diff)
+    assert bad.size == 0, f"{what}: {len(bad)} codes differ by more than one step"
+    assert_fp32_close(gpu_scale, ref_scale, what + " scale", exclude=ex_blk)
+
+
+def assert_dx_close(gpu_dx, dYb, Wb, what):
+    dY = rounding.bf16_bits_to_f32(dYb).astype(np.float64)
+    W = rounding.bf16_bits_to_f32(Wb).astype(np.float64)
+    exact = dY @ W
+    bound = SUM_ERR * (np.abs(dY) @ np.abs(W))
+    a = rounding.bf16_bits_to_f32(gpu_np(gpu_dx)).astype(np.float64)
+    ulp = np.maximum(np.abs(exact), 1e-38)
+    ulp = 2.0 ** (np.floor(np.log2(ulp)) - 7)
+    ok = np.abs(a - exact) <= ulp + bound
+    bad = np.argwhere(~ok)
+    assert bad.size == 0, f"{what}: {len(bad)} of {a.size} outside; first {bad[:3].tolist()}: " \
+        f"gpu={a[tuple(bad[0])]} exact={exact[tuple(bad[0])]}"

@@ -1,0 +1,114 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/forge.h declares, and rejects invalid arguments on the host
+before any CUDA call.  No computation is launched here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from optimizer_tcgen05_dw_gb300 import api
+from optimizer_tcgen05_dw_gb300.build import build, lib_path
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    build()
+    return api.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "forge.h")) as f:
+        src = f.read()
+    return re.findall(r"FORGE_API\s+[\w\s\*]+?\b(forge_\w+)\s*\(", src)
+
+
+def test_header_declares_the_entry_points():
+    names = set(_declared())
+    for n in ("forge_linear_bwd_step", "forge_linear_dgrad", "forge_unfused_wgrad",
+              "forge_unfused_opt_step", "forge_quantize_state", "forge_dequantize_state",
+              "forge_get_device_status", "forge_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    raw = ctypes.CDLL(lib_path("libforge.so"))
+    for name in _declared():
+        assert hasattr(raw, name), name
+    assert L.forge_abi_version() == 1
+
+
+def test_status_strings(L):
+    for code, name in api.STATUS.items():
+        assert L.forge_status_string(code).decode().startswith(name)
+
+
+def _lin(T=64, N=128, K=256, x=16, dy=16, dx=None):
+    return api.ForgeLinear(T, N, K, ctypes.c_void_p(x), ctypes.c_void_p(dy),
+                           None if dx is None else ctypes.c_void_p(dx))
+
+
+def _state(w=32, s1=48, s2=64, wdt=1, sdt=0, sc1=None, sc2=None):
+    return api.ForgeState(ctypes.c_void_p(w), wdt, sdt, ctypes.c_void_p(s1) if s1 else None,
+                          ctypes.c_void_p(s2) if s2 else None,
+                          ctypes.c_void_p(sc1) if sc1 else None, ctypes.c_void_p(sc2) if sc2 else None)
+
+
+@pytest.mark.parametrize("case", [
+    "null_lin", "bad_kind", "step0", "n_not_mult8", "int8_k_not_mult64", "missing_state",
+    "misaligned_x", "null_hp", "bad_wdtype", "int8_missing_scale"])
+def test_invalid_arguments_rejected_on_host(L, case):
+    hp = api.hparams()
+    lin, st, kind, step, hpp = _lin(), _state(), 0, 1, ctypes.byref(hp)
+    if case == "null_lin":
+        lin = None
+    elif case == "bad_kind":
+        kind = 9
+    elif case == "step0":
+        step = 0
+    elif case == "n_not_mult8":
+        lin = _lin(N=100)
+    elif case == "int8_k_not_mult64":
+        lin = _lin(K=200)
+        st = _state(sdt=1, sc1=80, sc2=96)
+    elif case == "missing_state":
+        st = _state(s2=0)
+    elif case == "misaligned_x":
+        lin = _lin(x=17)
+    elif case == "null_hp":
+        hpp = None
+    elif case == "bad_wdtype":
+        st = _state(wdt=5)
+    elif case == "int8_missing_scale":
+        st = _state(sdt=1, sc1=80)
+    rc = L.forge_linear_bwd_step(None if lin is None else ctypes.byref(lin), ctypes.byref(st),
+                                 kind, hpp, step, 0, None)
+    assert rc == 1, (case, rc, L.forge_last_error_message())
+    assert L.forge_last_error_message().decode() != ""
+
+
+def test_other_entry_points_validate(L):
+    assert L.forge_unfused_opt_step(None, None, 8, 8, 0, None, 1, 0, None) == 1
+    assert L.forge_quantize_state(None, None, None, 4, 100, 1, None) == 1  # cols % 64
+    assert L.forge_unfused_wgrad(ctypes.byref(_lin()), ctypes.c_void_p(3), None) == 1  # misaligned dW
+    assert L.forge_linear_dgrad(ctypes.byref(_lin(dx=16)), None, 7, None) == 1  # bad w_dtype
+
+
+def test_empty_problem_is_a_no_op(L):
+    """N == 0 or K == 0: nothing to do, no device touched."""
+    hp = api.hparams()
+    assert L.forge_linear_bwd_step(ctypes.byref(_lin(N=0)), ctypes.byref(_state()), 0,
+                                   ctypes.byref(hp), 1, 0, None) == 0
+
+
+def test_valid_call_without_a_gpu_reports_cuda_error(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    hp = api.hparams()
+    rc = L.forge_linear_bwd_step(ctypes.byref(_lin()), ctypes.byref(_state()), 0,
+                                 ctypes.byref(hp), 1, 0, None)
+    assert rc == 3

@@ -1,0 +1,157 @@
+"""Full-size parity on sampled tiles, in the launch configuration the bench times.
+
+The oracle cannot form dW for a whole Llama/Qwen layer at T = 16384 in a test,
+but every element's update depends only on its own coordinate (FORGE
+explainer, Technical Summary §2 "Exactness"), so it follows a set of sampled
+128 x 128 tiles (the four corners plus random interior tiles) through every
+step from the same initial state and seeded inputs, and those tiles of the
+GPU result are compared with it.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import linear_step as ls
+from oracle import optimizers as opt
+from oracle import quant, rounding
+from optimizer_tcgen05_dw_gb300 import api, inputs
+from optimizer_tcgen05_dw_gb300.build import build
+
+from _helpers import (SUM_ERR, assert_bf16_close, assert_fp32_close, assert_int8_close,
+                      oracle_hparams, to_bits)
+
+pytestmark = pytest.mark.gpu
+
+TILE = 128
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library(cuda_device):
+    build()
+    api.lib()
+    api.forge_set_wait_limit_ns(200_000_000)
+    yield
+    api.forge_set_wait_limit_ns(0)
+
+
+def _tiles(N, K, count, seed):
+    rng = np.random.default_rng(seed)
+    tn, tk = N // TILE, K // TILE
+    picks = {(0, 0), (0, tk - 1), (tn - 1, 0), (tn - 1, tk - 1)}
+    while len(picks) < count:
+        picks.add((int(rng.integers(0, tn)), int(rng.integers(0, tk))))
+    return sorted((a * TILE, b * TILE) for a, b in picks)
+
+
+def run_sampled(N, K, T, w_dtype, s_dtype, opt_name, hp, steps, seed, m_std=0.0, v_std=0.0,
+                x_std=1.0, dy_std=1e-3, n_tiles=12):
+    kind = opt.NAMES.index(opt_name)
+    tiles = _tiles(N, K, n_tiles, seed)
+    # initial state, drawn on the CPU from seeds; INT8 codes from the oracle quantiser
+    W = inputs.normal((N, K), 0.02, inputs.layer_seed(seed, 0, 0, 3), torch.float32)
+    st = {"w_dtype": w_dtype, "s_dtype": s_dtype,
+          "W": W.numpy() if w_dtype == "fp32" else rounding.bf16_bits_rne(W.numpy())}
+    del W
+    if opt.USES_S1[kind]:
+        m = inputs.normal((N, K), m_std, inputs.layer_seed(seed, 0, 0, 4), torch.float32).numpy()
+        if s_dtype == "int8":
+            st["s1"], st["s1_scale"] = quant.quantize_blocks(m, True)
+        else:
+            st["s1"] = m
+    if opt.USES_S2[kind]:
+        v = inputs.abs_normal((N, K), v_std, inputs.layer_seed(seed, 0, 0, 5)).numpy()
+        if s_dtype == "int8":
+            st["s2"], st["s2_scale"] = quant.quantize_blocks(v, False)
+        else:
+            st["s2"] = v
+    gpu = {"W": (torch.from_numpy(st["W"]) if w_dtype == "fp32"
+                 else inputs.bits_to_bf16(st["W"])).cuda()}
+    for k in ("s1", "s2", "s1_scale", "s2_scale"):
+        if st.get(k) is not None:
+            gpu[k] = torch.from_numpy(np.ascontiguousarray(st[k])).cuda()
+    # per-tile oracle state
+    def cut(a, n0, k0, block=1):
+        return None if a is None else np.ascontiguousarray(
+            a[n0:n0 + TILE, k0 // block:(k0 + TILE) // block])
+    ost = {t: {k: cut(st.get(k), *t, 64 if k.endswith("scale") else 1)
+               for k in ("W", "s1", "s2", "s1_scale", "s2_scale")} for t in tiles}
+    sens = {t: np.zeros((TILE, TILE), dtype=bool) for t in tiles}
+    ohp = oracle_hparams(hp)
+    for s in range(steps):
+        X = inputs.normal((T, K), x_std, inputs.layer_seed(seed, 0, s, 1), device="cuda")
+        dY = inputs.normal((T, N), dy_std, inputs.layer_seed(seed, 0, s, 2), device="cuda")
+        api.forge_linear_bwd_step(X, dY, gpu["W"], opt_name, hp, s + 1, seed, gpu.get("s1"),
+                                  gpu.get("s2"), gpu.get("s1_scale"), gpu.get("s2_scale"))
+        cols = sorted({k0 for _, k0 in tiles})
+        rows = sorted({n0 for n0, _ in tiles})
+        Xc = {k0: to_bits(X[:, k0:k0 + TILE].contiguous()) for k0 in cols}
+        dYc = {n0: to_bits(dY[:, n0:n0 + TILE].contiguous()) for n0 in rows}
+        del X, dY
+        for (n0, k0) in tiles:
+            g = ls.weight_gradient(Xc[k0], dYc[n0])
+            Xf = rounding.bf16_bits_to_f32(Xc[k0]).astype(np.float64)
+            dYf = rounding.bf16_bits_to_f32(dYc[n0]).astype(np.float64)
+            bound = SUM_ERR * (np.abs(dYf).T @ np.abs(Xf))
+            sens[(n0, k0)] |= np.abs(g.astype(np.float64)) <= bound
+            o = ost[(n0, k0)]
+            out = ls.update_block(kind, ohp, s + 1, seed, g, o["W"], w_dtype, o["s1"], o["s2"],
+                                  o["s1_scale"], o["s2_scale"], s_dtype, n0, k0, K)
+            o.update({k: out[k] for k in o})
+    api.forge_get_device_status()
+    torch.cuda.synchronize()
+    frac_sens = np.mean([m.mean() for m in sens.values()])
+    assert frac_sens < 1e-3
+    for (n0, k0) in tiles:
+        o, ex = ost[(n0, k0)], sens[(n0, k0)]
+        gw = gpu["W"][n0:n0 + TILE, k0:k0 + TILE].contiguous()
+        where = f"tile ({n0},{k0})"
+        if w_dtype == "bf16":
+            assert_bf16_close(gw, o["W"], "W " + where, exclude=ex)
+        else:
+            assert_fp32_close(gw, o["W"], "W " + where, exclude=ex)
+        for k in ("s1", "s2"):
+            if o[k] is None:
+                continue
+            gs = gpu[k][n0:n0 + TILE, k0:k0 + TILE].contiguous()
+            if s_dtype == "int8":
+                gsc = gpu[k + "_scale"][n0:n0 + TILE, k0 // 64:(k0 + TILE) // 64].contiguous()
+                assert_int8_close(gs, gsc, o[k], o[k + "_scale"], f"{k} {where}", exclude=ex)
+            else:
+                assert_fp32_close(gs, o[k], f"{k} {where}", exclude=ex)
+
+
+LLAMA = {n: (N, K) for n, N, K in inputs.LLAMA31_8B_LINEARS}
+QWEN = {n: (N, K) for n, N, K in inputs.QWEN3_14B_LINEARS}
+
+
+@pytest.mark.parametrize("layer", ["gate_proj", "down_proj", "k_proj"])
+def test_llama8b_bf16_fp32state_sampled(layer):
+    w = inputs.WORKLOADS["llama8b_bf16_fp32state"]
+    N, K = LLAMA[layer]
+    run_sampled(N, K, w.T, "bf16", "fp32", "adamw", w.hparams, steps=2, seed=2000 + N % 97,
+                m_std=1e-4, v_std=1e-6)
+
+
+@pytest.mark.parametrize("layer", ["up_proj", "o_proj"])
+def test_llama8b_bf16_int8state_sampled(layer):
+    w = inputs.WORKLOADS["llama8b_bf16_int8state"]
+    N, K = LLAMA[layer]
+    run_sampled(N, K, w.T, "bf16", "int8", "adamw", w.hparams, steps=2, seed=3000 + N % 89,
+                m_std=w.m_init_std, v_std=w.v_init_std)
+
+
+@pytest.mark.parametrize("opt_name", list(opt.NAMES))
+def test_optimizer_sweep_4096_sampled(opt_name):
+    w = inputs.WORKLOADS["sweep_4096"]
+    _, N, K = w.linears[0]
+    run_sampled(N, K, w.T, "bf16", "fp32", opt_name, inputs.SWEEP_HPARAMS[opt_name],
+                steps=w.steps, seed=4000 + opt.NAMES.index(opt_name), n_tiles=8)
+
+
+@pytest.mark.parametrize("layer", ["down_proj", "v_proj"])
+def test_qwen14b_int8_sampled(layer):
+    w = inputs.WORKLOADS["qwen14b_int8"]
+    N, K = QWEN[layer]
+    run_sampled(N, K, w.T, "bf16", "int8", "adamw", w.hparams, steps=2, seed=5000 + N % 83,
+                m_std=1e-4, v_std=1e-6)
