@@ -52,6 +52,17 @@ def _peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's value (replicas report the max time).  Works with
+    NCCL (device tensor) and gloo (CPU tensor)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -179,11 +190,14 @@ class Layer:
         self.seed = seed
 
 
-def build_workload(dev, T):
+def build_workload(dev, T, only=None):
+    names = [n for n in ORDER if not only or n in only]
     acts = {"x_attn": 4096, "x_o": 4096, "x_mlp": 4096, "x_down": 14336}
-    X = {a: inputs.normal((T, k), 1.0, 100 + i, torch.bfloat16, dev) for i, (a, k) in enumerate(acts.items())}
+    used = {ACT[n] for n in names}
+    X = {a: inputs.normal((T, k), 1.0, 100 + i, torch.bfloat16, dev)
+         for i, (a, k) in enumerate(acts.items()) if a in used}
     shapes = {n: (N, K) for n, N, K in inputs.LLAMA31_8B_LINEARS}
-    layers = [Layer(n, *shapes[n], T, dev, 1000 + 17 * i) for i, n in enumerate(ORDER)]
+    layers = [Layer(n, *shapes[n], T, dev, 1000 + 17 * ORDER.index(n)) for n in names]
     return X, layers
 
 
@@ -204,7 +218,7 @@ def run_ours(args):
     w = inputs.WORKLOADS[WORKLOAD_KEY]
     T = w.T
     hp = w.hparams
-    X, layers = build_workload(dev, T)
+    X, layers = build_workload(dev, T, args.layers)
     stream = torch.cuda.current_stream()
     flops_dw = sum(2.0 * L.N * L.K * T for L in layers)
     flops_step = 2.0 * flops_dw  # dW + dX
@@ -228,13 +242,6 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     s_no = 1
     for _ in range(args.warmup):
         step(s_no)
@@ -254,7 +261,7 @@ def run_ours(args):
     barrier()
     api.forge_get_device_status()
     ms = start.elapsed_time(end) / args.steps
-    ms = max_over_ranks(ms)
+    ms = max_over_ranks(ms, dist, dev)
     fused_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev[L.name])
     fused_launches = sum(len(v) for v in ev.values())
     fused_tflops = flops_dw * args.steps / (fused_ms * 1e-3) / 1e12
@@ -265,6 +272,16 @@ def run_ours(args):
     # algorithmic bytes of the fused kernel per step: X and dY once, W r/w (bf16), m and v r/w (fp32)
     params = sum(L.N * L.K for L in layers)
     bytes_fused = sum((L.T * L.K + L.T * L.N) * 2 for L in layers) + params * (4 + 16)
+
+    if args.no_extras:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s",
+                              "ms_per_step": round(ms, 4), "layers": [L.name for L in layers],
+                              "roofline_achieved": round(fused_tflops, 2),
+                              "note": "partial run (--no-extras): not a bench result"}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
 
     # ---- e2e: inputs from pinned host memory every step
     hostX = {k: v.cpu().pin_memory() for k, v in X.items()}
@@ -286,7 +303,7 @@ def run_ours(args):
         api.forge_get_device_status()  # device -> host read of the step's status word
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist, dev)
     e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
     del hostX, hostdY
 
@@ -317,7 +334,7 @@ def run_ours(args):
     u1.record(stream)
     torch.cuda.synchronize()
     api.forge_get_device_status()
-    unf_ms = max_over_ranks(u0.elapsed_time(u1) / u_steps)
+    unf_ms = max_over_ranks(u0.elapsed_time(u1) / u_steps, dist, dev)
     del dW
     torch.cuda.synchronize()
 
@@ -378,6 +395,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", nargs="*", default=None, choices=ORDER,
+                    help="restrict to some linears (profiling); the bench line uses all seven")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="time the step only (profiling runs): no e2e, unfused or CPU legs")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -109,6 +109,36 @@ class Problem:
         torch.cuda.synchronize()
         return g, dxs
 
+    def upload(self, st):
+        dev = "cuda"
+        W = (torch.from_numpy(np.ascontiguousarray(st["W"])) if self.w_dtype == "fp32"
+             else inputs.bits_to_bf16(st["W"])).to(dev)
+        out = {"W": W}
+        for k in ("s1", "s2", "s1_scale", "s2_scale"):
+            if st.get(k) is not None:
+                out[k] = torch.from_numpy(np.ascontiguousarray(st[k])).to(dev)
+        return out
+
+    def per_step_from_common_state(self, check):
+        """Every step starts both sides from the oracle's state; `check(step,
+        gpu_state, oracle_state, sensitive_mask)` compares that step's outputs."""
+        from optimizer_tcgen05_dw_gb300 import api
+        st = {k: v for k, v in self.state0.items()}
+        hp = oracle_hparams(self.hp)
+        for s in range(self.steps):
+            g = self.upload(st)
+            Xb, dYb = to_bits(self.X[s]), to_bits(self.dY[s])
+            api.forge_linear_bwd_step(self.X[s].cuda(), self.dY[s].cuda(), g["W"], self.opt,
+                                      self.hp, s + 1, self.seed, g.get("s1"), g.get("s2"),
+                                      g.get("s1_scale"), g.get("s2_scale"))
+            api.forge_get_device_status()
+            sens = self.sensitive(Xb, dYb, st)
+            out = ls.linear_bwd_step(Xb, dYb, st, self.kind, hp, s + 1, self.seed, want_dx=False)
+            st = dict(st)
+            st.update({k: out[k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale")})
+            check(s + 1, g, st, sens)
+        return st
+
     # ---- oracle side
     def run_oracle(self, want_dx=False):
         st = {k: (None if v is None else (v.copy() if isinstance(v, np.ndarray) else v))
@@ -167,10 +197,30 @@ def assert_fp32_close(gpu, ref, what, exclude=None, rtol=1e-5, atol=1e-7):
         f"{bad[:3].tolist()}: gpu={a[tuple(bad[0])]} ref={b[tuple(bad[0])]}"
 
 
-def assert_bf16_close(gpu, ref_bits, what, exclude=None):
-    d = rounding.bf16_ulp_distance(gpu_np(gpu), ref_bits)
+def _ulp_at(mag):
+    """bf16 ULP size at magnitude mag (normal range)."""
+    mag = np.maximum(np.asarray(mag, dtype=np.float64), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(mag)) - 7)
+
+
+def assert_bf16_close(gpu, ref_bits, what, exclude=None, free_running=False):
+    """<= 1 ULP on >= 99.9 % of elements, <= 2 ULP on all non-excluded ones.
+
+    One step from a common state (free_running=False): ULPs are the bf16 grid
+    steps between the two values.  A free-running multi-step trajectory
+    (free_running=True): once one stochastic rounding decision differs, the
+    trajectories stay one ULP apart in absolute terms, and a weight that later
+    passes near zero turns that gap into many ULPs of a smaller binade, so the
+    ULP is taken at the larger of the two values and the RMS weight."""
+    a_bits = gpu_np(gpu)
+    d = rounding.bf16_ulp_distance(a_bits, ref_bits)
     frac1 = float((d <= 1).mean())
     assert frac1 >= 0.999, f"{what}: only {frac1:.5f} of elements within 1 ULP"
+    if free_running:
+        a = rounding.bf16_bits_to_f32(a_bits).astype(np.float64)
+        b = rounding.bf16_bits_to_f32(ref_bits).astype(np.float64)
+        rms = float(np.sqrt(np.mean(b * b)))
+        d = np.abs(a - b) / _ulp_at(np.maximum(np.maximum(np.abs(a), np.abs(b)), rms))
     far = d > 2
     if exclude is not None:
         far &= ~exclude

@@ -107,7 +107,7 @@ def run_sampled(N, K, T, w_dtype, s_dtype, opt_name, hp, steps, seed, m_std=0.0,
         gw = gpu["W"][n0:n0 + TILE, k0:k0 + TILE].contiguous()
         where = f"tile ({n0},{k0})"
         if w_dtype == "bf16":
-            assert_bf16_close(gw, o["W"], "W " + where, exclude=ex)
+            assert_bf16_close(gw, o["W"], "W " + where, exclude=ex, free_running=steps > 1)
         else:
             assert_fp32_close(gw, o["W"], "W " + where, exclude=ex)
         for k in ("s1", "s2"):
