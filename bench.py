@@ -224,9 +224,13 @@ def run_ours(args):
     flops_step = 2.0 * flops_dw  # dW + dX
 
     ev = {L.name: [] for L in layers}
+    ev_dx = {L.name: [] for L in layers}
 
     def step(s, record=False):
         for L in layers:
+            if record:
+                z = torch.cuda.Event(enable_timing=True)
+                z.record(stream)
             api.forge_linear_dgrad(L.dY, L.W, L.dX)
             if record:
                 a = torch.cuda.Event(enable_timing=True)
@@ -236,6 +240,7 @@ def run_ours(args):
             if record:
                 b.record(stream)
                 ev[L.name].append((a, b))
+                ev_dx[L.name].append((z, a))
 
     def barrier():
         if dist is not None:
@@ -269,6 +274,8 @@ def run_ours(args):
     value = flops_step * world / (ms * 1e-3) / 1e12
     per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev[L.name]]) * 1e-3) / 1e12, 1)
                  for L in layers}
+    dx_per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev_dx[L.name]]) * 1e-3) / 1e12, 1)
+                    for L in layers}
     # algorithmic bytes of the fused kernel per step: X and dY once, W r/w (bf16), m and v r/w (fp32)
     params = sum(L.N * L.K for L in layers)
     bytes_fused = sum((L.T * L.K + L.T * L.N) * 2 for L in layers) + params * (4 + 16)
@@ -364,6 +371,7 @@ def run_ours(args):
                      "algorithmic_bytes_per_step": bytes_fused,
                      "launches_timed": fused_launches,
                      "per_layer_tflops": per_layer},
+        "dgrad_per_layer_tflops": dx_per_layer,
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": 4, "ms_per_step": round(e2e_ms, 4)},
         "unfused": {"ms_per_step": round(unf_ms, 4),

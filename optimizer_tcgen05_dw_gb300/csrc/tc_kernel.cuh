@@ -66,9 +66,20 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, con
   }
 }
 
+// Tile order: groups of kRasterGroup consecutive column tiles, row-major
+// inside a group.  The ~num_SMs tiles in flight at once then cover a compact
+// (num_SMs / 8) x 8 rectangle, so each wave streams a small set of operand
+// column blocks from HBM instead of every column block of one operand.
+constexpr int kRasterGroup = 8;
+
 __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& tm, int& tn) {
-  tm = tile / p.tiles_n;
-  tn = tile - tm * p.tiles_n;
+  const int span = p.tiles_m * kRasterGroup;
+  const int grp = tile / span;
+  const int first_n = grp * kRasterGroup;
+  const int width = min(kRasterGroup, p.tiles_n - first_n);
+  const int local = tile - grp * span;
+  tm = local / width;
+  tn = first_n + (local - tm * width);
 }
 
 // ------------------------------------------------------------------ roles
@@ -155,36 +166,64 @@ done:
 
 // ------------------------------------------------------------------ epilogues
 
+// W / state traffic of the epilogue touches each line once (read, then
+// written back): keep it out of L1 and mark it evict-first in L2, so it does
+// not displace the operand tiles the main loop re-reads from L2.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
+__device__ __forceinline__ void st_stream(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;"
+               ::"l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+__device__ __forceinline__ void ld8f(const float* p, float (&v)[8], uint64_t pol) {
+  const uint4 a = ld_stream(p, pol), b = ld_stream(p + 4, pol);
+  v[0] = __uint_as_float(a.x); v[1] = __uint_as_float(a.y);
+  v[2] = __uint_as_float(a.z); v[3] = __uint_as_float(a.w);
+  v[4] = __uint_as_float(b.x); v[5] = __uint_as_float(b.y);
+  v[6] = __uint_as_float(b.z); v[7] = __uint_as_float(b.w);
+}
+
+__device__ __forceinline__ void st8f(float* p, const float (&v)[8], uint64_t pol) {
+  st_stream(p, make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]),
+                          __float_as_uint(v[3])), pol);
+  st_stream(p + 4, make_uint4(__float_as_uint(v[4]), __float_as_uint(v[5]),
+                              __float_as_uint(v[6]), __float_as_uint(v[7])), pol);
+}
+
+__device__ __forceinline__ void ld8bf16(const uint16_t* p, float (&w)[8], uint64_t pol) {
+  const uint4 wb = ld_stream(p, pol);
+  const uint32_t wv[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    w[2 * j] = dev::bf16_to_f32(wv[j] & 0xFFFFu);
+    w[2 * j + 1] = dev::bf16_to_f32(wv[j] >> 16);
+  }
+}
+
 // 8 consecutive elements e0..e0+7 of one row of W (e0 % 8 == 0), fp32 or no
 // state: load, apply the rule, round, store.
 template <int KIND, int WDT>
-__device__ __forceinline__ void group8_fp32state(const float* g, int64_t e0, const GemmParams& p) {
+__device__ __forceinline__ void group8_fp32state(const float* g, int64_t e0, const GemmParams& p,
+                                                 uint64_t pol) {
   float w[8], s1[8], s2[8];
-  if (WDT == kWBf16) {
-    const uint4 wb = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0);
-    const uint32_t wv[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      w[2 * j] = dev::bf16_to_f32(wv[j] & 0xFFFFu);
-      w[2 * j + 1] = dev::bf16_to_f32(wv[j] >> 16);
-    }
-  } else {
-    const float4* wp = reinterpret_cast<const float4*>(static_cast<const float*>(p.W) + e0);
-    const float4 a = wp[0], b = wp[1];
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-  }
-  if (uses_s1(KIND)) {
-    const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(p.s1) + e0);
-    const float4 a = sp[0], b = sp[1];
-    s1[0] = a.x; s1[1] = a.y; s1[2] = a.z; s1[3] = a.w;
-    s1[4] = b.x; s1[5] = b.y; s1[6] = b.z; s1[7] = b.w;
-  }
-  if (uses_s2(KIND)) {
-    const float4* sp = reinterpret_cast<const float4*>(static_cast<const float*>(p.s2) + e0);
-    const float4 a = sp[0], b = sp[1];
-    s2[0] = a.x; s2[1] = a.y; s2[2] = a.z; s2[3] = a.w;
-    s2[4] = b.x; s2[5] = b.y; s2[6] = b.z; s2[7] = b.w;
-  }
+  if (WDT == kWBf16) ld8bf16(static_cast<const uint16_t*>(p.W) + e0, w, pol);
+  else ld8f(static_cast<const float*>(p.W) + e0, w, pol);
+  if (uses_s1(KIND)) ld8f(static_cast<const float*>(p.s1) + e0, s1, pol);
+  if (uses_s2(KIND)) ld8f(static_cast<const float*>(p.s2) + e0, s2, pol);
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
   if (WDT == kWBf16) {
@@ -194,28 +233,19 @@ __device__ __forceinline__ void group8_fp32state(const float* g, int64_t e0, con
     for (int j = 0; j < 4; ++j)
       o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(r, 2 * j)) |
              (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(r, 2 * j + 1)) << 16);
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.W) + e0) = make_uint4(o[0], o[1], o[2], o[3]);
+    st_stream(static_cast<uint16_t*>(p.W) + e0, make_uint4(o[0], o[1], o[2], o[3]), pol);
   } else {
-    float4* wp = reinterpret_cast<float4*>(static_cast<float*>(p.W) + e0);
-    wp[0] = make_float4(w[0], w[1], w[2], w[3]);
-    wp[1] = make_float4(w[4], w[5], w[6], w[7]);
+    st8f(static_cast<float*>(p.W) + e0, w, pol);
   }
-  if (uses_s1(KIND)) {
-    float4* sp = reinterpret_cast<float4*>(static_cast<float*>(p.s1) + e0);
-    sp[0] = make_float4(s1[0], s1[1], s1[2], s1[3]);
-    sp[1] = make_float4(s1[4], s1[5], s1[6], s1[7]);
-  }
-  if (uses_s2(KIND)) {
-    float4* sp = reinterpret_cast<float4*>(static_cast<float*>(p.s2) + e0);
-    sp[0] = make_float4(s2[0], s2[1], s2[2], s2[3]);
-    sp[1] = make_float4(s2[4], s2[5], s2[6], s2[7]);
-  }
+  if (uses_s1(KIND)) st8f(static_cast<float*>(p.s1) + e0, s1, pol);
+  if (uses_s2(KIND)) st8f(static_cast<float*>(p.s2) + e0, s2, pol);
 }
 
 template <int KIND, int WDT>
 __device__ __forceinline__ void epi_fused_fp32state(uint32_t tbase, int64_t row, int colbase,
                                                     bool row_ok, const GemmParams& p) {
   const int64_t K = p.Ncols;
+  const uint64_t pol = evict_first_policy();
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     float g[32];
@@ -224,7 +254,7 @@ __device__ __forceinline__ void epi_fused_fp32state(uint32_t tbase, int64_t row,
     const int col0 = colbase + c * 32;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      if (col0 + q * 8 < K) group8_fp32state<KIND, WDT>(g + q * 8, row * K + col0 + q * 8, p);
+      if (col0 + q * 8 < K) group8_fp32state<KIND, WDT>(g + q * 8, row * K + col0 + q * 8, p, pol);
     }
   }
 }

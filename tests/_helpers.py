@@ -1,17 +1,21 @@
 """Shared test utilities: input construction, oracle/GPU adapters, tolerance checks.
 
-Tolerances ("Tolerances"):
-* quantities with an exact FP32 input (integer-grid data, oracle-supplied
-  gradients): bit-exact;
-* FP32 weights and moments from realistic data: |gpu - ref| <= 1e-7 + 1e-5 |ref|;
-* BF16 weights: <= 1 ULP on >= 99.9 % of elements and <= 2 ULP on every
-  element whose result is decided by the FP32 gradient, i.e. outside the set
-  where the oracle's gradient is within the FP32 summation error of a sign
-  change (the explainer's §2 "Exactness": the summation order is the only
-  difference, and near a sign change it decides the update);
-* INT8 codes: within one step; scales rtol 1e-5 (bit-exact when inputs agree);
-* dX (bf16): |gpu - exact| <= 1 bf16 ULP of the exact value plus the FP32
-  summation bound 2^-20 * sum_n |dY W|.
+Tolerances:
+* exact FP32 inputs (integer-grid data, oracle-supplied gradients): bit-exact;
+* realistic data, one step from a common state: an *interval oracle*.  The GPU
+  sums the T token products on the tensor cores in FP32 (T/16 accumulator
+  updates), the oracle in float64; the FORGE explainer's §2 "Exactness" names
+  the summation order as the only difference.  The oracle is evaluated at
+  g - d, g and g + d, where d bounds the tensor-core summation error per
+  element, and every GPU output must lie in the hull of the three results
+  widened by the base tolerance: FP32 values 1e-7 + 1e-5 |x|, BF16 weights one
+  ULP (stochastic rounding turns a sub-ULP difference into a whole ULP), INT8
+  codes one step.  In addition >= 99.9 % of BF16 weights must be within 1 ULP
+  of the central result;
+* free-running multi-step BF16 trajectories: >= 99.9 % within 1 ULP, all
+  within 2 ULP measured at the weight scale;
+* dX (bf16): |gpu - exact| <= 1 bf16 ULP of the exact value plus the same
+  summation bound over the N reduction terms.
 """
 
 import numpy as np
@@ -119,24 +123,25 @@ class Problem:
                 out[k] = torch.from_numpy(np.ascontiguousarray(st[k])).to(dev)
         return out
 
-    def per_step_from_common_state(self, check):
-        """Every step starts both sides from the oracle's state; `check(step,
-        gpu_state, oracle_state, sensitive_mask)` compares that step's outputs."""
+    def per_step_from_common_state(self):
+        """Every step starts both sides from the oracle's (central) state; the
+        GPU result of that step must lie in the oracle's interval."""
         from optimizer_tcgen05_dw_gb300 import api
         st = {k: v for k, v in self.state0.items()}
         hp = oracle_hparams(self.hp)
         for s in range(self.steps):
-            g = self.upload(st)
+            g_dev = self.upload(st)
             Xb, dYb = to_bits(self.X[s]), to_bits(self.dY[s])
-            api.forge_linear_bwd_step(self.X[s].cuda(), self.dY[s].cuda(), g["W"], self.opt,
-                                      self.hp, s + 1, self.seed, g.get("s1"), g.get("s2"),
-                                      g.get("s1_scale"), g.get("s2_scale"))
+            api.forge_linear_bwd_step(self.X[s].cuda(), self.dY[s].cuda(), g_dev["W"], self.opt,
+                                      self.hp, s + 1, self.seed, g_dev.get("s1"), g_dev.get("s2"),
+                                      g_dev.get("s1_scale"), g_dev.get("s2_scale"))
             api.forge_get_device_status()
-            sens = self.sensitive(Xb, dYb, st)
-            out = ls.linear_bwd_step(Xb, dYb, st, self.kind, hp, s + 1, self.seed, want_dx=False)
+            g = ls.weight_gradient(Xb, dYb)
+            outs = oracle_interval(self.kind, hp, s + 1, self.seed, g, st, self.w_dtype,
+                                   self.s_dtype, 0, 0, self.K, grad_error_bound(Xb, dYb))
+            assert_in_interval(g_dev, outs, self.w_dtype, self.s_dtype, f"step {s + 1}")
             st = dict(st)
-            st.update({k: out[k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale")})
-            check(s + 1, g, st, sens)
+            st.update({k: outs[0][k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale")})
         return st
 
     # ---- oracle side
@@ -252,7 +257,9 @@ def assert_dx_close(gpu_dx, dYb, Wb, what):
     dY = rounding.bf16_bits_to_f32(dYb).astype(np.float64)
     W = rounding.bf16_bits_to_f32(Wb).astype(np.float64)
     exact = dY @ W
-    bound = SUM_ERR * (np.abs(dY) @ np.abs(W))
+    n_red = W.shape[0]
+    bound = 2.0 ** -24 * (np.ceil(n_red / 16.0) * 3.0 * np.sqrt((dY * dY) @ (W * W)) +
+                          4.0 * np.abs(exact))
     a = rounding.bf16_bits_to_f32(gpu_np(gpu_dx)).astype(np.float64)
     ulp = np.maximum(np.abs(exact), 1e-38)
     ulp = 2.0 ** (np.floor(np.log2(ulp)) - 7)
@@ -260,3 +267,80 @@ def assert_dx_close(gpu_dx, dYb, Wb, what):
     bad = np.argwhere(~ok)
     assert bad.size == 0, f"{what}: {len(bad)} of {a.size} outside; first {bad[:3].tolist()}: " \
         f"gpu={a[tuple(bad[0])]} exact={exact[tuple(bad[0])]}"
+
+
+# ---------------------------------------------------------------- interval oracle
+
+def grad_error_bound(Xb, dYb):
+    """Per-element bound on |g_gpu - g_exact| for g = sum_t dY[t,n] X[t,k]:
+    ceil(T/16) FP32 accumulator updates, each off by at most one rounding of a
+    partial sum no larger than 3x the random-walk scale sqrt(sum_t (dY X)^2),
+    plus the final rounding of g."""
+    X = rounding.bf16_bits_to_f32(Xb).astype(np.float64)
+    dY = rounding.bf16_bits_to_f32(dYb).astype(np.float64)
+    T = X.shape[0]
+    rw = np.sqrt((dY * dY).T @ (X * X))
+    g = dY.T @ X
+    return 2.0 ** -24 * (np.ceil(T / 16.0) * 3.0 * rw + 4.0 * np.abs(g)) + 1e-30
+
+
+def oracle_interval(kind, hp, step, seed, g, st_block, w_dtype, s_dtype, n0, k0, K, delta):
+    """Oracle results at g - delta, g, g + delta for one block of W."""
+    outs = []
+    for sgn in (0.0, -1.0, 1.0):
+        gg = (g.astype(np.float64) + sgn * delta).astype(np.float32)
+        outs.append(ls.update_block(kind, hp, step, seed, gg, st_block["W"], w_dtype,
+                                    st_block.get("s1"), st_block.get("s2"),
+                                    st_block.get("s1_scale"), st_block.get("s2_scale"),
+                                    s_dtype, n0, k0, K))
+    return outs
+
+
+def _hull(vals):
+    v = np.stack([np.asarray(x, dtype=np.float64) for x in vals])
+    return v.min(axis=0), v.max(axis=0)
+
+
+def assert_in_interval(gpu_state, outs, w_dtype, s_dtype, what):
+    """GPU outputs inside the hull of the oracle's interval results, widened
+    by the base tolerance (see module docstring)."""
+    central = outs[0]
+    # weights
+    a = gpu_np(gpu_state["W"])
+    if w_dtype == "bf16":
+        assert_bf16_close(gpu_state["W"], central["W"], what + " W (central)")
+        lo, hi = _hull([rounding.bf16_bits_to_f32(o["W"]) for o in outs])
+        af = rounding.bf16_bits_to_f32(a).astype(np.float64)
+        slack_lo, slack_hi = _ulp_at(np.abs(lo)), _ulp_at(np.abs(hi))
+        ok = (af >= lo - slack_lo) & (af <= hi + slack_hi)
+    else:
+        lo, hi = _hull([o["W"] for o in outs])
+        af = a.astype(np.float64)
+        ok = (af >= lo - (1e-7 + 1e-5 * np.abs(lo))) & (af <= hi + (1e-7 + 1e-5 * np.abs(hi)))
+    bad = np.argwhere(~ok)
+    assert bad.size == 0, f"{what} W: {len(bad)} of {a.size} outside the interval; first " \
+        f"{bad[:3].tolist()}: gpu={af[tuple(bad[0])]} interval=[{lo[tuple(bad[0])]}, {hi[tuple(bad[0])]}]"
+    # states
+    for key, signed in (("s1", True), ("s2", False)):
+        if central.get(key) is None:
+            continue
+        g = gpu_np(gpu_state[key])
+        if s_dtype == "int8":
+            lo, hi = _hull([o[key].astype(np.int64) for o in outs])
+            gi = g.astype(np.int64)
+            ok = (gi >= lo - 1) & (gi <= hi + 1)
+            bad = np.argwhere(~ok)
+            assert bad.size == 0, f"{what} {key}: {len(bad)} codes outside the interval"
+            slo, shi = _hull([o[key + "_scale"] for o in outs])
+            gs = gpu_np(gpu_state[key + "_scale"]).astype(np.float64)
+            ok = (gs >= slo * (1 - 1e-5) - 1e-30) & (gs <= shi * (1 + 1e-5) + 1e-30)
+            bad = np.argwhere(~ok)
+            assert bad.size == 0, f"{what} {key} scale: {len(bad)} outside the interval; first " \
+                f"{bad[:3].tolist()}: gpu={gs[tuple(bad[0])]} [{slo[tuple(bad[0])]}, {shi[tuple(bad[0])]}]"
+        else:
+            lo, hi = _hull([o[key] for o in outs])
+            gf = g.astype(np.float64)
+            ok = (gf >= lo - (1e-7 + 1e-5 * np.abs(lo))) & (gf <= hi + (1e-7 + 1e-5 * np.abs(hi)))
+            bad = np.argwhere(~ok)
+            assert bad.size == 0, f"{what} {key}: {len(bad)} of {g.size} outside the interval; first " \
+                f"{bad[:3].tolist()}: gpu={gf[tuple(bad[0])]} [{lo[tuple(bad[0])]}, {hi[tuple(bad[0])]}]"

@@ -2,10 +2,12 @@
 
 The oracle cannot form dW for a whole Llama/Qwen layer at T = 16384 in a test,
 but every element's update depends only on its own coordinate (FORGE
-explainer, Technical Summary §2 "Exactness"), so it follows a set of sampled
-128 x 128 tiles (the four corners plus random interior tiles) through every
-step from the same initial state and seeded inputs, and those tiles of the
-GPU result are compared with it.
+explainer, Technical Summary §2 "Exactness").  So it follows a set of sampled
+128 x 128 tiles (the four corners plus random interior tiles).  Before every
+step those tiles of the GPU state are set to the oracle's state, the full
+layer is stepped on the GPU, and the sampled tiles must lie in the oracle's
+interval for that step (tests/_helpers.py: the oracle evaluated at g - d, g,
+g + d with d the tensor-core summation bound).
 """
 
 import numpy as np
@@ -18,12 +20,12 @@ from oracle import quant, rounding
 from optimizer_tcgen05_dw_gb300 import api, inputs
 from optimizer_tcgen05_dw_gb300.build import build
 
-from _helpers import (SUM_ERR, assert_bf16_close, assert_fp32_close, assert_int8_close,
-                      oracle_hparams, to_bits)
+from _helpers import assert_in_interval, grad_error_bound, oracle_hparams, to_bits
 
 pytestmark = pytest.mark.gpu
 
 TILE = 128
+KEYS = ("W", "s1", "s2", "s1_scale", "s2_scale")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -44,14 +46,24 @@ def _tiles(N, K, count, seed):
     return sorted((a * TILE, b * TILE) for a, b in picks)
 
 
+def _region(key, n0, k0):
+    blk = 64 if key.endswith("scale") else 1
+    return slice(n0, n0 + TILE), slice(k0 // blk, (k0 + TILE) // blk)
+
+
+def _to_dev(key, arr, w_dtype):
+    if key == "W" and w_dtype == "bf16":
+        return inputs.bits_to_bf16(arr)
+    return torch.from_numpy(np.ascontiguousarray(arr))
+
+
 def run_sampled(N, K, T, w_dtype, s_dtype, opt_name, hp, steps, seed, m_std=0.0, v_std=0.0,
                 x_std=1.0, dy_std=1e-3, n_tiles=12):
     kind = opt.NAMES.index(opt_name)
     tiles = _tiles(N, K, n_tiles, seed)
     # initial state, drawn on the CPU from seeds; INT8 codes from the oracle quantiser
     W = inputs.normal((N, K), 0.02, inputs.layer_seed(seed, 0, 0, 3), torch.float32)
-    st = {"w_dtype": w_dtype, "s_dtype": s_dtype,
-          "W": W.numpy() if w_dtype == "fp32" else rounding.bf16_bits_rne(W.numpy())}
+    st = {"W": W.numpy() if w_dtype == "fp32" else rounding.bf16_bits_rne(W.numpy())}
     del W
     if opt.USES_S1[kind]:
         m = inputs.normal((N, K), m_std, inputs.layer_seed(seed, 0, 0, 4), torch.float32).numpy()
@@ -65,60 +77,35 @@ def run_sampled(N, K, T, w_dtype, s_dtype, opt_name, hp, steps, seed, m_std=0.0,
             st["s2"], st["s2_scale"] = quant.quantize_blocks(v, False)
         else:
             st["s2"] = v
-    gpu = {"W": (torch.from_numpy(st["W"]) if w_dtype == "fp32"
-                 else inputs.bits_to_bf16(st["W"])).cuda()}
-    for k in ("s1", "s2", "s1_scale", "s2_scale"):
-        if st.get(k) is not None:
-            gpu[k] = torch.from_numpy(np.ascontiguousarray(st[k])).cuda()
-    # per-tile oracle state
-    def cut(a, n0, k0, block=1):
-        return None if a is None else np.ascontiguousarray(
-            a[n0:n0 + TILE, k0 // block:(k0 + TILE) // block])
-    ost = {t: {k: cut(st.get(k), *t, 64 if k.endswith("scale") else 1)
-               for k in ("W", "s1", "s2", "s1_scale", "s2_scale")} for t in tiles}
-    sens = {t: np.zeros((TILE, TILE), dtype=bool) for t in tiles}
+    gpu = {k: _to_dev(k, st[k], w_dtype).cuda() for k in KEYS if st.get(k) is not None}
+    ost = {t: {k: np.ascontiguousarray(st[k][_region(k, *t)]) for k in KEYS if st.get(k) is not None}
+           for t in tiles}
+    del st
     ohp = oracle_hparams(hp)
     for s in range(steps):
+        # sampled tiles of the GPU state := the oracle's state
+        for t, o in ost.items():
+            for k, arr in o.items():
+                gpu[k][_region(k, *t)] = _to_dev(k, arr, w_dtype).cuda()
         X = inputs.normal((T, K), x_std, inputs.layer_seed(seed, 0, s, 1), device="cuda")
         dY = inputs.normal((T, N), dy_std, inputs.layer_seed(seed, 0, s, 2), device="cuda")
         api.forge_linear_bwd_step(X, dY, gpu["W"], opt_name, hp, s + 1, seed, gpu.get("s1"),
                                   gpu.get("s2"), gpu.get("s1_scale"), gpu.get("s2_scale"))
-        cols = sorted({k0 for _, k0 in tiles})
-        rows = sorted({n0 for n0, _ in tiles})
-        Xc = {k0: to_bits(X[:, k0:k0 + TILE].contiguous()) for k0 in cols}
-        dYc = {n0: to_bits(dY[:, n0:n0 + TILE].contiguous()) for n0 in rows}
+        api.forge_get_device_status()
+        Xc = {k0: to_bits(X[:, k0:k0 + TILE].contiguous()) for k0 in {k0 for _, k0 in tiles}}
+        dYc = {n0: to_bits(dY[:, n0:n0 + TILE].contiguous()) for n0 in {n0 for n0, _ in tiles}}
         del X, dY
         for (n0, k0) in tiles:
             g = ls.weight_gradient(Xc[k0], dYc[n0])
-            Xf = rounding.bf16_bits_to_f32(Xc[k0]).astype(np.float64)
-            dYf = rounding.bf16_bits_to_f32(dYc[n0]).astype(np.float64)
-            bound = SUM_ERR * (np.abs(dYf).T @ np.abs(Xf))
-            sens[(n0, k0)] |= np.abs(g.astype(np.float64)) <= bound
             o = ost[(n0, k0)]
-            out = ls.update_block(kind, ohp, s + 1, seed, g, o["W"], w_dtype, o["s1"], o["s2"],
-                                  o["s1_scale"], o["s2_scale"], s_dtype, n0, k0, K)
-            o.update({k: out[k] for k in o})
-    api.forge_get_device_status()
-    torch.cuda.synchronize()
-    frac_sens = np.mean([m.mean() for m in sens.values()])
-    assert frac_sens < 1e-3
-    for (n0, k0) in tiles:
-        o, ex = ost[(n0, k0)], sens[(n0, k0)]
-        gw = gpu["W"][n0:n0 + TILE, k0:k0 + TILE].contiguous()
-        where = f"tile ({n0},{k0})"
-        if w_dtype == "bf16":
-            assert_bf16_close(gw, o["W"], "W " + where, exclude=ex, free_running=steps > 1)
-        else:
-            assert_fp32_close(gw, o["W"], "W " + where, exclude=ex)
-        for k in ("s1", "s2"):
-            if o[k] is None:
-                continue
-            gs = gpu[k][n0:n0 + TILE, k0:k0 + TILE].contiguous()
-            if s_dtype == "int8":
-                gsc = gpu[k + "_scale"][n0:n0 + TILE, k0 // 64:(k0 + TILE) // 64].contiguous()
-                assert_int8_close(gs, gsc, o[k], o[k + "_scale"], f"{k} {where}", exclude=ex)
-            else:
-                assert_fp32_close(gs, o[k], f"{k} {where}", exclude=ex)
+            outs = [ls.update_block(kind, ohp, s + 1, seed,
+                                    (g.astype(np.float64) + sg * grad_error_bound(Xc[k0], dYc[n0])).astype(np.float32),
+                                    o["W"], w_dtype, o.get("s1"), o.get("s2"), o.get("s1_scale"),
+                                    o.get("s2_scale"), s_dtype, n0, k0, K)
+                    for sg in (0.0, -1.0, 1.0)]
+            got = {k: gpu[k][_region(k, n0, k0)].contiguous() for k in o}
+            assert_in_interval(got, outs, w_dtype, s_dtype, f"step {s + 1} tile ({n0},{k0})")
+            ost[(n0, k0)] = {k: outs[0][k] for k in o}
 
 
 LLAMA = {n: (N, K) for n, N, K in inputs.LLAMA31_8B_LINEARS}
