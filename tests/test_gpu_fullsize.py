@@ -20,7 +20,8 @@ from oracle import quant, rounding
 from optimizer_tcgen05_dw_gb300 import api, inputs
 from optimizer_tcgen05_dw_gb300.build import build
 
-from _helpers import assert_in_interval, grad_error_bound, oracle_hparams, to_bits
+from _helpers import (assert_in_interval, grad_error_bound, oracle_hparams, oracle_interval,
+                      to_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -98,14 +99,11 @@ def run_sampled(N, K, T, w_dtype, s_dtype, opt_name, hp, steps, seed, m_std=0.0,
         for (n0, k0) in tiles:
             g = ls.weight_gradient(Xc[k0], dYc[n0])
             o = ost[(n0, k0)]
-            outs = [ls.update_block(kind, ohp, s + 1, seed,
-                                    (g.astype(np.float64) + sg * grad_error_bound(Xc[k0], dYc[n0])).astype(np.float32),
-                                    o["W"], w_dtype, o.get("s1"), o.get("s2"), o.get("s1_scale"),
-                                    o.get("s2_scale"), s_dtype, n0, k0, K)
-                    for sg in (0.0, -1.0, 1.0)]
+            iv = oracle_interval(kind, ohp, s + 1, seed, g, o, w_dtype, s_dtype, n0, k0, K,
+                                 grad_error_bound(Xc[k0], dYc[n0]))
             got = {k: gpu[k][_region(k, n0, k0)].contiguous() for k in o}
-            assert_in_interval(got, outs, w_dtype, s_dtype, f"step {s + 1} tile ({n0},{k0})")
-            ost[(n0, k0)] = {k: outs[0][k] for k in o}
+            assert_in_interval(got, iv, w_dtype, s_dtype, f"step {s + 1} tile ({n0},{k0})")
+            ost[(n0, k0)] = {k: iv[0][0][k] for k in o}
 
 
 LLAMA = {n: (N, K) for n, N, K in inputs.LLAMA31_8B_LINEARS}
