@@ -103,23 +103,99 @@ forge_status_t encode_fn(EncodeFn* fn) {
   return FORGE_OK;
 }
 
-// A 2-D bf16 row-major tensor [outer x inner] and a box of box_outer rows of
-// box_inner (64) elements, 128-byte swizzled; out-of-range elements read 0.
-forge_status_t bf16_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer,
-                        uint32_t box_inner, uint32_t box_outer) {
+// A 2-D row-major tensor [outer x inner] of `esize`-byte elements, read and
+// written in boxes of box_outer rows x box_inner elements with the given
+// shared-memory swizzle; out-of-range elements read as 0 and are not written.
+forge_status_t tensor_map(CUtensorMap* m, const void* base, CUtensorMapDataType dtype, int esize,
+                          int64_t inner, int64_t outer, uint32_t box_inner, uint32_t box_outer,
+                          CUtensorMapSwizzle swizzle) {
   EncodeFn fn;
   forge_status_t st = encode_fn(&fn);
   if (st != FORGE_OK) return st;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(inner) * static_cast<cuuint64_t>(esize)};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(FORGE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for [%lld x %lld]", static_cast<int>(r),
                 static_cast<long long>(outer), static_cast<long long>(inner));
+  return FORGE_OK;
+}
+
+// An MN-major GEMM operand stored [rows x cols] (bf16, cols % 64 == 0) seen as
+// a 3-D tensor (64 columns, rows, cols/64 column blocks), so one box of
+// {64, box_rows, blocks} lands in shared memory as `blocks` consecutive
+// 128-byte-swizzled atoms of box_rows x 64: a whole stage operand per copy.
+forge_status_t mn_major_3d_map(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
+                               uint32_t box_rows, uint32_t blocks) {
+  EncodeFn fn;
+  forge_status_t st = encode_fn(&fn);
+  if (st != FORGE_OK) return st;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, blocks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(FORGE_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d) for [%lld x %lld]",
+                static_cast<int>(r), static_cast<long long>(rows), static_cast<long long>(cols));
+  return FORGE_OK;
+}
+
+// The weight-gradient operands dY [T x N] (A, 128 columns per tile) and
+// X [T x K] (B, 256 columns per tile): 3-D single-copy maps when N and K are
+// multiples of 64, else 2-D maps of one 64-column block per copy.
+forge_status_t wgrad_maps(const forge_linear_t* lin, int bk, CUtensorMap* ma, CUtensorMap* mb,
+                          int32_t* op3d);
+
+// GEMM operands: bf16, 64-element (128-byte) rows, 128-byte swizzle.
+forge_status_t bf16_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer,
+                        uint32_t box_inner, uint32_t box_outer) {
+  return tensor_map(m, base, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, box_inner, box_outer,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+forge_status_t wgrad_maps(const forge_linear_t* lin, int bk, CUtensorMap* ma, CUtensorMap* mb,
+                          int32_t* op3d) {
+  forge_status_t st;
+  if (lin->N % 64 == 0 && lin->K % 64 == 0) {
+    *op3d = 1;
+    if ((st = mn_major_3d_map(ma, lin->dY, lin->N, lin->T, bk, kTileM / 64)) != FORGE_OK) return st;
+    return mn_major_3d_map(mb, lin->X, lin->K, lin->T, bk, kTileN / 64);
+  }
+  *op3d = 0;
+  if ((st = bf16_map(ma, lin->dY, lin->N, lin->T, 64, bk)) != FORGE_OK) return st;
+  return bf16_map(mb, lin->X, lin->K, lin->T, 64, bk);
+}
+
+// Maps of the weight / state tiles the bf16-weight epilogue stages through
+// shared memory: W in 32-column boxes (64-byte rows, 64-byte swizzle), fp32
+// states in 32-column boxes (128-byte rows, 128-byte swizzle), INT8 codes in
+// 64-column boxes (64-byte rows, 64-byte swizzle); 128 rows each.
+forge_status_t epilogue_maps(const forge_state_t* st, int kind, int64_t N, int64_t K, CUtensorMap* mw,
+                             CUtensorMap* m1, CUtensorMap* m2) {
+  forge_status_t r = tensor_map(mw, st->W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 32, kTileM,
+                                CU_TENSOR_MAP_SWIZZLE_64B);
+  if (r != FORGE_OK) return r;
+  *m1 = *mw;
+  *m2 = *mw;
+  const bool int8 = st->s_dtype == FORGE_STATE_INT8_B64;
+  const void* bufs[2] = {st->s1, st->s2};
+  const bool used[2] = {uses_s1(kind), uses_s2(kind)};
+  CUtensorMap* maps[2] = {m1, m2};
+  for (int i = 0; i < 2; ++i) {
+    if (!used[i]) continue;
+    r = int8 ? tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, 64, kTileM,
+                          CU_TENSOR_MAP_SWIZZLE_64B)
+             : tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, K, N, 32, kTileM,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+    if (r != FORGE_OK) return r;
+  }
   return FORGE_OK;
 }
 
@@ -248,10 +324,10 @@ forge_status_t check_hp(int32_t kind, const forge_hparams_t* hp, int64_t step) {
   return FORGE_OK;
 }
 
-void fill_tiles(GemmParams& p, int64_t M, int64_t Ncols, int64_t red) {
+void fill_tiles(GemmParams& p, int64_t M, int64_t Ncols, int64_t red, int bk = kBlockK) {
   p.M = static_cast<int32_t>(M);
   p.Ncols = static_cast<int32_t>(Ncols);
-  p.num_kb = static_cast<int32_t>((red + kBlockK - 1) / kBlockK);
+  p.num_kb = static_cast<int32_t>((red + bk - 1) / bk);
   p.tiles_m = static_cast<int32_t>((M + kTileM - 1) / kTileM);
   p.tiles_n = static_cast<int32_t>((Ncols + kTileN - 1) / kTileN);
   p.num_tiles = p.tiles_m * p.tiles_n;
@@ -279,9 +355,14 @@ forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_
   CUtensorMap ma, mb;
   forge_status_t st;
   if ((st = bf16_map(&ma, lin->dY, N, T, 64, kTileM)) != FORGE_OK) return st;
-  if ((st = bf16_map(&mb, W, K, N, 64, kBlockK)) != FORGE_OK) return st;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
+  if (K % 64 == 0) {
+    p.op3d = 1;
+    if ((st = mn_major_3d_map(&mb, W, K, N, kBlockK, kTileN / 64)) != FORGE_OK) return st;
+  } else if ((st = bf16_map(&mb, W, K, N, 64, kBlockK)) != FORGE_OK) {
+    return st;
+  }
   fill_tiles(p, T, K, N);
   p.out = lin->dX;
   p.status = d.status;
@@ -334,12 +415,12 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
     return FORGE_OK;
   }
   // 2. the fused weight-gradient + optimizer pass.
+  const int bk = state->w_dtype == FORGE_W_BF16_SR ? kFusedBlockK : kBlockK;
   CUtensorMap ma, mb;
-  if ((st = bf16_map(&ma, lin->dY, lin->N, lin->T, 64, kBlockK)) != FORGE_OK) return st;
-  if ((st = bf16_map(&mb, lin->X, lin->K, lin->T, 64, kBlockK)) != FORGE_OK) return st;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
-  fill_tiles(p, lin->N, lin->K, lin->T);
+  if ((st = wgrad_maps(lin, bk, &ma, &mb, &p.op3d)) != FORGE_OK) return st;
+  fill_tiles(p, lin->N, lin->K, lin->T, bk);
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
@@ -348,7 +429,12 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
-  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, p, grid_for(p, d), s)) != cudaSuccess)
+  CUtensorMap mw = ma, m1 = ma, m2 = ma;
+  if (state->w_dtype == FORGE_W_BF16_SR &&
+      (st = epilogue_maps(state, opt_kind, lin->N, lin->K, &mw, &m1, &m2)) != FORGE_OK)
+    return st;
+  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, mw, m1, m2, p, grid_for(p, d), s)) !=
+      cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
 }
@@ -384,11 +470,10 @@ forge_status_t forge_unfused_wgrad(const forge_linear_t* lin, float* dW, void* s
     return FORGE_OK;
   }
   CUtensorMap ma, mb;
-  if ((st = bf16_map(&ma, lin->dY, lin->N, lin->T, 64, kBlockK)) != FORGE_OK) return st;
-  if ((st = bf16_map(&mb, lin->X, lin->K, lin->T, 64, kBlockK)) != FORGE_OK) return st;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
-  fill_tiles(p, lin->N, lin->K, lin->T);
+  if ((st = wgrad_maps(lin, kWgradBlockK, &ma, &mb, &p.op3d)) != FORGE_OK) return st;
+  fill_tiles(p, lin->N, lin->K, lin->T, kWgradBlockK);
   p.out = dW;
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();

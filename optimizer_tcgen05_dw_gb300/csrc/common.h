@@ -51,10 +51,29 @@ constexpr int kStages = 4;
 constexpr int kABytes = kTileM * kBlockK * 2;            // 16 KiB
 constexpr int kBBytes = kTileN * kBlockK * 2;            // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;           // 48 KiB
+// The FORGE step with bf16 weights streams its operands in 48-token stages
+// (36 KiB, four of them: 144 KiB), leaving 80 KiB for the staged epilogue.
+// Measured on GB300: four 48-token stages beat three 64-token or six
+// 32-token stages of the same ring size.
+#ifndef FORGE_FUSED_BK
+#define FORGE_FUSED_BK 48
+#endif
+#ifndef FORGE_FUSED_STAGES
+#define FORGE_FUSED_STAGES 4
+#endif
+#ifndef FORGE_WGRAD_BK
+#define FORGE_WGRAD_BK 64
+#endif
+#ifndef FORGE_WGRAD_STAGES
+#define FORGE_WGRAD_STAGES 4
+#endif
+constexpr int kFusedBlockK = FORGE_FUSED_BK;
+constexpr int kWgradBlockK = FORGE_WGRAD_BK;      // unfused weight-gradient pass
+constexpr int kWgradStages = FORGE_WGRAD_STAGES;
+constexpr int kFusedStages = FORGE_FUSED_STAGES;
 constexpr int kNumEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kNumEpiWarps);        // TMA warp, MMA warp, 8 epilogue warps
 constexpr int kTmemCols = 2 * kTileN;                    // double-buffered fp32 accumulator
-constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*barriers*/ + 1024 /*alignment*/;
 
 enum GemmMode : int32_t {
   kModeFusedOpt = 0,   // dW tile -> optimizer epilogue (the FORGE step)
@@ -79,6 +98,7 @@ struct GemmParams {
   uint64_t step;
   uint64_t wait_limit_ns;
   uint32_t* status;          // device status word (first error wins)
+  int32_t op3d;              // MN-major operands described as 3-D maps: one load per stage
   int32_t skip_loads;
 };
 

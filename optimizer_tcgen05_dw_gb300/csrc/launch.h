@@ -24,7 +24,11 @@ struct ElemParams {
 };
 
 // tc_fused.cu: the FORGE step (mode kModeFusedOpt) for one (W dtype, state dtype).
+// w, s1, s2: tensor maps of the weight / state tiles the bf16-weight epilogue
+// stages through shared memory (unused, any valid map, for fp32 weights or
+// for states the rule does not keep).
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
+                            const CUtensorMap& w, const CUtensorMap& s1, const CUtensorMap& s2,
                             const GemmParams& p, int grid, cudaStream_t s);
 // tc_plain.cu: unfused pass 1 (kModeWgradStore) or dX (kModeDgrad).
 cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,

@@ -40,14 +40,41 @@
 namespace forge {
 
 struct SharedState {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[8];
+  uint64_t empty[8];
   uint64_t tmem_full[2];
   uint64_t tmem_empty[2];
   uint64_t mma_done;
+  uint64_t epi_full[2];     // staged epilogue chunk landed (TMA epilogue only)
   uint32_t tmem_base;
   int32_t abort;
 };
+
+// Per-instantiation layout.  The FORGE step with bf16 weights stages its
+// weight/state tiles through shared memory with TMA (two 40 KiB chunk
+// buffers), which leaves room for a 3-stage operand ring; the other modes
+// keep 4 stages.
+constexpr int kEpiBufBytes = 40960;
+constexpr int kEpiThreads = 32 * kNumEpiWarps;
+constexpr int kEpiBarrier = 1;  // named barrier of the epilogue warps
+
+template <int MODE, int WDT>
+struct KCfg {
+  static constexpr bool kTmaEpi = (MODE == kModeFusedOpt && WDT == kWBf16);
+  static constexpr int kBK =
+      kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK);  // tokens per stage
+  static constexpr int kStg =
+      kTmaEpi ? kFusedStages : (MODE == kModeWgradStore ? kWgradStages : kStages);
+  static constexpr int kA = kTileM * kBK * 2;                     // bytes of A per stage
+  static constexpr int kB = kTileN * kBK * 2;
+  static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBufBytes : 0;
+  static constexpr int kSmem = kStg * (kA + kB) + kEpiBytes + 512 + 1024;
+};
+static_assert(sizeof(SharedState) <= 512, "shared state region");
+static_assert(KCfg<kModeFusedOpt, kWBf16>::kStg <= 8 && KCfg<kModeWgradStore, kWBf16>::kStg <= 8 &&
+                  kStages <= 8, "barrier arrays");
+static_assert(KCfg<kModeWgradStore, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeFusedOpt, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -84,7 +111,7 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
 
 // ------------------------------------------------------------------ roles
 
-template <int MODE>
+template <int MODE, int STG, int BK>
 __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, const GemmParams& p,
                               uint8_t* smA, uint8_t* smB, SharedState* ss) {
   uint32_t it = 0;
@@ -96,21 +123,27 @@ __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, cons
       tile_coords(tile, p, tm, tn);
       const int m0 = tm * kTileM, n0 = tn * kTileN;
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const int s = static_cast<int>(it % kStages);
-        const uint32_t ph = (it / kStages) & 1u;
+        const int s = static_cast<int>(it % STG);
+        const uint32_t ph = (it / STG) & 1u;
         if (!bounded_wait(&ss->empty[s], ph ^ 1u, p, ss)) goto drain;
-        ptx::mbar_arrive_expect_tx(&ss->full[s], kStageBytes);
-        uint8_t* a = smA + s * kABytes;
-        uint8_t* b = smB + s * kBBytes;
+        ptx::mbar_arrive_expect_tx(&ss->full[s], (kTileM + kTileN) * BK * 2);
+        uint8_t* a = smA + s * (kTileM * BK * 2);
+        uint8_t* b = smB + s * (kTileN * BK * 2);
         if (MODE == kModeDgrad) {
-          ptx::tma_load_2d(mA, &ss->full[s], a, kb * kBlockK, m0);
+          ptx::tma_load_2d(mA, &ss->full[s], a, kb * BK, m0);
+        } else if (p.op3d) {  // [2 column blocks][BK rows][64 columns] in one copy
+          ptx::tma_load_3d(mA, &ss->full[s], a, 0, kb * BK, m0 / 64);
         } else {
-          ptx::tma_load_2d(mA, &ss->full[s], a, m0, kb * kBlockK);
-          ptx::tma_load_2d(mA, &ss->full[s], a + 8192, m0 + 64, kb * kBlockK);
+          ptx::tma_load_2d(mA, &ss->full[s], a, m0, kb * BK);
+          ptx::tma_load_2d(mA, &ss->full[s], a + 64 * BK * 2, m0 + 64, kb * BK);
         }
+        if (p.op3d) {
+          ptx::tma_load_3d(mB, &ss->full[s], b, 0, kb * BK, n0 / 64);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          ptx::tma_load_2d(mB, &ss->full[s], b + j * 8192, n0 + 64 * j, kb * kBlockK);
+          for (int j = 0; j < 4; ++j)
+            ptx::tma_load_2d(mB, &ss->full[s], b + j * (64 * BK * 2), n0 + 64 * j, kb * BK);
+        }
         issued_mask |= 1u << s;
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
       }
@@ -119,11 +152,11 @@ __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, cons
 drain:
   // Every issued copy lands before the CTA can exit (already true unless a
   // consumer gave up early).
-  for (int s = 0; s < kStages; ++s)
+  for (int s = 0; s < STG; ++s)
     if (issued_mask & (1u << s)) bounded_wait(&ss->full[s], (last_parity >> s) & 1u, p, ss, false);
 }
 
-template <int MODE>
+template <int MODE, int STG, int BK>
 __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, SharedState* ss) {
   constexpr uint32_t kIdesc =
       ptx::idesc_bf16_f32(kTileM, kTileN, /*a_mn=*/MODE != kModeDgrad, /*b_mn=*/true);
@@ -137,20 +170,21 @@ __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, Shared
     {
       const uint32_t d_tmem = ss->tmem_base + static_cast<uint32_t>(acc * kTileN);
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const int s = static_cast<int>(it % kStages);
-        const uint32_t ph = (it / kStages) & 1u;
+        const int s = static_cast<int>(it % STG);
+        const uint32_t ph = (it / STG) & 1u;
         if (!bounded_wait(&ss->full[s], ph, p, ss)) goto done;
         ptx::tc_fence_after();
-        const uint32_t a0 = ptx::smem_addr(smA + s * kABytes);
-        const uint32_t b0 = ptx::smem_addr(smB + s * kBBytes);
+        const uint32_t a0 = ptx::smem_addr(smA + s * (kTileM * BK * 2));
+        const uint32_t b0 = ptx::smem_addr(smB + s * (kTileN * BK * 2));
 #pragma unroll
-        for (int kk = 0; kk < kBlockK / 16; ++kk) {
+        for (int kk = 0; kk < BK / 16; ++kk) {
           // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB.
           // K-major: 16 bf16 = 32 B inside the 128-byte swizzle row.
+          // MN-major atoms of 64 columns x BK rows sit BK*128 bytes apart (LBO).
           const uint64_t adesc = (MODE == kModeDgrad)
                                      ? ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024)
-                                     : ptx::smem_desc_sw128(a0 + kk * 2048, 8192, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(b0 + kk * 2048, 8192, 1024);
+                                     : ptx::smem_desc_sw128(a0 + kk * 2048, BK * 128, 1024);
+          const uint64_t bdesc = ptx::smem_desc_sw128(b0 + kk * 2048, BK * 128, 1024);
           ptx::mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
         }
         ptx::mma_commit(&ss->empty[s]);  // frees the stage once these MMAs finish
@@ -504,29 +538,314 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
   }
 }
 
+// ------------------------------------------------------------------ TMA-staged epilogue
+
+// Byte offset of 16-byte chunk c of row r in a box of 64-byte rows stored with
+// the 64-byte swizzle, and of 128-byte rows with the 128-byte swizzle (the
+// layouts the tensor-memory accelerator writes).  Eight consecutive rows
+// reading the same logical chunk hit eight different bank groups.
+__device__ __forceinline__ uint32_t sw64(int r, int c) {
+  return static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void unpack_bf16x8(uint4 v, float* w) {
+  const uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    w[2 * j] = dev::bf16_to_f32(a[j] & 0xFFFFu);
+    w[2 * j + 1] = dev::bf16_to_f32(a[j] >> 16);
+  }
+}
+
+__device__ __forceinline__ uint4 pack_sr_bf16x8(const float* w, uint4 rnd) {
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(rnd, 2 * j)) |
+           (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(rnd, 2 * j + 1)) << 16);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// fp32 states: a chunk is 128 rows x 32 columns (W 8 KiB, m and v 16 KiB
+// each); this thread owns 16 columns of row r, starting at element e0.
+template <int KIND>
+__device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int r, int half,
+                                               int64_t e0, const GemmParams& p) {
+  constexpr int kOffS1 = 8192, kOffS2 = 24576;
+  float g[16], w[16], s1[16], s2[16];
+  ptx::tmem_ld_32x32b_x16(taddr, g);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + sw64(r, 2 * half + i)), w + 8 * i);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (uses_s1(KIND)) {
+      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS1 + sw128(r, 4 * half + i));
+      s1[4 * i] = x.x; s1[4 * i + 1] = x.y; s1[4 * i + 2] = x.z; s1[4 * i + 3] = x.w;
+    } else {
+      s1[4 * i] = s1[4 * i + 1] = s1[4 * i + 2] = s1[4 * i + 3] = 0.f;
+    }
+    if (uses_s2(KIND)) {
+      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS2 + sw128(r, 4 * half + i));
+      s2[4 * i] = x.x; s2[4 * i + 1] = x.y; s2[4 * i + 2] = x.z; s2[4 * i + 3] = x.w;
+    } else {
+      s2[4 * i] = s2[4 * i + 1] = s2[4 * i + 2] = s2[4 * i + 3] = 0.f;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 rnd = dev::sr_words((static_cast<uint64_t>(e0) >> 3) + i, p.seed, p.step);
+    *reinterpret_cast<uint4*>(buf + sw64(r, 2 * half + i)) = pack_sr_bf16x8(w + 8 * i, rnd);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (uses_s1(KIND))
+      *reinterpret_cast<float4*>(buf + kOffS1 + sw128(r, 4 * half + i)) =
+          make_float4(s1[4 * i], s1[4 * i + 1], s1[4 * i + 2], s1[4 * i + 3]);
+    if (uses_s2(KIND))
+      *reinterpret_cast<float4*>(buf + kOffS2 + sw128(r, 4 * half + i)) =
+          make_float4(s2[4 * i], s2[4 * i + 1], s2[4 * i + 2], s2[4 * i + 3]);
+  }
+}
+
+// INT8 states: a chunk is 128 rows x 64 columns (one code block per row; W
+// in two 32-column boxes, codes 8 KiB per state); this thread owns 32
+// columns (half a block) of row r.  The new block absmax combines the two
+// halves through shared memory; the weights use the new float32 moments,
+// then the moments are quantised with the new absmax.
+template <int KIND>
+__device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int r, int half,
+                                               int64_t e0, float a1, float a2, float* n1_out,
+                                               float* n2_out, const GemmParams& p) {
+  constexpr int kOffS1 = 16384, kOffS2 = 24576, kOffAmax = 32768;
+  float m[32], v[32];  // new float32 moments, kept for the requantisation
+  uint8_t* wbox = buf + half * 8192;
+  float n1 = 0.f, n2 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // 16 columns at a time
+    float g[16], w[16];
+    ptx::tmem_ld_32x32b_x16(taddr + 16 * i, g);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(wbox + sw64(r, 2 * i)), w);
+    unpack_bf16x8(*reinterpret_cast<const uint4*>(wbox + sw64(r, 2 * i + 1)), w + 8);
+    const uint4 c1 = uses_s1(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, 2 * half + i))
+                                   : make_uint4(0, 0, 0, 0);
+    const uint4 c2 = uses_s2(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, 2 * half + i))
+                                   : make_uint4(0, 0, 0, 0);
+    const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t b1 = (q1[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      const uint32_t b2 = (q2[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      float mj = uses_s1(KIND) ? dev::dequant<true>(static_cast<int>(static_cast<int8_t>(b1)), a1) : 0.f;
+      float vj = uses_s2(KIND) ? dev::dequant<false>(static_cast<int>(b2), a2) : 0.f;
+      dev::rule<KIND>(w[j], g[j], mj, vj, p.sc);
+      if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, mj);
+      if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, vj);
+      m[16 * i + j] = mj;
+      v[16 * i + j] = vj;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 rnd = dev::sr_words((static_cast<uint64_t>(e0) >> 3) + 2 * i + h, p.seed, p.step);
+      *reinterpret_cast<uint4*>(wbox + sw64(r, 2 * i + h)) = pack_sr_bf16x8(w + 8 * h, rnd);
+    }
+  }
+  float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][half][row]
+  amax[(0 * 2 + half) * 128 + r] = n1;
+  amax[(1 * 2 + half) * 128 + r] = n2;
+  ptx::bar_sync(kEpiBarrier, kEpiThreads);
+  n1 = fmaxf(n1, amax[(0 * 2 + (half ^ 1)) * 128 + r]);
+  n2 = fmaxf(n2, amax[(1 * 2 + (half ^ 1)) * 128 + r]);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (uses_s1(KIND))
+        o1[j >> 2] |= (static_cast<uint32_t>(dev::quant<true>(m[16 * i + j], n1)) & 0xFFu) << (8 * (j & 3));
+      if (uses_s2(KIND))
+        o2[j >> 2] |= (static_cast<uint32_t>(dev::quant<false>(v[16 * i + j], n2)) & 0xFFu) << (8 * (j & 3));
+    }
+    if (uses_s1(KIND))
+      *reinterpret_cast<uint4*>(buf + kOffS1 + sw64(r, 2 * half + i)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    if (uses_s2(KIND))
+      *reinterpret_cast<uint4*>(buf + kOffS2 + sw64(r, 2 * half + i)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  }
+  *n1_out = n1;
+  *n2_out = n2;
+}
+
+// The epilogue of the FORGE step for bf16 weights.  One thread (warp 2,
+// lane 0) moves data: for chunk j+1 it waits until the bulk stores of chunk
+// j-1 have read their buffer, then issues the TMA loads of the W / state
+// boxes of chunk j+1; after all 256 epilogue threads have updated chunk j in
+// shared memory it issues the TMA stores of chunk j.  Loads of the next
+// tile's first chunks overlap the wait for its accumulator.
+template <int KIND, int SDT>
+__device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
+                                  const CUtensorMap* mS2, const GemmParams& p, SharedState* ss,
+                                  uint8_t* epi, int warp, int lane) {
+  constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
+  constexpr bool I8 = (SDT == kSInt8);
+  constexpr int kCC = I8 ? 64 : 32;
+  constexpr int kChunks = kTileN / kCC;
+  constexpr int kOffS1 = I8 ? 16384 : 8192;
+  constexpr int kOffS2 = 24576;
+  constexpr uint32_t kTx = (I8 ? 16384u : 8192u) + (U1 ? (I8 ? 8192u : 16384u) : 0u) +
+                           (U2 ? (I8 ? 8192u : 16384u) : 0u);
+  const int quarter = warp & 3, half = (warp - 2) >> 2;
+  const int r = quarter * 32 + lane;
+  const bool io = (warp == 2 && lane == 0);
+  const int64_t K = p.Ncols;
+  const int my_tiles =
+      p.num_tiles > static_cast<int>(blockIdx.x) ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
+  const int total = my_tiles * kChunks;
+
+  auto where = [&](int j, int& row0, int& col0) {
+    int tm, tn;
+    tile_coords(static_cast<int>(blockIdx.x) + (j / kChunks) * static_cast<int>(gridDim.x), p, tm, tn);
+    row0 = tm * kTileM;
+    col0 = tn * kTileN + (j % kChunks) * kCC;
+  };
+  auto issue = [&](int j) {
+    int row0, col0;
+    where(j, row0, col0);
+    uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
+    uint64_t* bar = &ss->epi_full[j & 1];
+    ptx::mbar_arrive_expect_tx(bar, kTx);
+    ptx::tma_load_2d(mW, bar, buf, col0, row0);
+    if (I8) ptx::tma_load_2d(mW, bar, buf + 8192, col0 + 32, row0);
+    if (U1) ptx::tma_load_2d(mS1, bar, buf + kOffS1, col0, row0);
+    if (U2) ptx::tma_load_2d(mS2, bar, buf + kOffS2, col0, row0);
+  };
+  auto store = [&](int j) {
+    int row0, col0;
+    where(j, row0, col0);
+    const uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
+    ptx::tma_store_2d(mW, buf, col0, row0);
+    if (I8) ptx::tma_store_2d(mW, buf + 8192, col0 + 32, row0);
+    if (U1) ptx::tma_store_2d(mS1, buf + kOffS1, col0, row0);
+    if (U2) ptx::tma_store_2d(mS2, buf + kOffS2, col0, row0);
+    ptx::bulk_commit_group();
+  };
+
+  int issued = 0, consumed = 0, local = -1;
+  float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};  // old INT8 scales
+  if (io && total > 0) {
+    issue(0);
+    issued = 1;
+  }
+  for (int j = 0; j < total; ++j) {
+    const int c = j % kChunks;
+    int row0, col0;
+    where(j, row0, col0);
+    const int64_t row = static_cast<int64_t>(row0) + r;
+    bool ok = true;
+    if (c == 0) {
+      ++local;
+      if (I8 && row < p.M) {  // old block scales of this row of the tile
+        const int64_t nb = K / 64, b0 = col0 / 64;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if ((b0 + q) * 64 < K) {
+            if (U1) a1[q] = p.s1_scale[row * nb + b0 + q];
+            if (U2) a2[q] = p.s2_scale[row * nb + b0 + q];
+          }
+        }
+      }
+      if (lane == 0) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
+    }
+    if (io && j + 1 < total) {
+      ptx::bulk_wait_group_read0();
+      issue(j + 1);
+      issued = j + 2;
+    }
+    if (lane == 0 && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
+    if (ptx::bar_red_or(kEpiBarrier, kEpiThreads, !ok)) break;  // same verdict in every warp
+    consumed = j + 1;
+    ptx::tc_fence_after();
+    const int acc = local & 1;
+    uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
+    const int col = col0 + half * (kCC / 2);
+    const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(acc * kTileN + c * kCC + half * (kCC / 2));
+    const int64_t e0 = row * K + col;
+    if (I8) {
+      float n1, n2;
+      const float o1 = c == 0 ? a1[0] : c == 1 ? a1[1] : c == 2 ? a1[2] : a1[3];
+      const float o2 = c == 0 ? a2[0] : c == 1 ? a2[1] : c == 2 ? a2[2] : a2[3];
+      epi_chunk_int8<KIND>(taddr, buf, r, half, e0, o1, o2, &n1, &n2, p);
+      if (half == 0 && row < p.M && col0 < K) {
+        const int64_t sidx = row * (K / 64) + col0 / 64;
+        if (U1) p.s1_scale[sidx] = n1;
+        if (U2) p.s2_scale[sidx] = n2;
+      }
+    } else {
+      epi_chunk_fp32<KIND>(taddr, buf, r, half, e0, p);
+    }
+    if (c == kChunks - 1) ptx::tc_fence_before();
+    ptx::fence_proxy_async_smem();
+    ptx::bar_sync(kEpiBarrier, kEpiThreads);
+    if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive(&ss->tmem_empty[acc]);
+    if (io) store(j);
+  }
+  if (io) {
+    ptx::bulk_wait_group0();
+    for (int j = consumed; j < issued; ++j)  // loads issued but not consumed (abort path)
+      bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss, false);
+  }
+}
+
+template <int SDT>
+__device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mW, const CUtensorMap* mS1,
+                                                      const CUtensorMap* mS2, const GemmParams& p,
+                                                      SharedState* ss, uint8_t* epi, int warp,
+                                                      int lane) {
+  switch (p.sc.kind) {
+    case kAdamW: epilogue_tma_role<kAdamW, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kNAdam: epilogue_tma_role<kNAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kRAdam: epilogue_tma_role<kRAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kLion: epilogue_tma_role<kLion, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kRMSprop: epilogue_tma_role<kRMSprop, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kAdaGrad: epilogue_tma_role<kAdaGrad, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kSGD: epilogue_tma_role<kSGD, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    default: epilogue_tma_role<kSGDMomentum, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int MODE, int WDT, int SDT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-              const GemmParams p) {
+              const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapS1,
+              const __grid_constant__ CUtensorMap mapS2, const GemmParams p) {
+  using Cfg = KCfg<MODE, WDT>;
+  constexpr int STG = Cfg::kStg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* smA = smem;
-  uint8_t* smB = smem + kStages * kABytes;
-  SharedState* ss = reinterpret_cast<SharedState*>(smB + kStages * kBBytes);
+  uint8_t* smB = smem + STG * Cfg::kA;
+  uint8_t* epi = smB + STG * Cfg::kB;
+  SharedState* ss = reinterpret_cast<SharedState*>(epi + Cfg::kEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STG; ++s) {
       ptx::mbar_init(&ss->full[s], 1);
       ptx::mbar_init(&ss->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ss->tmem_full[a], 1);
       ptx::mbar_init(&ss->tmem_empty[a], kNumEpiWarps);
+      ptx::mbar_init(&ss->epi_full[a], 1);
     }
     ptx::mbar_init(&ss->mma_done, 1);
     ss->abort = 0;
@@ -546,11 +865,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
 
   if (warp == 0) {
-    if (lane == 0) producer_role<MODE>(&mapA, &mapB, p, smA, smB, ss);
+    if (lane == 0) producer_role<MODE, STG, Cfg::kBK>(&mapA, &mapB, p, smA, smB, ss);
   } else if (warp == 1) {
-    if (lane == 0) mma_role<MODE>(p, smA, smB, ss);
+    if (lane == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
-    epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane);
+    if constexpr (Cfg::kTmaEpi)
+      epilogue_tma_dispatch<SDT>(&mapW, &mapS1, &mapS2, p, ss, epi, warp, lane);
+    else
+      epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane);
   }
 
   ptx::tc_fence_before();

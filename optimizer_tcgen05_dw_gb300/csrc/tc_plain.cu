@@ -9,9 +9,10 @@ template <int MODE>
 static cudaError_t run_plain(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                              int grid, cudaStream_t s) {
   auto* k = tc_kernel<MODE, kWBf16, kSFp32>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  constexpr int smem = KCfg<MODE, kWBf16>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, kSmemBytes, s>>>(a, b, p);
+  k<<<grid, kThreads, smem, s>>>(a, b, a, a, a, p);  // no staged epilogue in these modes
   return cudaGetLastError();
 }
 
