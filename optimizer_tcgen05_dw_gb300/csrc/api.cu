@@ -166,7 +166,7 @@ forge_status_t wgrad_maps(const forge_linear_t* lin, int bk, CUtensorMap* ma, CU
   if (lin->N % 64 == 0 && lin->K % 64 == 0) {
     *op3d = 1;
     if ((st = mn_major_3d_map(ma, lin->dY, lin->N, lin->T, bk, kTileM / 64)) != FORGE_OK) return st;
-    return mn_major_3d_map(mb, lin->X, lin->K, lin->T, bk, kTileN / 64);
+    return mn_major_3d_map(mb, lin->X, lin->K, lin->T, bk, kTileN / 2 / 64);  // half of B per CTA
   }
   *op3d = 0;
   if ((st = bf16_map(ma, lin->dY, lin->N, lin->T, 64, bk)) != FORGE_OK) return st;
@@ -328,13 +328,15 @@ void fill_tiles(GemmParams& p, int64_t M, int64_t Ncols, int64_t red, int bk = k
   p.M = static_cast<int32_t>(M);
   p.Ncols = static_cast<int32_t>(Ncols);
   p.num_kb = static_cast<int32_t>((red + bk - 1) / bk);
-  p.tiles_m = static_cast<int32_t>((M + kTileM - 1) / kTileM);
+  p.tiles_m = static_cast<int32_t>((M + 2 * kTileM - 1) / (2 * kTileM));  // 256-row pair tiles
   p.tiles_n = static_cast<int32_t>((Ncols + kTileN - 1) / kTileN);
   p.num_tiles = p.tiles_m * p.tiles_n;
 }
 
+// Clusters of two CTAs, at most one CTA per SM.
 int grid_for(const GemmParams& p, const DeviceInfo& d) {
-  return p.num_tiles < d.num_sms ? p.num_tiles : d.num_sms;
+  const int pairs = d.num_sms / 2;
+  return 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
 }
 
 forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype, cudaStream_t s,
@@ -359,7 +361,7 @@ forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_
   std::memset(&p, 0, sizeof(p));
   if (K % 64 == 0) {
     p.op3d = 1;
-    if ((st = mn_major_3d_map(&mb, W, K, N, kBlockK, kTileN / 64)) != FORGE_OK) return st;
+    if ((st = mn_major_3d_map(&mb, W, K, N, kBlockK, kTileN / 2 / 64)) != FORGE_OK) return st;
   } else if ((st = bf16_map(&mb, W, K, N, 64, kBlockK)) != FORGE_OK) {
     return st;
   }

@@ -42,21 +42,18 @@ inline constexpr bool uses_s2(int k) {
   return k == kAdamW || k == kNAdam || k == kRAdam || k == kRMSprop || k == kAdaGrad;
 }
 
-// Tensor-core GEMM geometry: a 128 x 256 output tile (two 128 x 128 optimizer
-// tiles side by side), 64-deep reduction blocks, a 4-stage shared-memory ring.
+// Tensor-core GEMM geometry: a CTA pair computes a 256 x 256 output tile
+// (each CTA 128 x 256: two 128 x 128 optimizer tiles side by side) in
+// 64-token stages; a stage holds this CTA's 128 rows of A and 128 of B's
+// 256 columns (32 KiB).  Plain modes keep a 6-stage ring (192 KiB); the FORGE
+// step with bf16 weights keeps four stages (128 KiB) next to the 80 KiB of
+// staged epilogue buffers.
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kBlockK = 64;
-constexpr int kStages = 4;
-constexpr int kABytes = kTileM * kBlockK * 2;            // 16 KiB
-constexpr int kBBytes = kTileN * kBlockK * 2;            // 32 KiB
-constexpr int kStageBytes = kABytes + kBBytes;           // 48 KiB
-// The FORGE step with bf16 weights streams its operands in 48-token stages
-// (36 KiB, four of them: 144 KiB), leaving 80 KiB for the staged epilogue.
-// Measured on GB300: four 48-token stages beat three 64-token or six
-// 32-token stages of the same ring size.
+constexpr int kStages = 6;
 #ifndef FORGE_FUSED_BK
-#define FORGE_FUSED_BK 48
+#define FORGE_FUSED_BK 64
 #endif
 #ifndef FORGE_FUSED_STAGES
 #define FORGE_FUSED_STAGES 4
@@ -65,7 +62,7 @@ constexpr int kStageBytes = kABytes + kBBytes;           // 48 KiB
 #define FORGE_WGRAD_BK 64
 #endif
 #ifndef FORGE_WGRAD_STAGES
-#define FORGE_WGRAD_STAGES 4
+#define FORGE_WGRAD_STAGES 6
 #endif
 constexpr int kFusedBlockK = FORGE_FUSED_BK;
 constexpr int kWgradBlockK = FORGE_WGRAD_BK;      // unfused weight-gradient pass

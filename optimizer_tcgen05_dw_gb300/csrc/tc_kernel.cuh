@@ -5,27 +5,31 @@
 // the optimizer is applied to the finished tile at once, the gradient tile is
 // discarded, and only the updated weights and moments are written back.
 //
-// GB300 design (one CTA per SM, persistent over output tiles):
-//   warp 0      one lane issues TMA tile loads of the two operands into a
-//               kStages-deep shared-memory ring (128-byte swizzle), each stage
-//               guarded by a "full" (bytes landed) and "empty" (MMAs done)
-//               mbarrier;
-//   warp 1      allocates 512 tensor-memory columns; one lane issues
-//               tcgen05.mma (M=128, N=256, K=16, bf16 -> fp32) into one of two
-//               TMEM accumulators, so the MMAs of tile i+1 overlap the
-//               epilogue of tile i;
-//   warps 2..9  the epilogue: tcgen05.ld pulls the finished fp32 tile into
-//               registers (one TMEM lane = one output row per thread, two
-//               warps per 32-lane quarter splitting the 256 columns), then
-//               either runs the optimizer on it (FORGE), stores it as fp32
-//               (unfused pass 1) or as bf16 (dX).
+// GB300 design: clusters of two CTAs (one per SM), persistent over output
+// tiles of 256 x 256; the pair runs tcgen05 with .cta_group::2, CTA r holding
+// rows [128 r, 128 r + 128) of the tile in its tensor memory.
+//   warp 0      one lane of each CTA issues TMA loads of its half of the
+//               operands (its 128 rows of A, its 128 columns of B) into a
+//               STG-deep shared-memory ring (128-byte swizzle); both halves
+//               complete on the leader CTA's "full" mbarrier;
+//   warp 1      allocates 512 tensor-memory columns (collectively with the
+//               peer); in the leader one lane issues tcgen05.mma (M=256,
+//               N=256, K=16, bf16 -> fp32) into one of two TMEM accumulators,
+//               so the MMAs of tile i+1 overlap the epilogue of tile i, and
+//               multicasts its commits to both CTAs' "empty" / "tmem full"
+//               barriers;
+//   warps 2..9  the epilogue of each CTA: tcgen05.ld pulls its 128 rows of
+//               the finished fp32 tile into registers (one TMEM lane = one
+//               output row), then runs the optimizer on it (FORGE), or stores
+//               it as fp32 (unfused pass 1) or bf16 (dX); the eight warps of
+//               both CTAs release the accumulator on the leader's barrier.
 // Operand layouts (all 128-byte swizzled atoms of 8 rows x 128 bytes):
-//   wgrad  A = dY^T tile [128 n x 64 t]: dY is [T x N] with n contiguous, so A
-//          is MN-major: two 64-wide column atoms 8 KiB apart (LBO), 8-row
-//          token groups 1 KiB apart (SBO).  B = X tile [256 k x 64 t], MN-major,
-//          four 64-wide atoms.
+//   wgrad  A = dY^T tile [128 n x BK t] per CTA: dY is [T x N] with n
+//          contiguous, so A is MN-major: two 64-wide column atoms BK*128
+//          bytes apart (LBO), 8-row token groups 1 KiB apart (SBO).
+//          B = X tile [128 k x BK t] per CTA, MN-major, two atoms.
 //   dgrad  A = dY tile [128 t x 64 n], K-major (n contiguous); B = W tile
-//          [256 k x 64 n], MN-major.
+//          [128 k x 64 n] per CTA, MN-major.
 // Every wait is bounded (GemmParams::wait_limit_ns): on expiry the CTA records
 // a timeout in the status word, all roles stop, in-flight copies and MMAs are
 // drained (again bounded), tensor memory is released and the CTA returns.
@@ -50,13 +54,15 @@ struct SharedState {
   int32_t abort;
 };
 
-// Per-instantiation layout.  The FORGE step with bf16 weights stages its
-// weight/state tiles through shared memory with TMA (two 40 KiB chunk
-// buffers), which leaves room for a 3-stage operand ring; the other modes
-// keep 4 stages.
+// Per-instantiation layout (per CTA).  The FORGE step with bf16 weights
+// stages its weight/state tiles through shared memory with TMA (two 40 KiB
+// chunk buffers) next to a 4-stage operand ring; the other modes use a
+// deeper ring.  A stage holds 128 rows of A and 128 columns of B (half of the
+// pair's 256): 32 KiB at 64 tokens.
 constexpr int kEpiBufBytes = 40960;
 constexpr int kEpiThreads = 32 * kNumEpiWarps;
 constexpr int kEpiBarrier = 1;  // named barrier of the epilogue warps
+constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 
 template <int MODE, int WDT>
 struct KCfg {
@@ -65,8 +71,8 @@ struct KCfg {
       kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK);  // tokens per stage
   static constexpr int kStg =
       kTmaEpi ? kFusedStages : (MODE == kModeWgradStore ? kWgradStages : kStages);
-  static constexpr int kA = kTileM * kBK * 2;                     // bytes of A per stage
-  static constexpr int kB = kTileN * kBK * 2;
+  static constexpr int kA = kTileM * kBK * 2;       // bytes of A per stage (this CTA's 128 rows)
+  static constexpr int kB = (kTileN / 2) * kBK * 2; // bytes of B per stage (this CTA's 128 columns)
   static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBufBytes : 0;
   static constexpr int kSmem = kStg * (kA + kB) + kEpiBytes + 512 + 1024;
 };
@@ -75,6 +81,7 @@ static_assert(KCfg<kModeFusedOpt, kWBf16>::kStg <= 8 && KCfg<kModeWgradStore, kW
                   kStages <= 8, "barrier arrays");
 static_assert(KCfg<kModeWgradStore, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeFusedOpt, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeDgrad, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -111,38 +118,45 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
 
 // ------------------------------------------------------------------ roles
 
+// Tile index of the pair's i-th tile, and the CTA's rank in the pair.
+__device__ __forceinline__ int pair_id() { return static_cast<int>(blockIdx.x) >> 1; }
+__device__ __forceinline__ int num_pairs() { return static_cast<int>(gridDim.x) >> 1; }
+
 template <int MODE, int STG, int BK>
 __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, const GemmParams& p,
-                              uint8_t* smA, uint8_t* smB, SharedState* ss) {
+                              uint8_t* smA, uint8_t* smB, SharedState* ss, uint32_t rank) {
+  constexpr int kA = kTileM * BK * 2, kB = (kTileN / 2) * BK * 2;
   uint32_t it = 0;
   uint32_t issued_mask = 0;
   uint32_t last_parity = 0;  // bit s: parity of the last phase armed on full[s]
+  const uint32_t full0 = ptx::mapa(ptx::smem_addr(&ss->full[0]), 0);  // the leader's barriers
   if (!p.skip_loads) {
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs()) {
       int tm, tn;
       tile_coords(tile, p, tm, tn);
-      const int m0 = tm * kTileM, n0 = tn * kTileN;
+      const int m0 = tm * kPairM + static_cast<int>(rank) * kTileM;      // this CTA's A rows
+      const int n0 = tn * kTileN + static_cast<int>(rank) * (kTileN / 2);  // this CTA's B columns
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = static_cast<int>(it % STG);
         const uint32_t ph = (it / STG) & 1u;
         if (!bounded_wait(&ss->empty[s], ph ^ 1u, p, ss)) goto drain;
-        ptx::mbar_arrive_expect_tx(&ss->full[s], (kTileM + kTileN) * BK * 2);
-        uint8_t* a = smA + s * (kTileM * BK * 2);
-        uint8_t* b = smB + s * (kTileN * BK * 2);
+        const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
+        if (rank == 0) ptx::mbar_arrive_expect_tx(&ss->full[s], 2u * (kA + kB));
+        uint8_t* a = smA + s * kA;
+        uint8_t* b = smB + s * kB;
         if (MODE == kModeDgrad) {
-          ptx::tma_load_2d(mA, &ss->full[s], a, kb * BK, m0);
+          ptx::tma_load_2d_pair(mA, bar, a, kb * BK, m0);
         } else if (p.op3d) {  // [2 column blocks][BK rows][64 columns] in one copy
-          ptx::tma_load_3d(mA, &ss->full[s], a, 0, kb * BK, m0 / 64);
+          ptx::tma_load_3d_pair(mA, bar, a, 0, kb * BK, m0 / 64);
         } else {
-          ptx::tma_load_2d(mA, &ss->full[s], a, m0, kb * BK);
-          ptx::tma_load_2d(mA, &ss->full[s], a + 64 * BK * 2, m0 + 64, kb * BK);
+          ptx::tma_load_2d_pair(mA, bar, a, m0, kb * BK);
+          ptx::tma_load_2d_pair(mA, bar, a + 64 * BK * 2, m0 + 64, kb * BK);
         }
         if (p.op3d) {
-          ptx::tma_load_3d(mB, &ss->full[s], b, 0, kb * BK, n0 / 64);
+          ptx::tma_load_3d_pair(mB, bar, b, 0, kb * BK, n0 / 64);
         } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            ptx::tma_load_2d(mB, &ss->full[s], b + j * (64 * BK * 2), n0 + 64 * j, kb * BK);
+          ptx::tma_load_2d_pair(mB, bar, b, n0, kb * BK);
+          ptx::tma_load_2d_pair(mB, bar, b + 64 * BK * 2, n0 + 64, kb * BK);
         }
         issued_mask |= 1u << s;
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
@@ -150,19 +164,24 @@ __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, cons
     }
   }
 drain:
-  // Every issued copy lands before the CTA can exit (already true unless a
-  // consumer gave up early).
-  for (int s = 0; s < STG; ++s)
-    if (issued_mask & (1u << s)) bounded_wait(&ss->full[s], (last_parity >> s) & 1u, p, ss, false);
+  // Every issued copy lands before the pair can exit (already true unless a
+  // consumer gave up early).  The leader's full barriers count both CTAs'
+  // copies; the peer's copies are covered by the leader's drain and the
+  // cluster barrier at the end of the kernel.
+  if (rank == 0)
+    for (int s = 0; s < STG; ++s)
+      if (issued_mask & (1u << s)) bounded_wait(&ss->full[s], (last_parity >> s) & 1u, p, ss, false);
 }
 
+// Leader CTA only.
 template <int MODE, int STG, int BK>
 __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, SharedState* ss) {
+  constexpr int kA = kTileM * BK * 2, kB = (kTileN / 2) * BK * 2;
   constexpr uint32_t kIdesc =
-      ptx::idesc_bf16_f32(kTileM, kTileN, /*a_mn=*/MODE != kModeDgrad, /*b_mn=*/true);
+      ptx::idesc_bf16_f32(kPairM, kTileN, /*a_mn=*/MODE != kModeDgrad, /*b_mn=*/true);
   uint32_t it = 0;
   int local = 0;
-  for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+  for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs(), ++local) {
     const int acc = local & 1;
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
     if (!bounded_wait(&ss->tmem_empty[acc], aph ^ 1u, p, ss)) goto done;
@@ -174,27 +193,27 @@ __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, Shared
         const uint32_t ph = (it / STG) & 1u;
         if (!bounded_wait(&ss->full[s], ph, p, ss)) goto done;
         ptx::tc_fence_after();
-        const uint32_t a0 = ptx::smem_addr(smA + s * (kTileM * BK * 2));
-        const uint32_t b0 = ptx::smem_addr(smB + s * (kTileN * BK * 2));
+        const uint32_t a0 = ptx::smem_addr(smA + s * kA);
+        const uint32_t b0 = ptx::smem_addr(smB + s * kB);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
-          // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB.
+          // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB;
+          // atoms of 64 columns x BK rows sit BK*128 bytes apart (LBO).
           // K-major: 16 bf16 = 32 B inside the 128-byte swizzle row.
-          // MN-major atoms of 64 columns x BK rows sit BK*128 bytes apart (LBO).
           const uint64_t adesc = (MODE == kModeDgrad)
                                      ? ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024)
                                      : ptx::smem_desc_sw128(a0 + kk * 2048, BK * 128, 1024);
           const uint64_t bdesc = ptx::smem_desc_sw128(b0 + kk * 2048, BK * 128, 1024);
-          ptx::mma_bf16(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          ptx::mma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
         }
-        ptx::mma_commit(&ss->empty[s]);  // frees the stage once these MMAs finish
+        ptx::mma_commit_pair_multicast(&ss->empty[s], 0x3);  // frees the stage in both CTAs
       }
-      ptx::mma_commit(&ss->tmem_full[acc]);  // accumulator complete
+      ptx::mma_commit_pair_multicast(&ss->tmem_full[acc], 0x3);  // accumulator complete
     }
   }
 done:
   // Tensor memory may be released only after every issued MMA has finished.
-  ptx::mma_commit(&ss->mma_done);
+  ptx::mma_commit_pair_multicast(&ss->mma_done, 0x1);
   bounded_wait(&ss->mma_done, 0u, p, ss, false);
 }
 
@@ -506,12 +525,14 @@ __device__ __forceinline__ void epi_store(uint32_t tbase, int64_t row, int colba
 }
 
 template <int MODE, int WDT, int SDT>
-__device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, int lane) {
+__device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, int lane,
+                              uint32_t rank) {
   const int quarter = warp & 3;           // TMEM lanes this warp may access
   const int half = (warp - 2) >> 2;       // which 128 of the 256 columns
   const int r = quarter * 32 + lane;
   int local = 0;
-  for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+  const uint32_t empty0 = ptx::mapa(ptx::smem_addr(&ss->tmem_empty[0]), 0);
+  for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs(), ++local) {
     const int acc = local & 1;
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
     // One lane waits and the verdict is broadcast, so the warp stays
@@ -523,7 +544,7 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
     ptx::tc_fence_after();
     int tm, tn;
     tile_coords(tile, p, tm, tn);
-    const int64_t row = static_cast<int64_t>(tm) * kTileM + r;
+    const int64_t row = static_cast<int64_t>(tm) * kPairM + rank * kTileM + r;
     const int colbase = tn * kTileN + half * 128;
     const bool row_ok = row < p.M;
     const uint32_t tbase = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
@@ -534,7 +555,7 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
       epi_store<MODE>(tbase, row, colbase, row_ok, p);
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ss->tmem_empty[acc]);
+    if (lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
   }
 }
 
@@ -689,7 +710,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 template <int KIND, int SDT>
 __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
                                   const CUtensorMap* mS2, const GemmParams& p, SharedState* ss,
-                                  uint8_t* epi, int warp, int lane) {
+                                  uint8_t* epi, int warp, int lane, uint32_t rank) {
   constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
   constexpr bool I8 = (SDT == kSInt8);
   constexpr int kCC = I8 ? 64 : 32;
@@ -702,35 +723,38 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
   const int r = quarter * 32 + lane;
   const bool io = (warp == 2 && lane == 0);
   const int64_t K = p.Ncols;
-  const int my_tiles =
-      p.num_tiles > static_cast<int>(blockIdx.x) ? (p.num_tiles - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1 : 0;
+  const int my_tiles = p.num_tiles > pair_id() ? (p.num_tiles - 1 - pair_id()) / num_pairs() + 1 : 0;
   const int total = my_tiles * kChunks;
+  const uint32_t empty0 = ptx::mapa(ptx::smem_addr(&ss->tmem_empty[0]), 0);
 
   auto where = [&](int j, int& row0, int& col0) {
     int tm, tn;
-    tile_coords(static_cast<int>(blockIdx.x) + (j / kChunks) * static_cast<int>(gridDim.x), p, tm, tn);
-    row0 = tm * kTileM;
+    tile_coords(pair_id() + (j / kChunks) * num_pairs(), p, tm, tn);
+    row0 = tm * kPairM + static_cast<int>(rank) * kTileM;
     col0 = tn * kTileN + (j % kChunks) * kCC;
   };
+  // Weight/state lines are touched once per step: evict-first in L2, so they
+  // do not displace the operand tiles the main loop re-reads from L2.
+  const uint64_t pol = evict_first_policy();
   auto issue = [&](int j) {
     int row0, col0;
     where(j, row0, col0);
     uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
     uint64_t* bar = &ss->epi_full[j & 1];
     ptx::mbar_arrive_expect_tx(bar, kTx);
-    ptx::tma_load_2d(mW, bar, buf, col0, row0);
-    if (I8) ptx::tma_load_2d(mW, bar, buf + 8192, col0 + 32, row0);
-    if (U1) ptx::tma_load_2d(mS1, bar, buf + kOffS1, col0, row0);
-    if (U2) ptx::tma_load_2d(mS2, bar, buf + kOffS2, col0, row0);
+    ptx::tma_load_2d_hint(mW, bar, buf, col0, row0, pol);
+    if (I8) ptx::tma_load_2d_hint(mW, bar, buf + 8192, col0 + 32, row0, pol);
+    if (U1) ptx::tma_load_2d_hint(mS1, bar, buf + kOffS1, col0, row0, pol);
+    if (U2) ptx::tma_load_2d_hint(mS2, bar, buf + kOffS2, col0, row0, pol);
   };
   auto store = [&](int j) {
     int row0, col0;
     where(j, row0, col0);
     const uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
-    ptx::tma_store_2d(mW, buf, col0, row0);
-    if (I8) ptx::tma_store_2d(mW, buf + 8192, col0 + 32, row0);
-    if (U1) ptx::tma_store_2d(mS1, buf + kOffS1, col0, row0);
-    if (U2) ptx::tma_store_2d(mS2, buf + kOffS2, col0, row0);
+    ptx::tma_store_2d_hint(mW, buf, col0, row0, pol);
+    if (I8) ptx::tma_store_2d_hint(mW, buf + 8192, col0 + 32, row0, pol);
+    if (U1) ptx::tma_store_2d_hint(mS1, buf + kOffS1, col0, row0, pol);
+    if (U2) ptx::tma_store_2d_hint(mS2, buf + kOffS2, col0, row0, pol);
     ptx::bulk_commit_group();
   };
 
@@ -791,7 +815,7 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
     if (c == kChunks - 1) ptx::tc_fence_before();
     ptx::fence_proxy_async_smem();
     ptx::bar_sync(kEpiBarrier, kEpiThreads);
-    if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive(&ss->tmem_empty[acc]);
+    if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
     if (io) store(j);
   }
   if (io) {
@@ -805,16 +829,16 @@ template <int SDT>
 __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mW, const CUtensorMap* mS1,
                                                       const CUtensorMap* mS2, const GemmParams& p,
                                                       SharedState* ss, uint8_t* epi, int warp,
-                                                      int lane) {
+                                                      int lane, uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_tma_role<kAdamW, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    case kNAdam: epilogue_tma_role<kNAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    case kRAdam: epilogue_tma_role<kRAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    case kLion: epilogue_tma_role<kLion, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    case kRMSprop: epilogue_tma_role<kRMSprop, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    case kAdaGrad: epilogue_tma_role<kAdaGrad, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    case kSGD: epilogue_tma_role<kSGD, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
-    default: epilogue_tma_role<kSGDMomentum, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane); break;
+    case kAdamW: epilogue_tma_role<kAdamW, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_tma_role<kNAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_tma_role<kRAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_tma_role<kLion, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_tma_role<kRMSprop, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_tma_role<kAdaGrad, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_tma_role<kSGD, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_tma_role<kSGDMomentum, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
   }
 }
 
@@ -836,15 +860,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   SharedState* ss = reinterpret_cast<SharedState*>(epi + Cfg::kEpiBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0 = leader of the pair
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STG; ++s) {
-      ptx::mbar_init(&ss->full[s], 1);
-      ptx::mbar_init(&ss->empty[s], 1);
+      ptx::mbar_init(&ss->full[s], 1);   // the leader's: armed once, both CTAs' bytes
+      ptx::mbar_init(&ss->empty[s], 1);  // each CTA's: the leader's multicast commit
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ss->tmem_full[a], 1);
-      ptx::mbar_init(&ss->tmem_empty[a], kNumEpiWarps);
+      ptx::mbar_init(&ss->tmem_empty[a], 2 * kNumEpiWarps);  // the leader's: both CTAs' warps
       ptx::mbar_init(&ss->epi_full[a], 1);
     }
     ptx::mbar_init(&ss->mma_done, 1);
@@ -857,31 +882,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) {
     __syncwarp();
-    ptx::tmem_alloc(&ss->tmem_base, kTmemCols);
-    ptx::tmem_relinquish();
+    ptx::tmem_alloc_pair(&ss->tmem_base, kTmemCols);
+    ptx::tmem_relinquish_pair();
   }
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
   ptx::tc_fence_after();
 
   if (warp == 0) {
-    if (lane == 0) producer_role<MODE, STG, Cfg::kBK>(&mapA, &mapB, p, smA, smB, ss);
+    if (lane == 0) producer_role<MODE, STG, Cfg::kBK>(&mapA, &mapB, p, smA, smB, ss, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
+    if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT>(&mapW, &mapS1, &mapS2, p, ss, epi, warp, lane);
+      epilogue_tma_dispatch<SDT>(&mapW, &mapS1, &mapS2, p, ss, epi, warp, lane, rank);
     else
-      epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane);
+      epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
 
   ptx::tc_fence_before();
   __syncthreads();
+  ptx::cluster_sync();  // the peer's shared and tensor memory stay valid until the pair is done
   if (warp == 1) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(ss->tmem_base, kTmemCols);
+    ptx::tmem_dealloc_pair(ss->tmem_base, kTmemCols);
   }
+}
+
+// Launch on clusters of two CTAs (the tcgen05 pair); grid is a multiple of 2.
+template <typename Kernel>
+inline cudaError_t launch_pair(Kernel k, int grid, int smem, cudaStream_t s, const CUtensorMap& a,
+                               const CUtensorMap& b, const CUtensorMap& w, const CUtensorMap& s1,
+                               const CUtensorMap& s2, const GemmParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, b, w, s1, s2, p);
 }
 
 }  // namespace forge
