@@ -13,7 +13,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "../../include/forge.h"
+#include "forge.h"
 #include "common.h"
 #include "launch.h"
 
@@ -222,7 +222,7 @@ OptScalars make_scalars(int kind, const forge_hparams_t& hp, int64_t step) {
       const double c1 = 1.0 - std::pow(b1, t), c2 = 1.0 - std::pow(b2, t);
       s.decay = static_cast<float>(1.0 - lr * wd);
       s.step_size = static_cast<float>(lr / c1);
-      s.sqrt_c2 = static_cast<float>(std::sqrt(c2));
+      s.inv_sqrt_c2 = static_cast<float>(1.0 / std::sqrt(c2));
       break;
     }
     case kNAdam: {
@@ -233,7 +233,7 @@ OptScalars make_scalars(int kind, const forge_hparams_t& hp, int64_t step) {
       for (int64_t i = 1; i <= step; ++i) prod *= mu(i);
       const double mu_t = mu(step), mu_next = mu(step + 1);
       const double prod_next = prod * mu_next;
-      s.c2 = static_cast<float>(c2);
+      s.inv_c2 = static_cast<float>(1.0 / c2);
       s.coef_g = static_cast<float>(lr * (1.0 - mu_t) / (1.0 - prod));
       s.coef_m = static_cast<float>(lr * mu_next / (1.0 - prod_next));
       break;

@@ -19,8 +19,8 @@ enum DeviceStatus : uint32_t { kStatusOk = 0, kStatusTimeout = 4 };
 // Per-step scalars of a rule, formed on the host in double from the float
 // hyper-parameters and the step number and rounded once to float.  Field use
 // per rule (everything else is zero):
-//   AdamW   decay b1 omb1 b2 omb2 step_size sqrt_c2 eps
-//   NAdam   l2 b1 omb1 b2 omb2 c2 eps coef_g coef_m
+//   AdamW   decay b1 omb1 b2 omb2 step_size inv_sqrt_c2 eps
+//   NAdam   l2 b1 omb1 b2 omb2 inv_c2 eps coef_g coef_m
 //   RAdam   l2 b1 omb1 b2 omb2 eps; rectified ? (step_size, sqrt_c2) : step_size
 //   Lion    decay lr b1 omb1 b2 omb2
 //   RMSprop l2 alpha oma lr eps
@@ -31,7 +31,7 @@ struct OptScalars {
   int32_t kind;
   int32_t rectified;
   float l2, decay, lr, b1, omb1, b2, omb2, eps;
-  float step_size, sqrt_c2, c2, coef_g, coef_m, alpha, oma, mom;
+  float step_size, sqrt_c2, inv_sqrt_c2, inv_c2, coef_g, coef_m, alpha, oma, mom;
 };
 
 // Which state buffers a rule keeps.
@@ -46,8 +46,8 @@ inline constexpr bool uses_s2(int k) {
 // (each CTA 128 x 256: two 128 x 128 optimizer tiles side by side) in
 // 64-token stages; a stage holds this CTA's 128 rows of A and 128 of B's
 // 256 columns (32 KiB).  Plain modes keep a 6-stage ring (192 KiB); the FORGE
-// step with bf16 weights keeps four stages (128 KiB) next to the 80 KiB of
-// staged epilogue buffers.
+// step with bf16 weights keeps five stages (160 KiB) next to the 64 KiB of
+// staged optimizer-state buffers.
 constexpr int kTileM = 128;
 constexpr int kTileN = 256;
 constexpr int kBlockK = 64;
@@ -56,7 +56,7 @@ constexpr int kStages = 6;
 #define FORGE_FUSED_BK 64
 #endif
 #ifndef FORGE_FUSED_STAGES
-#define FORGE_FUSED_STAGES 4
+#define FORGE_FUSED_STAGES 5
 #endif
 #ifndef FORGE_WGRAD_BK
 #define FORGE_WGRAD_BK 64
@@ -68,8 +68,8 @@ constexpr int kFusedBlockK = FORGE_FUSED_BK;
 constexpr int kWgradBlockK = FORGE_WGRAD_BK;      // unfused weight-gradient pass
 constexpr int kWgradStages = FORGE_WGRAD_STAGES;
 constexpr int kFusedStages = FORGE_FUSED_STAGES;
-constexpr int kNumEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kNumEpiWarps);        // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kNumEpiWarps = 8;                          // epilogue warps, plain epilogues
+constexpr int kNumEpiWarpsStaged = 16;                   // epilogue warps, staged FORGE epilogue
 constexpr int kTmemCols = 2 * kTileN;                    // double-buffered fp32 accumulator
 
 enum GemmMode : int32_t {

@@ -35,9 +35,9 @@ __device__ __forceinline__ float sign0(float c) {
 // One step of rule KIND on one element.  w: current weight (fp32 value),
 // g: fp32 gradient, s1/s2: dequantised states (updated in place).
 // Orders (each operation rounded):
-//   AdamW  m = b1*m + omb1*g;  v = b2*v + omb2*(g*g);  d = sqrt(v)/sqrt_c2 + eps;
+//   AdamW  m = b1*m + omb1*g;  v = b2*v + omb2*(g*g);  d = sqrt(v)*inv_sqrt_c2 + eps;
 //          w = w*decay - step_size*(m/d)
-//   NAdam  g += l2*w;  m, v as AdamW;  d = sqrt(v/c2) + eps;
+//   NAdam  g += l2*w;  m, v as AdamW;  d = sqrt(v*inv_c2) + eps;
 //          w = w - coef_g*(g/d);  w = w - coef_m*(m/d)
 //   RAdam  g += l2*w;  m, v as AdamW;  rectified: d = sqrt(v) + eps;
 //          w = w - step_size*((m*sqrt_c2)/d);  otherwise w = w - step_size*m
@@ -56,10 +56,10 @@ __device__ __forceinline__ void rule(float& w, float g, float& s1, float& s2,
     const float m = add(mul(sc.b1, s1), mul(sc.omb1, g));
     const float v = add(mul(sc.b2, s2), mul(sc.omb2, mul(g, g)));
     if (KIND == kAdamW) {
-      const float d = add(dvd(sqr(v), sc.sqrt_c2), sc.eps);
+      const float d = add(mul(sqr(v), sc.inv_sqrt_c2), sc.eps);
       w = sub(mul(w, sc.decay), mul(sc.step_size, dvd(m, d)));
     } else if (KIND == kNAdam) {
-      const float d = add(sqr(dvd(v, sc.c2)), sc.eps);
+      const float d = add(sqr(mul(v, sc.inv_c2)), sc.eps);
       w = sub(w, mul(sc.coef_g, dvd(g, d)));
       w = sub(w, mul(sc.coef_m, dvd(m, d)));
     } else {

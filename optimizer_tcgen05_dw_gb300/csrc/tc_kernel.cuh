@@ -59,8 +59,7 @@ struct SharedState {
 // chunk buffers) next to a 4-stage operand ring; the other modes use a
 // deeper ring.  A stage holds 128 rows of A and 128 columns of B (half of the
 // pair's 256): 32 KiB at 64 tokens.
-constexpr int kEpiBufBytes = 40960;
-constexpr int kEpiThreads = 32 * kNumEpiWarps;
+constexpr int kEpiBufBytes = 32768;
 constexpr int kEpiBarrier = 1;  // named barrier of the epilogue warps
 constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 
@@ -75,6 +74,10 @@ struct KCfg {
   static constexpr int kB = (kTileN / 2) * kBK * 2; // bytes of B per stage (this CTA's 128 columns)
   static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBufBytes : 0;
   static constexpr int kSmem = kStg * (kA + kB) + kEpiBytes + 512 + 1024;
+  // TMA warp, MMA warp, epilogue warps (four per 32-lane quarter of TMEM in the
+  // staged epilogue, two in the plain ones).
+  static constexpr int kEpiWarps = kTmaEpi ? kNumEpiWarpsStaged : kNumEpiWarps;
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
 };
 static_assert(sizeof(SharedState) <= 512, "shared state region");
 static_assert(KCfg<kModeFusedOpt, kWBf16>::kStg <= 8 && KCfg<kModeWgradStore, kWBf16>::kStg <= 8 &&
@@ -590,113 +593,100 @@ __device__ __forceinline__ uint4 pack_sr_bf16x8(const float* w, uint4 rnd) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// fp32 states: a chunk is 128 rows x 32 columns (W 8 KiB, m and v 16 KiB
-// each); this thread owns 16 columns of row r, starting at element e0.
+// fp32 states: a chunk is 128 rows x 32 columns (m and v 16 KiB each in
+// shared memory); this thread owns 8 columns of row r (two 16-byte chunks of
+// each state), starting at element e0.  Its 8 bf16 weights come in and go out
+// in registers (`wv`).
 template <int KIND>
-__device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int r, int half,
-                                               int64_t e0, const GemmParams& p) {
-  constexpr int kOffS1 = 8192, kOffS2 = 24576;
-  float g[16], w[16], s1[16], s2[16];
-  ptx::tmem_ld_32x32b_x16(taddr, g);
+__device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int r, int sub,
+                                               int64_t e0, uint4& wv, const GemmParams& p) {
+  constexpr int kOffS1 = 0, kOffS2 = 16384;
+  float g[8], w[8], s1[8], s2[8];
+  ptx::tmem_ld_32x32b_x8(taddr, g);
+  unpack_bf16x8(wv, w);
 #pragma unroll
-  for (int i = 0; i < 2; ++i)
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + sw64(r, 2 * half + i)), w + 8 * i);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < 2; ++i) {
     if (uses_s1(KIND)) {
-      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS1 + sw128(r, 4 * half + i));
+      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS1 + sw128(r, 2 * sub + i));
       s1[4 * i] = x.x; s1[4 * i + 1] = x.y; s1[4 * i + 2] = x.z; s1[4 * i + 3] = x.w;
     } else {
       s1[4 * i] = s1[4 * i + 1] = s1[4 * i + 2] = s1[4 * i + 3] = 0.f;
     }
     if (uses_s2(KIND)) {
-      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS2 + sw128(r, 4 * half + i));
+      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS2 + sw128(r, 2 * sub + i));
       s2[4 * i] = x.x; s2[4 * i + 1] = x.y; s2[4 * i + 2] = x.z; s2[4 * i + 3] = x.w;
     } else {
       s2[4 * i] = s2[4 * i + 1] = s2[4 * i + 2] = s2[4 * i + 3] = 0.f;
     }
   }
 #pragma unroll
-  for (int j = 0; j < 16; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+  for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+  wv = pack_sr_bf16x8(w, dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step));
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint4 rnd = dev::sr_words((static_cast<uint64_t>(e0) >> 3) + i, p.seed, p.step);
-    *reinterpret_cast<uint4*>(buf + sw64(r, 2 * half + i)) = pack_sr_bf16x8(w + 8 * i, rnd);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
     if (uses_s1(KIND))
-      *reinterpret_cast<float4*>(buf + kOffS1 + sw128(r, 4 * half + i)) =
+      *reinterpret_cast<float4*>(buf + kOffS1 + sw128(r, 2 * sub + i)) =
           make_float4(s1[4 * i], s1[4 * i + 1], s1[4 * i + 2], s1[4 * i + 3]);
     if (uses_s2(KIND))
-      *reinterpret_cast<float4*>(buf + kOffS2 + sw128(r, 4 * half + i)) =
+      *reinterpret_cast<float4*>(buf + kOffS2 + sw128(r, 2 * sub + i)) =
           make_float4(s2[4 * i], s2[4 * i + 1], s2[4 * i + 2], s2[4 * i + 3]);
   }
 }
 
-// INT8 states: a chunk is 128 rows x 64 columns (one code block per row; W
-// in two 32-column boxes, codes 8 KiB per state); this thread owns 32
-// columns (half a block) of row r.  The new block absmax combines the two
-// halves through shared memory; the weights use the new float32 moments,
-// then the moments are quantised with the new absmax.
+// INT8 states: a chunk is 128 rows x 64 columns (one code block per row;
+// codes 8 KiB per state in shared memory); this thread owns 16 columns (a
+// quarter block) of row r, its 16 bf16 weights in registers (`wv`).  The new
+// block absmax combines the four quarters through shared memory; the weights
+// use the new float32 moments, then the moments are quantised with the new
+// absmax.
 template <int KIND>
-__device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int r, int half,
-                                               int64_t e0, float a1, float a2, float* n1_out,
-                                               float* n2_out, const GemmParams& p) {
-  constexpr int kOffS1 = 16384, kOffS2 = 24576, kOffAmax = 32768;
-  float m[32], v[32];  // new float32 moments, kept for the requantisation
-  uint8_t* wbox = buf + half * 8192;
+__device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int r, int sub,
+                                               int64_t e0, uint4 (&wv)[2], float a1, float a2,
+                                               float* n1_out, float* n2_out, int nthreads,
+                                               const GemmParams& p) {
+  constexpr int kOffS1 = 0, kOffS2 = 8192, kOffAmax = 16384;
+  float g[16], w[16], m[16], v[16];
+  ptx::tmem_ld_32x32b_x16(taddr, g);
+  unpack_bf16x8(wv[0], w);
+  unpack_bf16x8(wv[1], w + 8);
+  const uint4 c1 = uses_s1(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub))
+                                 : make_uint4(0, 0, 0, 0);
+  const uint4 c2 = uses_s2(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub))
+                                 : make_uint4(0, 0, 0, 0);
+  const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
   float n1 = 0.f, n2 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {  // 16 columns at a time
-    float g[16], w[16];
-    ptx::tmem_ld_32x32b_x16(taddr + 16 * i, g);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(wbox + sw64(r, 2 * i)), w);
-    unpack_bf16x8(*reinterpret_cast<const uint4*>(wbox + sw64(r, 2 * i + 1)), w + 8);
-    const uint4 c1 = uses_s1(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, 2 * half + i))
-                                   : make_uint4(0, 0, 0, 0);
-    const uint4 c2 = uses_s2(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, 2 * half + i))
-                                   : make_uint4(0, 0, 0, 0);
-    const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t b1 = (q1[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      const uint32_t b2 = (q2[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      float mj = uses_s1(KIND) ? dev::dequant<true>(static_cast<int>(static_cast<int8_t>(b1)), a1) : 0.f;
-      float vj = uses_s2(KIND) ? dev::dequant<false>(static_cast<int>(b2), a2) : 0.f;
-      dev::rule<KIND>(w[j], g[j], mj, vj, p.sc);
-      if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, mj);
-      if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, vj);
-      m[16 * i + j] = mj;
-      v[16 * i + j] = vj;
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 rnd = dev::sr_words((static_cast<uint64_t>(e0) >> 3) + 2 * i + h, p.seed, p.step);
-      *reinterpret_cast<uint4*>(wbox + sw64(r, 2 * i + h)) = pack_sr_bf16x8(w + 8 * h, rnd);
-    }
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t b1 = (q1[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+    const uint32_t b2 = (q2[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+    m[j] = uses_s1(KIND) ? dev::dequant<true>(static_cast<int>(static_cast<int8_t>(b1)), a1) : 0.f;
+    v[j] = uses_s2(KIND) ? dev::dequant<false>(static_cast<int>(b2), a2) : 0.f;
+    dev::rule<KIND>(w[j], g[j], m[j], v[j], p.sc);
+    if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, m[j]);
+    if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, v[j]);
   }
-  float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][half][row]
-  amax[(0 * 2 + half) * 128 + r] = n1;
-  amax[(1 * 2 + half) * 128 + r] = n2;
-  ptx::bar_sync(kEpiBarrier, kEpiThreads);
-  n1 = fmaxf(n1, amax[(0 * 2 + (half ^ 1)) * 128 + r]);
-  n2 = fmaxf(n2, amax[(1 * 2 + (half ^ 1)) * 128 + r]);
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
+  for (int h = 0; h < 2; ++h)
+    wv[h] = pack_sr_bf16x8(w + 8 * h, dev::sr_words((static_cast<uint64_t>(e0) >> 3) + h, p.seed, p.step));
+  float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][quarter][row]
+  amax[(0 * 4 + sub) * 128 + r] = n1;
+  amax[(1 * 4 + sub) * 128 + r] = n2;
+  ptx::bar_sync(kEpiBarrier, nthreads);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (uses_s1(KIND))
-        o1[j >> 2] |= (static_cast<uint32_t>(dev::quant<true>(m[16 * i + j], n1)) & 0xFFu) << (8 * (j & 3));
-      if (uses_s2(KIND))
-        o2[j >> 2] |= (static_cast<uint32_t>(dev::quant<false>(v[16 * i + j], n2)) & 0xFFu) << (8 * (j & 3));
-    }
-    if (uses_s1(KIND))
-      *reinterpret_cast<uint4*>(buf + kOffS1 + sw64(r, 2 * half + i)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-    if (uses_s2(KIND))
-      *reinterpret_cast<uint4*>(buf + kOffS2 + sw64(r, 2 * half + i)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+  for (int o = 0; o < 4; ++o) {
+    n1 = fmaxf(n1, amax[(0 * 4 + o) * 128 + r]);
+    n2 = fmaxf(n2, amax[(1 * 4 + o) * 128 + r]);
   }
+  uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    if (uses_s1(KIND)) o1[j >> 2] |= (static_cast<uint32_t>(dev::quant<true>(m[j], n1)) & 0xFFu) << (8 * (j & 3));
+    if (uses_s2(KIND)) o2[j >> 2] |= (static_cast<uint32_t>(dev::quant<false>(v[j], n2)) & 0xFFu) << (8 * (j & 3));
+  }
+  if (uses_s1(KIND))
+    *reinterpret_cast<uint4*>(buf + kOffS1 + sw64(r, sub)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+  if (uses_s2(KIND))
+    *reinterpret_cast<uint4*>(buf + kOffS2 + sw64(r, sub)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
   *n1_out = n1;
   *n2_out = n2;
 }
@@ -715,11 +705,12 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
   constexpr bool I8 = (SDT == kSInt8);
   constexpr int kCC = I8 ? 64 : 32;
   constexpr int kChunks = kTileN / kCC;
-  constexpr int kOffS1 = I8 ? 16384 : 8192;
-  constexpr int kOffS2 = 24576;
-  constexpr uint32_t kTx = (I8 ? 16384u : 8192u) + (U1 ? (I8 ? 8192u : 16384u) : 0u) +
-                           (U2 ? (I8 ? 8192u : 16384u) : 0u);
-  const int quarter = warp & 3, half = (warp - 2) >> 2;
+  constexpr int kOffS1 = 0;
+  constexpr int kOffS2 = I8 ? 8192 : 16384;
+  constexpr uint32_t kTx = (U1 ? (I8 ? 8192u : 16384u) : 0u) + (U2 ? (I8 ? 8192u : 16384u) : 0u);
+  constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
+  constexpr int kNT = 32 * kNumEpiWarpsStaged;  // epilogue threads
+  const int quarter = warp & 3, sub = (warp - 2) >> 2;  // TMEM lane quarter, column quarter
   const int r = quarter * 32 + lane;
   const bool io = (warp == 2 && lane == 0);
   const int64_t K = p.Ncols;
@@ -742,8 +733,6 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
     uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
     uint64_t* bar = &ss->epi_full[j & 1];
     ptx::mbar_arrive_expect_tx(bar, kTx);
-    ptx::tma_load_2d_hint(mW, bar, buf, col0, row0, pol);
-    if (I8) ptx::tma_load_2d_hint(mW, bar, buf + 8192, col0 + 32, row0, pol);
     if (U1) ptx::tma_load_2d_hint(mS1, bar, buf + kOffS1, col0, row0, pol);
     if (U2) ptx::tma_load_2d_hint(mS2, bar, buf + kOffS2, col0, row0, pol);
   };
@@ -751,19 +740,38 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
     int row0, col0;
     where(j, row0, col0);
     const uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
-    ptx::tma_store_2d_hint(mW, buf, col0, row0, pol);
-    if (I8) ptx::tma_store_2d_hint(mW, buf + 8192, col0 + 32, row0, pol);
     if (U1) ptx::tma_store_2d_hint(mS1, buf + kOffS1, col0, row0, pol);
     if (U2) ptx::tma_store_2d_hint(mS2, buf + kOffS2, col0, row0, pol);
     ptx::bulk_commit_group();
   };
 
+  // This thread's weights of chunk j: loaded from global one chunk ahead (they
+  // are 2 of the 10 or 4.25 bytes per element, so they bypass the staging).
+  // Plain (L1-allocating) accesses: the four warps that own the 64 bytes of a
+  // row's chunk then share one L1 fill instead of four L2 requests.
+  auto w_ptr = [&](int j, bool& ok) -> uint16_t* {
+    int row0, col0;
+    where(j, row0, col0);
+    const int64_t row = static_cast<int64_t>(row0) + r;
+    const int col = col0 + sub * kWPerThread;
+    ok = row < p.M && col < K;
+    return static_cast<uint16_t*>(p.W) + row * K + col;
+  };
+  auto w_load = [&](int j, uint4 (&v)[kWPerThread / 8]) {
+    bool ok;
+    const uint16_t* q = w_ptr(j, ok);
+#pragma unroll
+    for (int h = 0; h < kWPerThread / 8; ++h)
+      v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
+  };
+  uint4 wnext[kWPerThread / 8];
   int issued = 0, consumed = 0, local = -1;
   float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};  // old INT8 scales
   if (io && total > 0) {
     issue(0);
     issued = 1;
   }
+  if (total > 0) w_load(0, wnext);
   for (int j = 0; j < total; ++j) {
     const int c = j % kChunks;
     int row0, col0;
@@ -790,31 +798,44 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
       issued = j + 2;
     }
     if (lane == 0 && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
-    if (ptx::bar_red_or(kEpiBarrier, kEpiThreads, !ok)) break;  // same verdict in every warp
+    if (ptx::bar_red_or(kEpiBarrier, kNT, !ok)) break;  // same verdict in every warp
     consumed = j + 1;
+    uint4 wcur[kWPerThread / 8];
+#pragma unroll
+    for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
+    if (j + 1 < total) w_load(j + 1, wnext);
     ptx::tc_fence_after();
     const int acc = local & 1;
     uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
-    const int col = col0 + half * (kCC / 2);
+    const int col = col0 + sub * (kCC / 4);
     const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                           static_cast<uint32_t>(acc * kTileN + c * kCC + half * (kCC / 2));
+                           static_cast<uint32_t>(acc * kTileN + c * kCC + sub * (kCC / 4));
     const int64_t e0 = row * K + col;
     if (I8) {
       float n1, n2;
       const float o1 = c == 0 ? a1[0] : c == 1 ? a1[1] : c == 2 ? a1[2] : a1[3];
       const float o2 = c == 0 ? a2[0] : c == 1 ? a2[1] : c == 2 ? a2[2] : a2[3];
-      epi_chunk_int8<KIND>(taddr, buf, r, half, e0, o1, o2, &n1, &n2, p);
-      if (half == 0 && row < p.M && col0 < K) {
+      epi_chunk_int8<KIND>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
+                           &n1, &n2, kNT, p);
+      if (sub == 0 && row < p.M && col0 < K) {
         const int64_t sidx = row * (K / 64) + col0 / 64;
         if (U1) p.s1_scale[sidx] = n1;
         if (U2) p.s2_scale[sidx] = n2;
       }
     } else {
-      epi_chunk_fp32<KIND>(taddr, buf, r, half, e0, p);
+      epi_chunk_fp32<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
+    }
+    {
+      bool ok;
+      uint16_t* q = w_ptr(j, ok);
+      if (ok) {
+#pragma unroll
+        for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
+      }
     }
     if (c == kChunks - 1) ptx::tc_fence_before();
     ptx::fence_proxy_async_smem();
-    ptx::bar_sync(kEpiBarrier, kEpiThreads);
+    ptx::bar_sync(kEpiBarrier, kNT);
     if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
     if (io) store(j);
   }
@@ -845,7 +866,7 @@ __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mW, con
 // ------------------------------------------------------------------ kernel
 
 template <int MODE, int WDT, int SDT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapS1,
               const __grid_constant__ CUtensorMap mapS2, const GemmParams p) {
@@ -869,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&ss->tmem_full[a], 1);
-      ptx::mbar_init(&ss->tmem_empty[a], 2 * kNumEpiWarps);  // the leader's: both CTAs' warps
+      ptx::mbar_init(&ss->tmem_empty[a], 2 * Cfg::kEpiWarps);  // the leader's: both CTAs' warps
       ptx::mbar_init(&ss->epi_full[a], 1);
     }
     ptx::mbar_init(&ss->mma_done, 1);
@@ -913,12 +934,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Launch on clusters of two CTAs (the tcgen05 pair); grid is a multiple of 2.
 template <typename Kernel>
-inline cudaError_t launch_pair(Kernel k, int grid, int smem, cudaStream_t s, const CUtensorMap& a,
+inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaStream_t s,
+                               const CUtensorMap& a,
                                const CUtensorMap& b, const CUtensorMap& w, const CUtensorMap& s1,
                                const CUtensorMap& s2, const GemmParams& p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];

@@ -21,8 +21,10 @@ gradient (g <- g + wd w) for the others, as torch.optim does by default.
 
 Arithmetic: every scalar that depends only on the step and the hyper-parameters
 is formed on the host in float64 from the float32 hyper-parameters and rounded
-once to float32; every per-element operation is one IEEE float32 operation in
-the order written in each rule below (no fused multiply-add).
+once to float32 (bias corrections enter as reciprocals where that saves a
+per-element division: AdamW scales sqrt(v) by 1/sqrt(1 - b2^t), NAdam scales
+v by 1/(1 - b2^t)); every per-element operation is one IEEE float32 operation
+in the order written in each rule below (no fused multiply-add).
 
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
 """
@@ -76,7 +78,7 @@ def step_scalars(kind: int, hp: Hparams, step: int) -> dict:
         c1 = 1.0 - b1 ** t
         c2 = 1.0 - b2 ** t
         sc.update(decay=_f(1.0 - lr * wd), b1=_f(b1), omb1=_f(1.0 - b1), b2=_f(b2),
-                  omb2=_f(1.0 - b2), step_size=_f(lr / c1), sqrt_c2=_f(math.sqrt(c2)),
+                  omb2=_f(1.0 - b2), step_size=_f(lr / c1), inv_sqrt_c2=_f(1.0 / math.sqrt(c2)),
                   eps=_f(eps))
     elif kind == NADAM:
         c2 = 1.0 - b2 ** t
@@ -86,7 +88,7 @@ def step_scalars(kind: int, hp: Hparams, step: int) -> dict:
         for i in range(step):
             prod_t *= mu[i]
         prod_next = prod_t * mu_next
-        sc.update(b1=_f(b1), omb1=_f(1.0 - b1), b2=_f(b2), omb2=_f(1.0 - b2), c2=_f(c2),
+        sc.update(b1=_f(b1), omb1=_f(1.0 - b1), b2=_f(b2), omb2=_f(1.0 - b2), inv_c2=_f(1.0 / c2),
                   eps=_f(eps), coef_g=_f(lr * (1.0 - mu_t) / (1.0 - prod_t)),
                   coef_m=_f(lr * mu_next / (1.0 - prod_next)))
     elif kind == RADAM:
@@ -139,13 +141,13 @@ def apply_rule(kind: int, sc: dict, w, g, s1=None, s2=None):
     if kind == ADAMW:
         m = sc["b1"] * s1 + sc["omb1"] * g
         v = sc["b2"] * s2 + sc["omb2"] * (g * g)
-        denom = np.sqrt(v) / sc["sqrt_c2"] + sc["eps"]
+        denom = np.sqrt(v) * sc["inv_sqrt_c2"] + sc["eps"]
         w = w * sc["decay"] - sc["step_size"] * (m / denom)
         return w, m, v
     if kind == NADAM:
         m = sc["b1"] * s1 + sc["omb1"] * g
         v = sc["b2"] * s2 + sc["omb2"] * (g * g)
-        denom = np.sqrt(v / sc["c2"]) + sc["eps"]
+        denom = np.sqrt(v * sc["inv_c2"]) + sc["eps"]
         w = w - sc["coef_g"] * (g / denom)
         w = w - sc["coef_m"] * (m / denom)
         return w, m, v
