@@ -41,14 +41,21 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// try_wait suspends the thread until the phase completes or the suspend-time
+// hint (nanoseconds) runs out.  A long hint keeps a waiting thread from
+// re-issuing the wait (and the timer checks around it) in a loop, which takes
+// issue slots from the MMA and copy threads sharing its scheduler; a completed
+// phase still wakes it at once.
+constexpr uint32_t kWaitSuspendNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "n"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }

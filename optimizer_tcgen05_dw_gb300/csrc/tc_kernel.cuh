@@ -55,8 +55,8 @@ struct SharedState {
 };
 
 // Per-instantiation layout (per CTA).  The FORGE step with bf16 weights
-// stages its weight/state tiles through shared memory with TMA (two 40 KiB
-// chunk buffers) next to a 4-stage operand ring; the other modes use a
+// stages its optimizer-state tiles through shared memory with TMA (two 32 KiB
+// chunk buffers) next to a 5-stage operand ring; the other modes use a
 // deeper ring.  A stage holds 128 rows of A and 128 columns of B (half of the
 // pair's 256): 32 KiB at 64 tokens.
 constexpr int kEpiBufBytes = 32768;
@@ -538,12 +538,12 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
   for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs(), ++local) {
     const int acc = local & 1;
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
-    // One lane waits and the verdict is broadcast, so the warp stays
-    // converged for the .sync.aligned tensor-memory loads that follow.
-    int ok = 0;
-    if (lane == 0) ok = bounded_wait(&ss->tmem_full[acc], aph, p, ss) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-    if (!ok) break;
+    // One thread waits; the others block on the named barrier, which also
+    // hands every warp the same verdict, so warps stay converged for the
+    // .sync.aligned tensor-memory loads that follow.
+    bool ok = true;
+    if (warp == 2 && lane == 0) ok = bounded_wait(&ss->tmem_full[acc], aph, p, ss);
+    if (ptx::bar_red_or(kEpiBarrier, 32 * kNumEpiWarps, !ok)) break;
     ptx::tc_fence_after();
     int tm, tn;
     tile_coords(tile, p, tm, tn);
@@ -790,15 +790,18 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
           }
         }
       }
-      if (lane == 0) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
+      if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
     }
     if (io && j + 1 < total) {
       ptx::bulk_wait_group_read0();
       issue(j + 1);
       issued = j + 2;
     }
-    if (lane == 0 && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
-    if (ptx::bar_red_or(kEpiBarrier, kNT, !ok)) break;  // same verdict in every warp
+    // Only the I/O thread waits (on the accumulator above and on the staged
+    // chunk here); the rest block on the named barrier, which orders their
+    // reads after its waits and gives every warp the same verdict.
+    if (io && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
+    if (ptx::bar_red_or(kEpiBarrier, kNT, !ok)) break;
     consumed = j + 1;
     uint4 wcur[kWPerThread / 8];
 #pragma unroll
