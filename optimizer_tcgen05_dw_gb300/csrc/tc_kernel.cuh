@@ -60,7 +60,8 @@ struct SharedState {
 // deeper ring.  A stage holds 128 rows of A and 128 columns of B (half of the
 // pair's 256): 32 KiB at 64 tokens.
 constexpr int kEpiBufBytes = 32768;
-constexpr int kEpiBarrier = 1;  // named barrier of the epilogue warps
+constexpr int kEpiBarrier = 1;       // named barrier of the epilogue warps
+constexpr int kEpiInnerBarrier = 2;  // the staged epilogue's compute warps only
 constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 
 template <int MODE, int WDT>
@@ -77,7 +78,7 @@ struct KCfg {
   // TMA warp, MMA warp, epilogue warps (four per 32-lane quarter of TMEM in the
   // staged epilogue, two in the plain ones).
   static constexpr int kEpiWarps = kTmaEpi ? kNumEpiWarpsStaged : kNumEpiWarps;
-  static constexpr int kThreads = 32 * (2 + kEpiWarps);
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + (kTmaEpi ? 1 : 0));  // + the I/O warp
 };
 static_assert(sizeof(SharedState) <= 512, "shared state region");
 static_assert(KCfg<kModeFusedOpt, kWBf16>::kStg <= 8 && KCfg<kModeWgradStore, kWBf16>::kStg <= 8 &&
@@ -645,10 +646,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
                                                float* n1_out, float* n2_out, int nthreads,
                                                const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 8192, kOffAmax = 16384;
-  float g[16], w[16], m[16], v[16];
-  ptx::tmem_ld_32x32b_x16(taddr, g);
-  unpack_bf16x8(wv[0], w);
-  unpack_bf16x8(wv[1], w + 8);
+  float m[16], v[16];  // the new moments stay live until the block absmax is known
   const uint4 c1 = uses_s1(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub))
                                  : make_uint4(0, 0, 0, 0);
   const uint4 c2 = uses_s2(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub))
@@ -656,22 +654,27 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
   float n1 = 0.f, n2 = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t b1 = (q1[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-    const uint32_t b2 = (q2[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-    m[j] = uses_s1(KIND) ? dev::dequant<true>(static_cast<int>(static_cast<int8_t>(b1)), a1) : 0.f;
-    v[j] = uses_s2(KIND) ? dev::dequant<false>(static_cast<int>(b2), a2) : 0.f;
-    dev::rule<KIND>(w[j], g[j], m[j], v[j], p.sc);
-    if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, m[j]);
-    if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, v[j]);
-  }
+  for (int h = 0; h < 2; ++h) {  // two halves of 8 columns: gradient and weights
+    float g[8], w[8];
+    ptx::tmem_ld_32x32b_x8(taddr + 8 * h, g);
+    unpack_bf16x8(wv[h], w);
 #pragma unroll
-  for (int h = 0; h < 2; ++h)
-    wv[h] = pack_sr_bf16x8(w + 8 * h, dev::sr_words((static_cast<uint64_t>(e0) >> 3) + h, p.seed, p.step));
+    for (int i = 0; i < 8; ++i) {
+      const int j = 8 * h + i;
+      const uint32_t b1 = (q1[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      const uint32_t b2 = (q2[j >> 2] >> (8 * (j & 3))) & 0xFFu;
+      m[j] = uses_s1(KIND) ? dev::dequant<true>(static_cast<int>(static_cast<int8_t>(b1)), a1) : 0.f;
+      v[j] = uses_s2(KIND) ? dev::dequant<false>(static_cast<int>(b2), a2) : 0.f;
+      dev::rule<KIND>(w[i], g[i], m[j], v[j], p.sc);
+      if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, m[j]);
+      if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, v[j]);
+    }
+    wv[h] = pack_sr_bf16x8(w, dev::sr_words((static_cast<uint64_t>(e0) >> 3) + h, p.seed, p.step));
+  }
   float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][quarter][row]
   amax[(0 * 4 + sub) * 128 + r] = n1;
   amax[(1 * 4 + sub) * 128 + r] = n2;
-  ptx::bar_sync(kEpiBarrier, nthreads);
+  ptx::bar_sync(kEpiInnerBarrier, nthreads);
 #pragma unroll
   for (int o = 0; o < 4; ++o) {
     n1 = fmaxf(n1, amax[(0 * 4 + o) * 128 + r]);
@@ -691,155 +694,119 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   *n2_out = n2;
 }
 
-// The epilogue of the FORGE step for bf16 weights.  One thread (warp 2,
-// lane 0) moves data: for chunk j+1 it waits until the bulk stores of chunk
-// j-1 have read their buffer, then issues the TMA loads of the W / state
-// boxes of chunk j+1; after all 256 epilogue threads have updated chunk j in
-// shared memory it issues the TMA stores of chunk j.  Loads of the next
-// tile's first chunks overlap the wait for its accumulator.
+// Chunk geometry of the staged FORGE epilogue for one state dtype.  A chunk
+// is 128 rows x kCC columns of the CTA's 128 x 256 half of a pair tile:
+// fp32 states 32 columns (m and v 16 KiB each in shared memory), INT8 states
+// 64 columns (one code block per row; 8 KiB of codes per state).
 template <int KIND, int SDT>
-__device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
-                                  const CUtensorMap* mS2, const GemmParams& p, SharedState* ss,
-                                  uint8_t* epi, int warp, int lane, uint32_t rank) {
-  constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
-  constexpr bool I8 = (SDT == kSInt8);
-  constexpr int kCC = I8 ? 64 : 32;
-  constexpr int kChunks = kTileN / kCC;
-  constexpr int kOffS1 = 0;
-  constexpr int kOffS2 = I8 ? 8192 : 16384;
-  constexpr uint32_t kTx = (U1 ? (I8 ? 8192u : 16384u) : 0u) + (U2 ? (I8 ? 8192u : 16384u) : 0u);
-  constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
-  constexpr int kNT = 32 * kNumEpiWarpsStaged;  // epilogue threads
-  const int quarter = warp & 3, sub = (warp - 2) >> 2;  // TMEM lane quarter, column quarter
-  const int r = quarter * 32 + lane;
-  const bool io = (warp == 2 && lane == 0);
-  const int64_t K = p.Ncols;
-  const int my_tiles = p.num_tiles > pair_id() ? (p.num_tiles - 1 - pair_id()) / num_pairs() + 1 : 0;
-  const int total = my_tiles * kChunks;
-  const uint32_t empty0 = ptx::mapa(ptx::smem_addr(&ss->tmem_empty[0]), 0);
+struct StagedGeom {
+  static constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
+  static constexpr bool I8 = (SDT == kSInt8);
+  static constexpr int kCC = I8 ? 64 : 32;
+  static constexpr int kChunks = kTileN / kCC;
+  static constexpr int kOffS1 = 0;
+  static constexpr int kOffS2 = I8 ? 8192 : 16384;
+  static constexpr uint32_t kStateBytes = I8 ? 8192u : 16384u;
+  static constexpr uint32_t kTx = (U1 ? kStateBytes : 0u) + (U2 ? kStateBytes : 0u);
+  static constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
+  static constexpr int kNC = 32 * kNumEpiWarpsStaged;  // compute threads
+  static constexpr int kNB = kNC + 32;                 // compute threads + the I/O warp
+};
 
-  auto where = [&](int j, int& row0, int& col0) {
+// The pair's tiles in order, and the origin of each in this CTA: its first W
+// row and first column.  The origins of the tile in hand and of the next one
+// are kept, found once per tile (tile_coords divides): chunk j and the chunk
+// j + 1 prefetched ahead of it always lie in one of the two.
+template <int kChunks>
+struct TileWalk {
+  int cur_tile = 0, cur_row0 = 0, cur_col0 = 0, nxt_row0 = 0, nxt_col0 = 0;
+  int my_tiles = 0;
+  __device__ __forceinline__ void origin(int i, const GemmParams& p, uint32_t rank, int& row0,
+                                         int& col0) const {
     int tm, tn;
-    tile_coords(pair_id() + (j / kChunks) * num_pairs(), p, tm, tn);
+    tile_coords(pair_id() + i * num_pairs(), p, tm, tn);
     row0 = tm * kPairM + static_cast<int>(rank) * kTileM;
-    col0 = tn * kTileN + (j % kChunks) * kCC;
-  };
+    col0 = tn * kTileN;
+  }
+  __device__ __forceinline__ void init(const GemmParams& p, uint32_t rank) {
+    my_tiles = p.num_tiles > pair_id() ? (p.num_tiles - 1 - pair_id()) / num_pairs() + 1 : 0;
+    if (my_tiles > 0) origin(0, p, rank, cur_row0, cur_col0);
+    if (my_tiles > 1) origin(1, p, rank, nxt_row0, nxt_col0);
+  }
+  // Tile `local` (> 0) becomes the one in hand.
+  __device__ __forceinline__ void advance(int local, const GemmParams& p, uint32_t rank) {
+    cur_tile = local;
+    cur_row0 = nxt_row0;
+    cur_col0 = nxt_col0;
+    if (local + 1 < my_tiles) origin(local + 1, p, rank, nxt_row0, nxt_col0);
+  }
+  __device__ __forceinline__ void where(int j, int kCC, int& row0, int& col0) const {
+    const bool next = (j / kChunks) != cur_tile;
+    row0 = next ? nxt_row0 : cur_row0;
+    col0 = (next ? nxt_col0 : cur_col0) + (j % kChunks) * kCC;
+  }
+};
+
+// The I/O warp of the FORGE epilogue (bf16 weights).  Its lane 0 moves the
+// optimizer states: before the compute warps start chunk j it waits for the
+// accumulator (first chunk of a tile) and for chunk j's staged states; while
+// they work on chunk j it waits until the bulk stores of chunk j-1 have read
+// their buffer and issues the TMA loads of chunk j+1 into it; after they have
+// written chunk j back to shared memory it issues chunk j's TMA stores.  None
+// of its waits sits between two chunks of the compute warps.
+template <int KIND, int SDT>
+__device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
+                                 const GemmParams& p, SharedState* ss, uint8_t* epi, int lane,
+                                 uint32_t rank) {
+  using G = StagedGeom<KIND, SDT>;
+  TileWalk<G::kChunks> walk;
+  walk.init(p, rank);
+  const int total = walk.my_tiles * G::kChunks;
+  const bool io = (lane == 0);
   // Weight/state lines are touched once per step: evict-first in L2, so they
   // do not displace the operand tiles the main loop re-reads from L2.
   const uint64_t pol = evict_first_policy();
   auto issue = [&](int j) {
     int row0, col0;
-    where(j, row0, col0);
+    walk.where(j, G::kCC, row0, col0);
     uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
     uint64_t* bar = &ss->epi_full[j & 1];
-    ptx::mbar_arrive_expect_tx(bar, kTx);
-    if (U1) ptx::tma_load_2d_hint(mS1, bar, buf + kOffS1, col0, row0, pol);
-    if (U2) ptx::tma_load_2d_hint(mS2, bar, buf + kOffS2, col0, row0, pol);
+    ptx::mbar_arrive_expect_tx(bar, G::kTx);
+    if (G::U1) ptx::tma_load_2d_hint(mS1, bar, buf + G::kOffS1, col0, row0, pol);
+    if (G::U2) ptx::tma_load_2d_hint(mS2, bar, buf + G::kOffS2, col0, row0, pol);
   };
   auto store = [&](int j) {
     int row0, col0;
-    where(j, row0, col0);
+    walk.where(j, G::kCC, row0, col0);
     const uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
-    if (U1) ptx::tma_store_2d_hint(mS1, buf + kOffS1, col0, row0, pol);
-    if (U2) ptx::tma_store_2d_hint(mS2, buf + kOffS2, col0, row0, pol);
+    if (G::U1) ptx::tma_store_2d_hint(mS1, buf + G::kOffS1, col0, row0, pol);
+    if (G::U2) ptx::tma_store_2d_hint(mS2, buf + G::kOffS2, col0, row0, pol);
     ptx::bulk_commit_group();
   };
-
-  // This thread's weights of chunk j: loaded from global one chunk ahead (they
-  // are 2 of the 10 or 4.25 bytes per element, so they bypass the staging).
-  // Plain (L1-allocating) accesses: the four warps that own the 64 bytes of a
-  // row's chunk then share one L1 fill instead of four L2 requests.
-  auto w_ptr = [&](int j, bool& ok) -> uint16_t* {
-    int row0, col0;
-    where(j, row0, col0);
-    const int64_t row = static_cast<int64_t>(row0) + r;
-    const int col = col0 + sub * kWPerThread;
-    ok = row < p.M && col < K;
-    return static_cast<uint16_t*>(p.W) + row * K + col;
-  };
-  auto w_load = [&](int j, uint4 (&v)[kWPerThread / 8]) {
-    bool ok;
-    const uint16_t* q = w_ptr(j, ok);
-#pragma unroll
-    for (int h = 0; h < kWPerThread / 8; ++h)
-      v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
-  };
-  uint4 wnext[kWPerThread / 8];
   int issued = 0, consumed = 0, local = -1;
-  float a1[4] = {0.f, 0.f, 0.f, 0.f}, a2[4] = {0.f, 0.f, 0.f, 0.f};  // old INT8 scales
   if (io && total > 0) {
     issue(0);
     issued = 1;
   }
-  if (total > 0) w_load(0, wnext);
   for (int j = 0; j < total; ++j) {
-    const int c = j % kChunks;
-    int row0, col0;
-    where(j, row0, col0);
-    const int64_t row = static_cast<int64_t>(row0) + r;
+    const int c = j % G::kChunks;
     bool ok = true;
     if (c == 0) {
       ++local;
-      if (I8 && row < p.M) {  // old block scales of this row of the tile
-        const int64_t nb = K / 64, b0 = col0 / 64;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if ((b0 + q) * 64 < K) {
-            if (U1) a1[q] = p.s1_scale[row * nb + b0 + q];
-            if (U2) a2[q] = p.s2_scale[row * nb + b0 + q];
-          }
-        }
-      }
+      if (local > 0) walk.advance(local, p, rank);
       if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
     }
+    if (io && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
+    // Releases the compute warps into chunk j (ordering their tensor- and
+    // shared-memory reads after the waits above), or stops everyone.
+    if (ptx::bar_red_or(kEpiBarrier, G::kNB, !ok)) break;
+    consumed = j + 1;
     if (io && j + 1 < total) {
-      ptx::bulk_wait_group_read0();
+      ptx::bulk_wait_group_read0();  // chunk j-1's stores have read buffer (j+1)&1
       issue(j + 1);
       issued = j + 2;
     }
-    // Only the I/O thread waits (on the accumulator above and on the staged
-    // chunk here); the rest block on the named barrier, which orders their
-    // reads after its waits and gives every warp the same verdict.
-    if (io && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
-    if (ptx::bar_red_or(kEpiBarrier, kNT, !ok)) break;
-    consumed = j + 1;
-    uint4 wcur[kWPerThread / 8];
-#pragma unroll
-    for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
-    if (j + 1 < total) w_load(j + 1, wnext);
-    ptx::tc_fence_after();
-    const int acc = local & 1;
-    uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
-    const int col = col0 + sub * (kCC / 4);
-    const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                           static_cast<uint32_t>(acc * kTileN + c * kCC + sub * (kCC / 4));
-    const int64_t e0 = row * K + col;
-    if (I8) {
-      float n1, n2;
-      const float o1 = c == 0 ? a1[0] : c == 1 ? a1[1] : c == 2 ? a1[2] : a1[3];
-      const float o2 = c == 0 ? a2[0] : c == 1 ? a2[1] : c == 2 ? a2[2] : a2[3];
-      epi_chunk_int8<KIND>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
-                           &n1, &n2, kNT, p);
-      if (sub == 0 && row < p.M && col0 < K) {
-        const int64_t sidx = row * (K / 64) + col0 / 64;
-        if (U1) p.s1_scale[sidx] = n1;
-        if (U2) p.s2_scale[sidx] = n2;
-      }
-    } else {
-      epi_chunk_fp32<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
-    }
-    {
-      bool ok;
-      uint16_t* q = w_ptr(j, ok);
-      if (ok) {
-#pragma unroll
-        for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
-      }
-    }
-    if (c == kChunks - 1) ptx::tc_fence_before();
-    ptx::fence_proxy_async_smem();
-    ptx::bar_sync(kEpiBarrier, kNT);
-    if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
+    ptx::bar_sync(kEpiBarrier, G::kNB);  // chunk j is back in shared memory
     if (io) store(j);
   }
   if (io) {
@@ -849,20 +816,119 @@ __device__ void epilogue_tma_role(const CUtensorMap* mW, const CUtensorMap* mS1,
   }
 }
 
+// A compute warp of the FORGE epilogue (bf16 weights).  Warp w reads TMEM
+// lanes 32*(w%4).. (its rows) and a quarter of each chunk's columns; its bf16
+// weights (and old INT8 scales) come straight from global memory one chunk
+// ahead, its states from the staged chunk in shared memory.
+template <int KIND, int SDT>
+__device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint8_t* epi,
+                                      int warp, int lane, uint32_t rank) {
+  using G = StagedGeom<KIND, SDT>;
+  constexpr int kCC = G::kCC, kChunks = G::kChunks, kWPerThread = G::kWPerThread;
+  const int quarter = warp & 3, sub = (warp - 2) >> 2;  // TMEM lane quarter, column quarter
+  const int r = quarter * 32 + lane;
+  const int64_t K = p.Ncols;
+  TileWalk<kChunks> walk;
+  walk.init(p, rank);
+  const int total = walk.my_tiles * kChunks;
+  const uint32_t empty0 = ptx::mapa(ptx::smem_addr(&ss->tmem_empty[0]), 0);
+
+  // This thread's weights of chunk j (and, for INT8 states, the old absmax of
+  // its code block): loaded one chunk ahead.  They are 2 of the 10 or 4.25
+  // bytes per element, so they bypass the staging; plain (L1-allocating)
+  // loads let the four warps that own the 64 bytes of a row's chunk share one
+  // L1 fill instead of four L2 requests.
+  auto prefetch = [&](int j, uint4 (&v)[kWPerThread / 8], float& o1, float& o2) {
+    int row0, col0;
+    walk.where(j, kCC, row0, col0);
+    const int64_t row = static_cast<int64_t>(row0) + r;
+    const int col = col0 + sub * kWPerThread;
+    const bool ok = row < p.M && col < K;
+    const uint16_t* q = static_cast<const uint16_t*>(p.W) + row * K + col;
+#pragma unroll
+    for (int h = 0; h < kWPerThread / 8; ++h)
+      v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
+    if (G::I8) {  // one code block per chunk
+      const bool okb = row < p.M && col0 < K;
+      const int64_t sidx = row * (K / 64) + col0 / 64;
+      if (G::U1) o1 = okb ? p.s1_scale[sidx] : 0.f;
+      if (G::U2) o2 = okb ? p.s2_scale[sidx] : 0.f;
+    }
+  };
+  uint4 wnext[kWPerThread / 8];
+  float o1next = 0.f, o2next = 0.f;  // old INT8 scales of the next chunk
+  int local = -1;
+  if (total > 0) prefetch(0, wnext, o1next, o2next);
+  for (int j = 0; j < total; ++j) {
+    const int c = j % kChunks;
+    if (c == 0) {
+      ++local;
+      if (local > 0) walk.advance(local, p, rank);
+    }
+    if (ptx::bar_red_or(kEpiBarrier, G::kNB, false)) break;  // the I/O warp's verdict
+    int row0, col0;
+    walk.where(j, kCC, row0, col0);
+    const int64_t row = static_cast<int64_t>(row0) + r;
+    uint4 wcur[kWPerThread / 8];
+#pragma unroll
+    for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
+    const float o1 = o1next, o2 = o2next;
+    if (j + 1 < total) prefetch(j + 1, wnext, o1next, o2next);
+    ptx::tc_fence_after();
+    const int acc = local & 1;
+    uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
+    const int col = col0 + sub * kWPerThread;
+    const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                           static_cast<uint32_t>(acc * kTileN + c * kCC + sub * kWPerThread);
+    const int64_t e0 = row * K + col;
+    if (G::I8) {
+      float n1, n2;
+      epi_chunk_int8<KIND>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
+                           &n1, &n2, G::kNC, p);
+      if (sub == 0 && row < p.M && col0 < K) {
+        const int64_t sidx = row * (K / 64) + col0 / 64;
+        if (G::U1) p.s1_scale[sidx] = n1;
+        if (G::U2) p.s2_scale[sidx] = n2;
+      }
+    } else {
+      epi_chunk_fp32<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
+    }
+    if (row < p.M && col < K) {
+      uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
+#pragma unroll
+      for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
+    }
+    if (c == kChunks - 1) ptx::tc_fence_before();
+    ptx::fence_proxy_async_smem();
+    ptx::bar_sync(kEpiBarrier, G::kNB);
+    if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
+  }
+}
+
+template <int KIND, int SDT>
+__device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CUtensorMap* mS2,
+                                                const GemmParams& p, SharedState* ss, uint8_t* epi,
+                                                int warp, int lane, uint32_t rank) {
+  if (warp == 2 + kNumEpiWarpsStaged)
+    epilogue_io_role<KIND, SDT>(mS1, mS2, p, ss, epi, lane, rank);
+  else
+    epilogue_compute_role<KIND, SDT>(p, ss, epi, warp, lane, rank);
+}
+
 template <int SDT>
-__device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mW, const CUtensorMap* mS1,
-                                                      const CUtensorMap* mS2, const GemmParams& p,
-                                                      SharedState* ss, uint8_t* epi, int warp,
-                                                      int lane, uint32_t rank) {
+__device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, const CUtensorMap* mS2,
+                                                      const GemmParams& p, SharedState* ss,
+                                                      uint8_t* epi, int warp, int lane,
+                                                      uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_tma_role<kAdamW, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kNAdam: epilogue_tma_role<kNAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kRAdam: epilogue_tma_role<kRAdam, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kLion: epilogue_tma_role<kLion, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kRMSprop: epilogue_tma_role<kRMSprop, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kAdaGrad: epilogue_tma_role<kAdaGrad, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kSGD: epilogue_tma_role<kSGD, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    default: epilogue_tma_role<kSGDMomentum, SDT>(mW, mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kAdamW: epilogue_staged<kAdamW, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_staged<kNAdam, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_staged<kRAdam, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_staged<kLion, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_staged<kRMSprop, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_staged<kAdaGrad, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_staged<kSGD, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_staged<kSGDMomentum, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
   }
 }
 
@@ -920,7 +986,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT>(&mapW, &mapS1, &mapS2, p, ss, epi, warp, lane, rank);
+      epilogue_tma_dispatch<SDT>(&mapS1, &mapS2, p, ss, epi, warp, lane, rank);
     else
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
