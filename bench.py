@@ -2,16 +2,17 @@
 """Benchmark of the FORGE fused backward step on Llama-3.1-8B-shaped linears.
 
 One step = the backward of the seven linear layers of one decoder layer
-(down, up, gate, o, v, k, q; T = 16384 tokens): for each layer, dX = dY W from
-the pre-update weights, then the fused weight-gradient + AdamW step (bf16
-weights with stochastic rounding, fp32 moments).  Inputs are seeded synthetic
+(down, up, gate, o, v, k, q; T = 16384 tokens): for each layer one launch
+computes dX = dY W from the pre-update weights and the fused weight-gradient
++ AdamW step (bf16 weights with stochastic rounding, fp32 moments).  Inputs are seeded synthetic
 tensors resident in HBM; each activation/gradient tensor is >= 134 MB, larger
 than the 129 MB L2, so no L2 flush is needed between steps.
 
 Printed: one JSON line (rank 0).  ``value`` = (2NKT for dW + 2NKT for dX,
 summed over the layers and ranks) / step time, in TFLOP/s.  ``roofline`` is the
-fused wgrad+optimizer kernel's own rate (CUDA events around its launches)
-against the measured dense-bf16 peak.  ``e2e`` repeats the step with the
+step kernel's own rate (CUDA events around its launches) against the measured
+dense-bf16 peak.  ``two_launch`` times the same step with dX and the fused
+step as separate launches (and each kernel's rate).  ``e2e`` repeats the step with the
 inputs copied from pinned host memory inside the timed region (on a copy
 stream, overlapping the previous step's compute) and the status word read
 back every step.  ``unfused``
@@ -247,23 +248,19 @@ def run_ours(args):
     flops_step = 2.0 * flops_dw  # dW + dX
 
     ev = {L.name: [] for L in layers}
-    ev_dx = {L.name: [] for L in layers}
 
     def step(s, record=False):
+        """One backward step: per linear, dX and the FORGE step in one launch."""
         for L in layers:
-            if record:
-                z = torch.cuda.Event(enable_timing=True)
-                z.record(stream)
-            api.forge_linear_dgrad(L.dY, L.W, L.dX)
             if record:
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-            api.forge_linear_bwd_step(X[ACT[L.name]], L.dY, L.W, "adamw", hp, s, L.seed, L.m, L.v)
+            api.forge_linear_bwd_step(X[ACT[L.name]], L.dY, L.W, "adamw", hp, s, L.seed, L.m, L.v,
+                                      dX=L.dX)
             if record:
                 b.record(stream)
                 ev[L.name].append((a, b))
-                ev_dx[L.name].append((z, a))
 
     def barrier():
         if dist is not None:
@@ -290,24 +287,23 @@ def run_ours(args):
     api.forge_get_device_status()
     ms = start.elapsed_time(end) / args.steps
     ms = max_over_ranks(ms, dist, dev)
-    fused_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev[L.name])
-    fused_launches = sum(len(v) for v in ev.values())
-    fused_tflops = flops_dw * args.steps / (fused_ms * 1e-3) / 1e12
+    kern_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev[L.name])
+    launches = sum(len(v) for v in ev.values())
+    kern_tflops = flops_step * args.steps / (kern_ms * 1e-3) / 1e12
     hbm_gbs, peak_burst, peak_sust, peak_src = _peaks()
     value = flops_step * world / (ms * 1e-3) / 1e12
-    per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev[L.name]]) * 1e-3) / 1e12, 1)
+    per_layer = {L.name: round(4.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev[L.name]]) * 1e-3) / 1e12, 1)
                  for L in layers}
-    dx_per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev_dx[L.name]]) * 1e-3) / 1e12, 1)
-                    for L in layers}
-    # algorithmic bytes of the fused kernel per step: X and dY once, W r/w (bf16), m and v r/w (fp32)
+    # algorithmic bytes of the step launches: X, dY and W read once, W and the
+    # fp32 m, v read and written, dX written
     params = sum(L.N * L.K for L in layers)
-    bytes_fused = sum((L.T * L.K + L.T * L.N) * 2 for L in layers) + params * (4 + 16)
+    bytes_step = sum(2 * (2 * L.T * L.K + L.T * L.N) for L in layers) + params * (4 + 16)
 
     if args.no_extras:
         if rank == 0:
             print(json.dumps({"metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s",
                               "ms_per_step": round(ms, 4), "layers": [L.name for L in layers],
-                              "roofline_achieved": round(fused_tflops, 2),
+                              "roofline_achieved": round(kern_tflops, 2),
                               "note": "partial run (--no-extras): not a bench result"}), flush=True)
         if dist is not None:
             dist.destroy_process_group()
@@ -360,6 +356,48 @@ def run_ours(args):
     e2e_val = flops_step * world / (e2e_ms * 1e-3) / 1e12
     del hostX, hostdY, bufX, bufdY
 
+    # ---- the same step as two launches per linear (dX, then the fused step)
+    ev2 = {L.name: [] for L in layers}
+    ev2_dx = {L.name: [] for L in layers}
+
+    def two_launch_step(s, record=False):
+        for L in layers:
+            if record:
+                z = torch.cuda.Event(enable_timing=True)
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                z.record(stream)
+            api.forge_linear_dgrad(L.dY, L.W, L.dX)
+            if record:
+                a.record(stream)
+            api.forge_linear_bwd_step(X[ACT[L.name]], L.dY, L.W, "adamw", hp, s, L.seed, L.m, L.v)
+            if record:
+                b.record(stream)
+                ev2_dx[L.name].append((z, a))
+                ev2[L.name].append((a, b))
+
+    for _ in range(2):
+        two_launch_step(s_no)
+        s_no += 1
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t_steps = args.steps
+    t0.record(stream)
+    for _ in range(t_steps):
+        two_launch_step(s_no, record=True)
+        s_no += 1
+    t1.record(stream)
+    torch.cuda.synchronize()
+    api.forge_get_device_status()
+    two_ms = max_over_ranks(t0.elapsed_time(t1) / t_steps, dist, dev)
+    fused_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev2[L.name])
+    fused_tflops = flops_dw * t_steps / (fused_ms * 1e-3) / 1e12
+    fused_per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev2[L.name]]) * 1e-3) / 1e12, 1)
+                       for L in layers}
+    dx_per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev2_dx[L.name]]) * 1e-3) / 1e12, 1)
+                    for L in layers}
+
     # ---- unfused two-pass schedule on the same layers: all dW alive before the optimizer
     torch.cuda.reset_peak_memory_stats(dev)
     base_alloc = torch.cuda.memory_allocated(dev)
@@ -407,19 +445,25 @@ def run_ours(args):
                    "flops_counted": "2NKT (dW) + 2NKT (dX) per linear",
                    "l2": "no flush: every X/dY >= 134 MB and the states (1.7 GB) exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "tensor", "kernel": "fused wgrad+optimizer (tc_kernel, FORGE epilogue)",
-                     "achieved": round(fused_tflops, 2),
+        "roofline": {"bound": "tensor",
+                     "kernel": "one-launch FORGE step (tc_kernel mode 3: dX tiles, then dW tiles "
+                               "with the AdamW epilogue), 4NKT flops per launch",
+                     "achieved": round(kern_tflops, 2),
                      "peak": peak_sust, "unit": "TFLOP/s",
-                     "frac": round(fused_tflops / peak_sust, 4),
+                     "frac": round(kern_tflops / peak_sust, 4),
                      "peak_kind": f"bf16 sustained, {peak_src}",
-                     "frac_of_burst_peak": round(fused_tflops / peak_burst, 4),
+                     "frac_of_burst_peak": round(kern_tflops / peak_burst, 4),
                      "traffic": _profiled_traffic(),
-                     "traffic_unit": "DRAM bytes per fused launch (mean of the 7 layers, ncu)",
-                     "algorithmic_bytes_per_launch": round(bytes_fused / len(layers)),
-                     "algorithmic_bytes_per_step": bytes_fused,
-                     "launches_timed": fused_launches,
+                     "traffic_unit": "DRAM bytes per step launch (mean of the 7 layers, ncu)",
+                     "algorithmic_bytes_per_launch": round(bytes_step / len(layers)),
+                     "algorithmic_bytes_per_step": bytes_step,
+                     "launches_timed": launches,
                      "per_layer_tflops": per_layer},
-        "dgrad_per_layer_tflops": dx_per_layer,
+        "two_launch": {"ms_per_step": round(two_ms, 4),
+                       "value": round(flops_step * world / (two_ms * 1e-3) / 1e12, 2),
+                       "fused_wgrad_opt_tflops": round(fused_tflops, 2),
+                       "fused_per_layer_tflops": fused_per_layer,
+                       "dgrad_per_layer_tflops": dx_per_layer},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": 4, "ms_per_step": round(e2e_ms, 4)},
         "unfused": {"ms_per_step": round(unf_ms, 4),
@@ -428,8 +472,8 @@ def run_ours(args):
                     "dW_pool_bytes": params * 4,
                     "peak_alloc_bytes_fused": base_alloc,
                     "peak_alloc_bytes_unfused": unf_peak},
-        "hbm_bytes_per_param_algorithmic": round(bytes_fused / params, 3),
-        "gpu_launches": 2 * len(layers) * args.steps,
+        "hbm_bytes_per_param_algorithmic": round(bytes_step / params, 3),
+        "gpu_launches": len(layers) * args.steps,
         "clocks": ck,
     }
     if not args.no_cpu_baseline:

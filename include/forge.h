@@ -113,17 +113,29 @@ typedef struct forge_hparams {
  * Mechanism" and §5 "Limitations"):
  *   1. if lin->dX != NULL: dX = dY W from the PRE-update W (bf16 operands, FP32
  *      accumulation, bf16 result; FP32 master weights enter as their nearest
- *      bf16), launched first on `stream`;
+ *      bf16);
  *   2. for every W tile: g = dY^T X accumulated over all T tokens in FP32 in
  *      tensor memory, then the rule `opt_kind` applied elementwise (per-step
  *      scalars formed on the host in double from `hp` and `step`), then W
  *      written back (FP32, or BF16 by stochastic rounding) and the states
  *      written back (FP32, or INT8 requantised with the new block absmax).
- * step is 1-based (bias corrections).  Nothing is allocated; no gradient
- * tensor is written.  Returns FORGE_OK once both launches are enqueued. */
+ * With bf16 weights, dX requested, N and K multiples of 64 and T > 0, both
+ * run in ONE persistent launch (the dX tiles first; a W tile is written only
+ * after every dX tile of its 256-column block has finished reading W); the
+ * launch uses a library-owned counter array in device memory (cleared on
+ * `stream` first), so two such calls must not run concurrently on one device
+ * (order them on one stream, or call forge_set_step_fusion(0)).  Otherwise
+ * dX is a separate launch enqueued first on `stream`.  Both forms compute the
+ * same bits.  step is 1-based (bias corrections).  Nothing is allocated; no
+ * gradient tensor is written.  Returns FORGE_OK once the launches are
+ * enqueued. */
 FORGE_API forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_state_t* state,
                                      int32_t opt_kind, const forge_hparams_t* hp,
                                      int64_t step, uint64_t seed, void* stream);
+
+/* Whether forge_linear_bwd_step may run dX and the FORGE step in one launch
+ * (non-zero, the default) or always uses two launches (0).  Process-wide. */
+FORGE_API void forge_set_step_fusion(int32_t enable);
 
 /* dX = dY W alone (step 1 above); W is fp32 or bf16 per w_dtype. */
 FORGE_API forge_status_t forge_linear_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype,

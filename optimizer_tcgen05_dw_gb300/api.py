@@ -73,6 +73,7 @@ _SIGNATURES = {
     "forge_get_device_status": (c_int32, [c_void_p]),
     "forge_set_wait_limit_ns": (c_int32, [c_uint64]),
     "forge_debug_skip_loads": (c_int32, [c_int32]),
+    "forge_set_step_fusion": (None, [c_int32]),
     "forge_status_string": (ctypes.c_char_p, [c_int32]),
     "forge_last_error_message": (ctypes.c_char_p, []),
     "forge_abi_version": (c_int32, []),
@@ -241,6 +242,11 @@ def forge_get_device_status(stream=None):
 
 def forge_set_wait_limit_ns(ns: int):
     _check(lib().forge_set_wait_limit_ns(int(ns)))
+
+
+def forge_set_step_fusion(enable: bool):
+    """Allow (default) or forbid the one-launch dX + FORGE step."""
+    lib().forge_set_step_fusion(1 if enable else 0)
 
 
 def forge_debug_skip_loads(enable: bool):

@@ -2,10 +2,12 @@
 // per-step optimizer scalars, TMA tensor maps, and kernel launches.
 //
 // Nothing here allocates device memory: every buffer is the caller's.  The
-// library's only device state is one status word per device (below).
+// library's only device state is one status word per device and the
+// one-launch step's dX-completion counters (below), both static.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -21,6 +23,13 @@ namespace forge {
 
 // Device-side status word: 0 = OK, otherwise the first error a kernel saw.
 __device__ uint32_t g_device_status;
+
+// Per column block of W, the dX tiles of the current one-launch step whose
+// MMAs have finished; cleared on the stream before each such launch.  Steps
+// launched concurrently on different streams of one device would share
+// them, so the one-launch path is taken only while the caller keeps its
+// steps on one device ordered (forge.h, forge_set_step_fusion).
+__device__ uint32_t g_dx_done[kMaxDxBlocks];
 
 namespace {
 
@@ -40,6 +49,7 @@ forge_status_t cuda_fail(cudaError_t e, const char* what) {
 
 std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
 std::atomic<int32_t> g_skip_loads{0};
+std::atomic<int32_t> g_step_fusion{1};
 
 // ---------------------------------------------------------------- per device
 
@@ -48,6 +58,8 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   int num_sms = 0;
   uint32_t* status = nullptr;
+  uint32_t* dx_done = nullptr;
+  int step_pairs[2] = {0, 0};  // resident one-launch-step pairs, fp32 / INT8 states
   int cc_major = 0, cc_minor = 0;
 };
 
@@ -71,6 +83,13 @@ forge_status_t device_info(DeviceInfo* out) {
     if ((e = cudaGetSymbolAddress(&sym, g_device_status)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(status word)");
     d.status = static_cast<uint32_t*>(sym);
+    if ((e = cudaGetSymbolAddress(&sym, g_dx_done)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(dX counters)");
+    d.dx_done = static_cast<uint32_t*>(sym);
+    if (d.cc_major == 10 && d.cc_minor == 3) {
+      d.step_pairs[0] = step_max_pairs(kSFp32);
+      d.step_pairs[1] = step_max_pairs(kSInt8);
+    }
     g_dev[dev] = d;
     g_dev_ready[dev] = true;
   }
@@ -173,24 +192,22 @@ forge_status_t wgrad_maps(const forge_linear_t* lin, int bk, CUtensorMap* ma, CU
   return bf16_map(mb, lin->X, lin->K, lin->T, 64, bk);
 }
 
-// Maps of the weight / state tiles the bf16-weight epilogue stages through
-// shared memory: W in 32-column boxes (64-byte rows, 64-byte swizzle), fp32
-// states in 32-column boxes (128-byte rows, 128-byte swizzle), INT8 codes in
-// 64-column boxes (64-byte rows, 64-byte swizzle); 128 rows each.
-forge_status_t epilogue_maps(const forge_state_t* st, int kind, int64_t N, int64_t K, CUtensorMap* mw,
-                             CUtensorMap* m1, CUtensorMap* m2) {
-  forge_status_t r = tensor_map(mw, st->W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 32, kTileM,
-                                CU_TENSOR_MAP_SWIZZLE_64B);
-  if (r != FORGE_OK) return r;
-  *m1 = *mw;
-  *m2 = *mw;
+// Maps of the state tiles the bf16-weight epilogue stages through shared
+// memory: fp32 states in 32-column boxes (128-byte rows, 128-byte swizzle),
+// INT8 codes in 64-column boxes (64-byte rows, 64-byte swizzle); 128 rows
+// each.  A rule that keeps no such state gets a copy of `other` (unused).
+forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t K,
+                          const CUtensorMap& other, CUtensorMap* m1, CUtensorMap* m2) {
+  *m1 = other;
+  *m2 = other;
   const bool int8 = st->s_dtype == FORGE_STATE_INT8_B64;
   const void* bufs[2] = {st->s1, st->s2};
   const bool used[2] = {uses_s1(kind), uses_s2(kind)};
   CUtensorMap* maps[2] = {m1, m2};
   for (int i = 0; i < 2; ++i) {
     if (!used[i]) continue;
-    r = int8 ? tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, 64, kTileM,
+    forge_status_t r =
+        int8 ? tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, 64, kTileM,
                           CU_TENSOR_MAP_SWIZZLE_64B)
              : tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, K, N, 32, kTileM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -375,6 +392,51 @@ forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_
   return FORGE_OK;
 }
 
+// dX and the FORGE step in one persistent launch (bf16 weights; N and K
+// multiples of 64; T > 0): dX tiles over (T, K) reducing over N, then dW
+// tiles over (N, K) reducing over T.
+forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state, int32_t opt_kind,
+                           const OptScalars& sc, int64_t step, uint64_t seed, cudaStream_t s,
+                           const DeviceInfo& d) {
+  const int64_t T = lin->T, N = lin->N, K = lin->K;
+  forge_status_t st;
+  CUtensorMap ma, mb, mda, mdb, m1, m2;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((st = wgrad_maps(lin, kFusedBlockK, &ma, &mb, &p.op3d)) != FORGE_OK) return st;
+  if ((st = bf16_map(&mda, lin->dY, N, T, 64, kTileM)) != FORGE_OK) return st;
+  if ((st = mn_major_3d_map(&mdb, state->W, K, N, kFusedBlockK, kTileN / 2 / 64)) != FORGE_OK) return st;
+  if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
+  fill_tiles(p, N, K, T, kFusedBlockK);
+  p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
+  p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
+  p.sc = sc;
+  p.seed = seed;
+  p.step = static_cast<uint64_t>(step);
+  p.status = d.status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.skip_loads = g_skip_loads.load();
+  p.dx_rows = static_cast<int32_t>(T);
+  p.dx_tiles_m = static_cast<int32_t>((T + 2 * kTileM - 1) / (2 * kTileM));
+  p.dx_tiles = p.dx_tiles_m * p.tiles_n;
+  p.dx_num_kb = static_cast<int32_t>((N + kFusedBlockK - 1) / kFusedBlockK);
+  p.dx_out = lin->dX;
+  p.dx_done = d.dx_done;
+  p.dx_target = static_cast<uint32_t>(2 * p.dx_tiles_m);
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(d.dx_done, 0, static_cast<size_t>(p.tiles_n) * sizeof(uint32_t), s)) != cudaSuccess)
+    return cuda_fail(e, "clearing the dX counters");
+  // Every pair must be resident at once (dW tiles wait for other pairs' dX
+  // tiles): at most the occupancy limit, at most one pair per tile.
+  const int sdt = state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0;
+  const int pairs = std::min(d.num_sms / 2, d.step_pairs[sdt]);
+  const int tiles = p.num_tiles + p.dx_tiles;
+  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, p, 2 * std::min(tiles, pairs), s)) !=
+      cudaSuccess)
+    return cuda_fail(e, "one-launch step");
+  return FORGE_OK;
+}
+
 forge_status_t check_device(const DeviceInfo& d) {
   if (d.cc_major != 10 || d.cc_minor != 3)
     return fail(FORGE_ERR_UNSUPPORTED, "libforge is built for sm_103a; device is sm_%d%d", d.cc_major, d.cc_minor);
@@ -401,9 +463,16 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   if ((st = device_info(&d)) != FORGE_OK) return st;
   if ((st = check_device(d)) != FORGE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const OptScalars sc = make_scalars(opt_kind, *hp, step);
+  // One launch for dX and the FORGE step (bf16 weights, 64-aligned N and K):
+  // the dX tiles first, each dW tile's update after the dX tiles that read its
+  // weights.
+  if (lin->dX != nullptr && lin->T > 0 && state->w_dtype == FORGE_W_BF16_SR && lin->N % 64 == 0 &&
+      lin->K % 64 == 0 && (lin->K + kTileN - 1) / kTileN <= kMaxDxBlocks && g_step_fusion.load() &&
+      d.step_pairs[state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0] > 0)
+    return launch_step(lin, state, opt_kind, sc, step, seed, s, d);
   // 1. dX from the pre-update weights, enqueued first on the same stream.
   if (lin->dX != nullptr && (st = launch_dgrad(lin, state->W, state->w_dtype, s, d)) != FORGE_OK) return st;
-  const OptScalars sc = make_scalars(opt_kind, *hp, step);
   cudaError_t e;
   if (lin->T == 0) {
     // No tokens: the gradient is exactly zero; apply the rule to it.
@@ -431,15 +500,17 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
-  CUtensorMap mw = ma, m1 = ma, m2 = ma;
+  CUtensorMap m1 = ma, m2 = ma;
   if (state->w_dtype == FORGE_W_BF16_SR &&
-      (st = epilogue_maps(state, opt_kind, lin->N, lin->K, &mw, &m1, &m2)) != FORGE_OK)
+      (st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK)
     return st;
-  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, mw, m1, m2, p, grid_for(p, d), s)) !=
+  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, m1, m2, p, grid_for(p, d), s)) !=
       cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
 }
+
+void forge_set_step_fusion(int32_t enable) { g_step_fusion.store(enable != 0 ? 1 : 0); }
 
 forge_status_t forge_linear_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype, void* stream) {
   g_msg[0] = '\0';

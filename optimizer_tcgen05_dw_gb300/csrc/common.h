@@ -75,8 +75,13 @@ constexpr int kTmemCols = 2 * kTileN;                    // double-buffered fp32
 enum GemmMode : int32_t {
   kModeFusedOpt = 0,   // dW tile -> optimizer epilogue (the FORGE step)
   kModeWgradStore = 1, // dW tile -> fp32 store (unfused pass 1)
-  kModeDgrad = 2       // dX tile -> bf16 store
+  kModeDgrad = 2,      // dX tile -> bf16 store
+  kModeStep = 3        // one launch: the dX tiles, then the dW tiles -> optimizer epilogue
 };
+
+// Column blocks (of kTileN) whose dX-completion counters the one-launch step
+// keeps in device memory: K up to 1M.
+constexpr int kMaxDxBlocks = 4096;
 
 // Parameters of one tensor-core launch.  Output tile space is M x Ncols
 // (wgrad: M = N_out rows of W, Ncols = K; dgrad: M = T, Ncols = K).
@@ -97,6 +102,18 @@ struct GemmParams {
   uint32_t* status;          // device status word (first error wins)
   int32_t op3d;              // MN-major operands described as 3-D maps: one load per stage
   int32_t skip_loads;
+  // kModeStep: the dX tiles (a T x Ncols output, reduction over M) that run
+  // ahead of the dW tiles in the same launch.  A dW tile writes its weights
+  // only after every dX tile of its column block has finished its MMAs (so
+  // has read the pre-update weights): dx_done[column block] counts them, one
+  // per CTA of the pair, up to dx_target.
+  int32_t dx_rows;           // T
+  int32_t dx_tiles_m;        // 256-row pair tiles over T
+  int32_t dx_tiles;          // dx_tiles_m * tiles_n
+  int32_t dx_num_kb;         // reduction blocks of 64 over M
+  void* dx_out;              // bf16 [dx_rows x Ncols]
+  uint32_t* dx_done;         // [tiles_n], zero at launch
+  uint32_t dx_target;        // 2 * dx_tiles_m
 };
 
 }  // namespace forge

@@ -24,12 +24,21 @@ struct ElemParams {
 };
 
 // tc_fused.cu: the FORGE step (mode kModeFusedOpt) for one (W dtype, state dtype).
-// w, s1, s2: tensor maps of the weight / state tiles the bf16-weight epilogue
-// stages through shared memory (unused, any valid map, for fp32 weights or
-// for states the rule does not keep).
+// s1, s2: tensor maps of the state tiles the bf16-weight epilogue stages
+// through shared memory (unused, any valid map, for fp32 weights or for
+// states the rule does not keep).
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
-                            const CUtensorMap& w, const CUtensorMap& s1, const CUtensorMap& s2,
-                            const GemmParams& p, int grid, cudaStream_t s);
+                            const CUtensorMap& s1, const CUtensorMap& s2, const GemmParams& p,
+                            int grid, cudaStream_t s);
+// tc_step.cu: dX and the FORGE step in one launch (mode kModeStep, bf16
+// weights): a, b the dW operands, da, db the dX operands (dY K-major, W).
+cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
+                           const CUtensorMap& s2, const GemmParams& p, int grid, cudaStream_t s);
+// CTA pairs of the one-launch step that can be resident at once (its dW tiles
+// wait for dX tiles of other pairs, so its grid must not exceed this); 0 if
+// the query fails.
+int step_max_pairs(int sdt);
 // tc_plain.cu: unfused pass 1 (kModeWgradStore) or dX (kModeDgrad).
 cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t s);

@@ -66,7 +66,7 @@ constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 
 template <int MODE, int WDT>
 struct KCfg {
-  static constexpr bool kTmaEpi = (MODE == kModeFusedOpt && WDT == kWBf16);
+  static constexpr bool kTmaEpi = ((MODE == kModeFusedOpt || MODE == kModeStep) && WDT == kWBf16);
   static constexpr int kBK =
       kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK);  // tokens per stage
   static constexpr int kStg =
@@ -110,14 +110,17 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, con
 // column blocks from HBM instead of every column block of one operand.
 constexpr int kRasterGroup = 8;
 
-__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& tm, int& tn) {
-  const int span = p.tiles_m * kRasterGroup;
+__device__ __forceinline__ void tile_coords_of(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
+  const int span = tiles_m * kRasterGroup;
   const int grp = tile / span;
   const int first_n = grp * kRasterGroup;
-  const int width = min(kRasterGroup, p.tiles_n - first_n);
+  const int width = min(kRasterGroup, tiles_n - first_n);
   const int local = tile - grp * span;
   tm = local / width;
   tn = first_n + (local - tm * width);
+}
+__device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& tm, int& tn) {
+  tile_coords_of(tile, p.tiles_m, p.tiles_n, tm, tn);
 }
 
 // ------------------------------------------------------------------ roles
@@ -126,15 +129,47 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
 __device__ __forceinline__ int pair_id() { return static_cast<int>(blockIdx.x) >> 1; }
 __device__ __forceinline__ int num_pairs() { return static_cast<int>(gridDim.x) >> 1; }
 
+// One-launch step: a pair first runs its dX tiles, dealt round-robin from
+// the last pair down (so the pairs that get an extra dW tile get one dX tile
+// fewer), then its dW tiles pair_id(), pair_id() + num_pairs(), ...
+__device__ __forceinline__ int my_dx_tiles(const GemmParams& p) {
+  const int rp = num_pairs() - 1 - pair_id();
+  return p.dx_tiles > rp ? (p.dx_tiles - 1 - rp) / num_pairs() + 1 : 0;
+}
+__device__ __forceinline__ void dx_tile_coords(int i, const GemmParams& p, int& tm, int& tn) {
+  tile_coords_of(num_pairs() - 1 - pair_id() + i * num_pairs(), p.dx_tiles_m, p.tiles_n, tm, tn);
+}
+
 template <int MODE, int STG, int BK>
-__device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, const GemmParams& p,
-                              uint8_t* smA, uint8_t* smB, SharedState* ss, uint32_t rank) {
+__device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, const CUtensorMap* mDA,
+                              const CUtensorMap* mDB, const GemmParams& p, uint8_t* smA,
+                              uint8_t* smB, SharedState* ss, uint32_t rank) {
   constexpr int kA = kTileM * BK * 2, kB = (kTileN / 2) * BK * 2;
   uint32_t it = 0;
   uint32_t issued_mask = 0;
   uint32_t last_parity = 0;  // bit s: parity of the last phase armed on full[s]
   const uint32_t full0 = ptx::mapa(ptx::smem_addr(&ss->full[0]), 0);  // the leader's barriers
   if (!p.skip_loads) {
+    if (MODE == kModeStep) {  // the dX tiles: A = dY (K-major), B = W (MN-major)
+      const int ndx = my_dx_tiles(p);
+      for (int i = 0; i < ndx; ++i) {
+        int tm, tn;
+        dx_tile_coords(i, p, tm, tn);
+        const int m0 = tm * kPairM + static_cast<int>(rank) * kTileM;
+        const int n0 = tn * kTileN + static_cast<int>(rank) * (kTileN / 2);
+        for (int kb = 0; kb < p.dx_num_kb; ++kb, ++it) {
+          const int s = static_cast<int>(it % STG);
+          const uint32_t ph = (it / STG) & 1u;
+          if (!bounded_wait(&ss->empty[s], ph ^ 1u, p, ss)) goto drain;
+          const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
+          if (rank == 0) ptx::mbar_arrive_expect_tx(&ss->full[s], 2u * (kA + kB));
+          ptx::tma_load_2d_pair(mDA, bar, smA + s * kA, kb * BK, m0);
+          ptx::tma_load_3d_pair(mDB, bar, smB + s * kB, 0, kb * BK, n0 / 64);
+          issued_mask |= 1u << s;
+          last_parity = (last_parity & ~(1u << s)) | (ph << s);
+        }
+      }
+    }
     for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs()) {
       int tm, tn;
       tile_coords(tile, p, tm, tn);
@@ -181,40 +216,48 @@ drain:
 template <int MODE, int STG, int BK>
 __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, SharedState* ss) {
   constexpr int kA = kTileM * BK * 2, kB = (kTileN / 2) * BK * 2;
-  constexpr uint32_t kIdesc =
-      ptx::idesc_bf16_f32(kPairM, kTileN, /*a_mn=*/MODE != kModeDgrad, /*b_mn=*/true);
   uint32_t it = 0;
   int local = 0;
-  for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs(), ++local) {
+  // One tile into accumulator local & 1: num_kb stages; A K-major (dX: dY) or
+  // MN-major (dW: dY^T); B MN-major.  False if the CTA is aborting.
+  auto run_tile = [&](int num_kb, bool a_kmajor) -> bool {
     const int acc = local & 1;
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
-    if (!bounded_wait(&ss->tmem_empty[acc], aph ^ 1u, p, ss)) goto done;
+    if (!bounded_wait(&ss->tmem_empty[acc], aph ^ 1u, p, ss)) return false;
     ptx::tc_fence_after();
-    {
-      const uint32_t d_tmem = ss->tmem_base + static_cast<uint32_t>(acc * kTileN);
-      for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
-        const int s = static_cast<int>(it % STG);
-        const uint32_t ph = (it / STG) & 1u;
-        if (!bounded_wait(&ss->full[s], ph, p, ss)) goto done;
-        ptx::tc_fence_after();
-        const uint32_t a0 = ptx::smem_addr(smA + s * kA);
-        const uint32_t b0 = ptx::smem_addr(smB + s * kB);
+    const uint32_t idesc = a_kmajor ? ptx::idesc_bf16_f32(kPairM, kTileN, false, true)
+                                    : ptx::idesc_bf16_f32(kPairM, kTileN, true, true);
+    const uint32_t d_tmem = ss->tmem_base + static_cast<uint32_t>(acc * kTileN);
+    for (int kb = 0; kb < num_kb; ++kb, ++it) {
+      const int s = static_cast<int>(it % STG);
+      const uint32_t ph = (it / STG) & 1u;
+      if (!bounded_wait(&ss->full[s], ph, p, ss)) return false;
+      ptx::tc_fence_after();
+      const uint32_t a0 = ptx::smem_addr(smA + s * kA);
+      const uint32_t b0 = ptx::smem_addr(smB + s * kB);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB;
-          // atoms of 64 columns x BK rows sit BK*128 bytes apart (LBO).
-          // K-major: 16 bf16 = 32 B inside the 128-byte swizzle row.
-          const uint64_t adesc = (MODE == kModeDgrad)
-                                     ? ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024)
-                                     : ptx::smem_desc_sw128(a0 + kk * 2048, BK * 128, 1024);
-          const uint64_t bdesc = ptx::smem_desc_sw128(b0 + kk * 2048, BK * 128, 1024);
-          ptx::mma_bf16_pair(d_tmem, adesc, bdesc, kIdesc, (kb | kk) != 0 ? 1u : 0u);
-        }
-        ptx::mma_commit_pair_multicast(&ss->empty[s], 0x3);  // frees the stage in both CTAs
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB;
+        // atoms of 64 columns x BK rows sit BK*128 bytes apart (LBO).
+        // K-major: 16 bf16 = 32 B inside the 128-byte swizzle row.
+        const uint64_t adesc = a_kmajor ? ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024)
+                                        : ptx::smem_desc_sw128(a0 + kk * 2048, BK * 128, 1024);
+        const uint64_t bdesc = ptx::smem_desc_sw128(b0 + kk * 2048, BK * 128, 1024);
+        ptx::mma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
       }
-      ptx::mma_commit_pair_multicast(&ss->tmem_full[acc], 0x3);  // accumulator complete
+      ptx::mma_commit_pair_multicast(&ss->empty[s], 0x3);  // frees the stage in both CTAs
     }
+    ptx::mma_commit_pair_multicast(&ss->tmem_full[acc], 0x3);  // accumulator complete
+    ++local;
+    return true;
+  };
+  if (MODE == kModeStep) {
+    const int ndx = my_dx_tiles(p);
+    for (int i = 0; i < ndx; ++i)
+      if (!run_tile(p.dx_num_kb, true)) goto done;
   }
+  for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs())
+    if (!run_tile(p.num_kb, MODE == kModeDgrad)) goto done;
 done:
   // Tensor memory may be released only after every issued MMA has finished.
   ptx::mma_commit_pair_multicast(&ss->mma_done, 0x1);
@@ -747,14 +790,64 @@ struct TileWalk {
   }
 };
 
+// Bounded wait until a grid-wide counter reaches `target` (acquire).  False if
+// the CTA is aborting or the wait expired (the expiry is recorded).
+__device__ __forceinline__ bool bounded_wait_count(const uint32_t* cnt, uint32_t target,
+                                                   const GemmParams& p, SharedState* ss) {
+  if (ptx::ld_acquire_gpu(cnt) >= target) return true;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (true) {
+    __nanosleep(256);
+    if (ptx::ld_acquire_gpu(cnt) >= target) return true;
+    if (*reinterpret_cast<volatile int32_t*>(&ss->abort)) return false;
+    if (ptx::global_timer_ns() - t0 > p.wait_limit_ns) {
+      *reinterpret_cast<volatile int32_t*>(&ss->abort) = 1;
+      atomicCAS(p.status, 0u, static_cast<uint32_t>(kStatusTimeout));
+      return false;
+    }
+  }
+}
+
+// One dX tile of the one-launch step, by a compute warp: 64 columns
+// (sub*64..) of TMEM lane row r, rounded to bf16 (nearest even) and stored
+// to dX row `row`, columns col0.. (whole groups of 8 inside the K columns).
+__device__ __forceinline__ void epi_dx_store(uint32_t taddr, int64_t row, int col0,
+                                             const GemmParams& p) {
+  const bool row_ok = row < p.dx_rows;
+  uint16_t* out = static_cast<uint16_t*>(p.dx_out) + row * static_cast<int64_t>(p.Ncols);
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    float g[32];
+    ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
+    if (!row_ok) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int col = col0 + c * 32 + q * 8;
+      if (col >= p.Ncols) continue;
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(g[8 * q + 2 * j], g[8 * q + 2 * j + 1]);
+        o[j] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(out + col) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
 // The I/O warp of the FORGE epilogue (bf16 weights).  Its lane 0 moves the
 // optimizer states: before the compute warps start chunk j it waits for the
 // accumulator (first chunk of a tile) and for chunk j's staged states; while
 // they work on chunk j it waits until the bulk stores of chunk j-1 have read
 // their buffer and issues the TMA loads of chunk j+1 into it; after they have
 // written chunk j back to shared memory it issues chunk j's TMA stores.  None
-// of its waits sits between two chunks of the compute warps.
-template <int KIND, int SDT>
+// of its waits sits between two chunks of the compute warps.  In the
+// one-launch step (STEP) the pair's dX tiles come first: for each it waits
+// for the accumulator, then counts the tile done in its column block (its
+// MMAs, and so its reads of the weights, are complete); before a dW tile's
+// first chunk it waits until all dX tiles of the tile's column block are
+// counted, so no weight is written while a dX tile may still read it.
+template <int KIND, int SDT, bool STEP>
 __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                  const GemmParams& p, SharedState* ss, uint8_t* epi, int lane,
                                  uint32_t rank) {
@@ -788,13 +881,34 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
     issue(0);
     issued = 1;
   }
-  for (int j = 0; j < total; ++j) {
+  bool aborted = false;
+  if (STEP) {
+    const int ndx = my_dx_tiles(p);
+    for (int i = 0; i < ndx; ++i) {
+      ++local;
+      bool ok = true;
+      if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
+      if (io && ok) {
+        int tm, tn;
+        dx_tile_coords(i, p, tm, tn);
+        ptx::red_release_gpu_add(p.dx_done + tn, 1u);
+      }
+      if (ptx::bar_red_or(kEpiBarrier, G::kNB, !ok)) {
+        aborted = true;
+        break;
+      }
+      ptx::bar_sync(kEpiBarrier, G::kNB);  // the compute warps have stored the tile
+    }
+  }
+  const int first = local + 1;  // accumulator index of the first dW tile
+  for (int j = 0; j < total && !aborted; ++j) {
     const int c = j % G::kChunks;
     bool ok = true;
     if (c == 0) {
       ++local;
-      if (local > 0) walk.advance(local, p, rank);
+      if (local > first) walk.advance(local - first, p, rank);
       if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
+      if (STEP && io && ok) ok = bounded_wait_count(p.dx_done + walk.cur_col0 / kTileN, p.dx_target, p, ss);
     }
     if (io && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
     // Releases the compute warps into chunk j (ordering their tensor- and
@@ -820,7 +934,7 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
 // lanes 32*(w%4).. (its rows) and a quarter of each chunk's columns; its bf16
 // weights (and old INT8 scales) come straight from global memory one chunk
 // ahead, its states from the staged chunk in shared memory.
-template <int KIND, int SDT>
+template <int KIND, int SDT, bool STEP>
 __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint8_t* epi,
                                       int warp, int lane, uint32_t rank) {
   using G = StagedGeom<KIND, SDT>;
@@ -858,12 +972,31 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   uint4 wnext[kWPerThread / 8];
   float o1next = 0.f, o2next = 0.f;  // old INT8 scales of the next chunk
   int local = -1;
+  if (STEP) {  // the pair's dX tiles: 64 columns per warp, straight to global memory
+    const int ndx = my_dx_tiles(p);
+    for (int i = 0; i < ndx; ++i) {
+      ++local;
+      if (ptx::bar_red_or(kEpiBarrier, G::kNB, false)) return;  // the I/O warp's verdict
+      ptx::tc_fence_after();
+      int tm, tn;
+      dx_tile_coords(i, p, tm, tn);
+      const int acc = local & 1;
+      const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                             static_cast<uint32_t>(acc * kTileN + sub * 64);
+      epi_dx_store(taddr, static_cast<int64_t>(tm) * kPairM + static_cast<int>(rank) * kTileM + r,
+                   tn * kTileN + sub * 64, p);
+      ptx::tc_fence_before();
+      ptx::bar_sync(kEpiBarrier, G::kNB);
+      if (lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
+    }
+  }
+  const int first = local + 1;  // accumulator index of the first dW tile
   if (total > 0) prefetch(0, wnext, o1next, o2next);
   for (int j = 0; j < total; ++j) {
     const int c = j % kChunks;
     if (c == 0) {
       ++local;
-      if (local > 0) walk.advance(local, p, rank);
+      if (local > first) walk.advance(local - first, p, rank);
     }
     if (ptx::bar_red_or(kEpiBarrier, G::kNB, false)) break;  // the I/O warp's verdict
     int row0, col0;
@@ -905,30 +1038,30 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   }
 }
 
-template <int KIND, int SDT>
+template <int KIND, int SDT, bool STEP>
 __device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                                 const GemmParams& p, SharedState* ss, uint8_t* epi,
                                                 int warp, int lane, uint32_t rank) {
   if (warp == 2 + kNumEpiWarpsStaged)
-    epilogue_io_role<KIND, SDT>(mS1, mS2, p, ss, epi, lane, rank);
+    epilogue_io_role<KIND, SDT, STEP>(mS1, mS2, p, ss, epi, lane, rank);
   else
-    epilogue_compute_role<KIND, SDT>(p, ss, epi, warp, lane, rank);
+    epilogue_compute_role<KIND, SDT, STEP>(p, ss, epi, warp, lane, rank);
 }
 
-template <int SDT>
+template <int SDT, bool STEP>
 __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                                       const GemmParams& p, SharedState* ss,
                                                       uint8_t* epi, int warp, int lane,
                                                       uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_staged<kAdamW, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kNAdam: epilogue_staged<kNAdam, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kRAdam: epilogue_staged<kRAdam, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kLion: epilogue_staged<kLion, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kRMSprop: epilogue_staged<kRMSprop, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kAdaGrad: epilogue_staged<kAdaGrad, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kSGD: epilogue_staged<kSGD, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    default: epilogue_staged<kSGDMomentum, SDT>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kAdamW: epilogue_staged<kAdamW, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_staged<kNAdam, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_staged<kRAdam, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_staged<kLion, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_staged<kRMSprop, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_staged<kSGD, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_staged<kSGDMomentum, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
   }
 }
 
@@ -937,7 +1070,8 @@ __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, co
 template <int MODE, int WDT, int SDT>
 __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-              const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapS1,
+              const __grid_constant__ CUtensorMap mapDA, const __grid_constant__ CUtensorMap mapDB,
+              const __grid_constant__ CUtensorMap mapS1,
               const __grid_constant__ CUtensorMap mapS2, const GemmParams p) {
   using Cfg = KCfg<MODE, WDT>;
   constexpr int STG = Cfg::kStg;
@@ -969,6 +1103,10 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tensormap(&mapA);
     ptx::prefetch_tensormap(&mapB);
+    if (MODE == kModeStep) {
+      ptx::prefetch_tensormap(&mapDA);
+      ptx::prefetch_tensormap(&mapDB);
+    }
   }
   if (warp == 1) {
     __syncwarp();
@@ -981,12 +1119,12 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
   ptx::tc_fence_after();
 
   if (warp == 0) {
-    if (lane == 0) producer_role<MODE, STG, Cfg::kBK>(&mapA, &mapB, p, smA, smB, ss, rank);
+    if (lane == 0) producer_role<MODE, STG, Cfg::kBK>(&mapA, &mapB, &mapDA, &mapDB, p, smA, smB, ss, rank);
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT>(&mapS1, &mapS2, p, ss, epi, warp, lane, rank);
+      epilogue_tma_dispatch<SDT, MODE == kModeStep>(&mapS1, &mapS2, p, ss, epi, warp, lane, rank);
     else
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
@@ -1004,8 +1142,8 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
 // Launch on clusters of two CTAs (the tcgen05 pair); grid is a multiple of 2.
 template <typename Kernel>
 inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaStream_t s,
-                               const CUtensorMap& a,
-                               const CUtensorMap& b, const CUtensorMap& w, const CUtensorMap& s1,
+                               const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
+                               const CUtensorMap& db, const CUtensorMap& s1,
                                const CUtensorMap& s2, const GemmParams& p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
@@ -1019,7 +1157,7 @@ inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaSt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, w, s1, s2, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, da, db, s1, s2, p);
 }
 
 }  // namespace forge

@@ -1,0 +1,50 @@
+// Instantiations of the tensor-core kernel for the one-launch step: the dX
+// tiles (dX = dY W from the weights before the update), then the FORGE
+// weight-gradient + optimizer tiles, with bf16 weights.
+#include "launch.h"
+#include "tc_kernel.cuh"
+
+namespace forge {
+
+template <int SDT>
+static cudaError_t run_step(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
+                            const CUtensorMap& db, const CUtensorMap& s1, const CUtensorMap& s2,
+                            const GemmParams& p, int grid, cudaStream_t s) {
+  auto* k = tc_kernel<kModeStep, kWBf16, SDT>;
+  constexpr int smem = KCfg<kModeStep, kWBf16>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pair(k, grid, KCfg<kModeStep, kWBf16>::kThreads, smem, s, a, b, da, db, s1, s2, p);
+}
+
+template <int SDT>
+static int step_pairs() {
+  auto* k = tc_kernel<kModeStep, kWBf16, SDT>;
+  constexpr int smem = KCfg<kModeStep, kWBf16>::kSmem;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(KCfg<kModeStep, kWBf16>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+int step_max_pairs(int sdt) { return sdt == kSInt8 ? step_pairs<kSInt8>() : step_pairs<kSFp32>(); }
+
+cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
+                           const CUtensorMap& s2, const GemmParams& p, int grid, cudaStream_t s) {
+  return sdt == kSInt8 ? run_step<kSInt8>(a, b, da, db, s1, s2, p, grid, s)
+                       : run_step<kSFp32>(a, b, da, db, s1, s2, p, grid, s);
+}
+
+}  // namespace forge

@@ -20,8 +20,8 @@ from oracle import quant, rounding
 from optimizer_tcgen05_dw_gb300 import api, inputs
 from optimizer_tcgen05_dw_gb300.build import build
 
-from _helpers import (assert_in_interval, grad_error_bound, oracle_hparams, oracle_interval,
-                      to_bits)
+from _helpers import (assert_dx_close, assert_in_interval, grad_error_bound, oracle_hparams,
+                      oracle_interval, to_bits)
 
 pytestmark = pytest.mark.gpu
 
@@ -140,3 +140,41 @@ def test_qwen14b_int8_sampled(layer):
     N, K = QWEN[layer]
     run_sampled(N, K, w.T, "bf16", "int8", "adamw", w.hparams, steps=2, seed=5000 + N % 83,
                 m_std=1e-4, v_std=1e-6)
+
+
+@pytest.mark.parametrize("layer", ["q_proj", "k_proj"])
+def test_llama8b_one_launch_step_with_dx(layer):
+    """The bench's launch: dX and the FORGE step of a full-size layer in one
+    launch.  Same bits as the two-launch form (dX launch, then the fused
+    launch) for W, m, v and dX, and sampled 128 x 128 tiles of dX equal the
+    oracle's dY W from the pre-update weights."""
+    w = inputs.WORKLOADS["llama8b_bf16_fp32state"]
+    N, K = LLAMA[layer]
+    T = w.T
+    seed = 6000 + N % 79
+    X = inputs.normal((T, K), 1.0, inputs.layer_seed(seed, 0, 0, 1), device="cuda")
+    dY = inputs.normal((T, N), w.dy_std, inputs.layer_seed(seed, 0, 0, 2), device="cuda")
+    W0 = inputs.normal((N, K), 0.02, inputs.layer_seed(seed, 0, 0, 3), torch.bfloat16, "cuda")
+    outs = []
+    for one_launch in (True, False):
+        W = W0.clone()
+        m = torch.zeros((N, K), dtype=torch.float32, device="cuda")
+        v = torch.zeros((N, K), dtype=torch.float32, device="cuda")
+        dX = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+        api.forge_set_step_fusion(one_launch)
+        try:
+            api.forge_linear_bwd_step(X, dY, W, "adamw", w.hparams, 1, seed, m, v, dX=dX)
+            api.forge_get_device_status()
+        finally:
+            api.forge_set_step_fusion(True)
+        outs.append((W, m, v, dX))
+    for a, b, name in zip(outs[0], outs[1], ("W", "m", "v", "dX")):
+        assert torch.equal(a, b), name
+    dX = outs[0][3]
+    rng = np.random.default_rng(seed)
+    W0b = to_bits(W0)
+    for _ in range(6):
+        t0 = int(rng.integers(0, T // TILE)) * TILE
+        k0 = int(rng.integers(0, K // TILE)) * TILE
+        assert_dx_close(dX[t0:t0 + TILE, k0:k0 + TILE].contiguous(), to_bits(dY[t0:t0 + TILE].contiguous()),
+                        np.ascontiguousarray(W0b[:, k0:k0 + TILE]), f"dX tile ({t0},{k0})")

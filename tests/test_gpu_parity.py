@@ -25,7 +25,8 @@ pytestmark = pytest.mark.gpu
 
 OPTS = list(opt.NAMES)
 DTYPES = [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "int8")]
-RAGGED = dict(T=200, N=264, K=320)
+RAGGED = dict(T=200, N=264, K=320)     # dX as its own launch (N % 64 != 0)
+RAGGED64 = dict(T=200, N=320, K=384)   # dX and the step in one launch
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,13 +55,15 @@ def _compare_exact(prob, gpu, ref):
 
 # --------------------------------------------------------------- exact inputs
 
+@pytest.mark.parametrize("shape", [RAGGED, RAGGED64], ids=["two_launch", "one_launch"])
 @pytest.mark.parametrize("opt_name", OPTS)
 @pytest.mark.parametrize("w_dtype,s_dtype", DTYPES)
-def test_fused_step_bitexact_on_integer_grid(opt_name, w_dtype, s_dtype):
+def test_fused_step_bitexact_on_integer_grid(opt_name, w_dtype, s_dtype, shape):
     """Integer-grid X and dY make every FP32 sum exact, so the tensor-core
     gradient equals the oracle's and the fused step must match bit for bit:
-    optimizer, stochastic rounding and INT8 requantisation included."""
-    prob = Problem(**RAGGED, w_dtype=w_dtype, s_dtype=s_dtype, opt_name=opt_name,
+    optimizer, stochastic rounding and INT8 requantisation included.  With
+    bf16 weights and 64-aligned N, K the dX tiles run in the same launch."""
+    prob = Problem(**shape, w_dtype=w_dtype, s_dtype=s_dtype, opt_name=opt_name,
                    hp=_hp(opt_name), grid=True, steps=3, seed=11)
     gpu, gdx = prob.run_gpu(fused=True, want_dx=True)
     ref, rdx, _ = prob.run_oracle(want_dx=True)
@@ -224,6 +227,33 @@ def test_edge_shapes(shape):
     assert_dx_close(gdx[0], to_bits(prob.dY[0]), prob.state0["W"], "dX")
 
 
+@pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
+@pytest.mark.parametrize("opt_name", ["adamw", "lion", "sgd"])
+def test_one_launch_step_equals_two_launches(opt_name, s_dtype):
+    """dX and the step in one launch compute the same bits as the dX launch
+    followed by the fused launch: same tiles, same reduction order.  96 pair
+    tiles (64 dX + 32 dW) on 76 pairs, so pairs run several tiles and dW tiles
+    wait on dX tiles of other pairs; large SGD steps make any weight written
+    before its last dX read visible in dX."""
+    hp = {"lr": 0.5} if opt_name == "sgd" else _hp(opt_name)
+    prob = Problem(T=2048, N=1024, K=2048, w_dtype="bf16", s_dtype=s_dtype, opt_name=opt_name,
+                   hp=hp, seed=71, steps=3, device_inputs=True)
+    outs = []
+    for fused_launch in (True, False):
+        api.forge_set_step_fusion(fused_launch)
+        try:
+            outs.append(prob.run_gpu(fused=True, want_dx=True))
+        finally:
+            api.forge_set_step_fusion(True)
+    (g1, dx1), (g2, dx2) = outs
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+    for s_ in range(prob.steps):
+        assert torch.equal(dx1[s_], dx2[s_]), f"dX step {s_ + 1}"
+    # and dX of step 1 is the pre-update weights' product (oracle)
+    assert_dx_close(dx1[0].cpu(), to_bits(prob.dY[0].cpu()), prob.state0["W"], "dX")
+
+
 def test_resume_is_exact():
     """States are plain caller tensors and rounding noise is a function of
     (seed, step, index): 4 steps equal 2 steps, a host round-trip, 2 steps."""
@@ -290,3 +320,28 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     gpu, _ = prob.run_gpu()
     ref, _, _ = prob.run_oracle()
     _compare_exact(prob, gpu, ref)
+
+
+def test_one_launch_step_timeout_reports_and_context_survives():
+    """The same with dX in the launch: the dX tiles' and dW tiles' waits (and
+    the wait on the dX counters) all end, and the next step is exact."""
+    prob = Problem(T=512, N=256, K=512, w_dtype="bf16", s_dtype="fp32", opt_name="sgd",
+                   hp={"lr": 1e-2}, grid=True, seed=62, steps=1)
+    g = prob.gpu_state()
+    dX = torch.empty((prob.T, prob.K), dtype=torch.bfloat16, device="cuda")
+    api.forge_set_wait_limit_ns(50_000_000)
+    api.forge_debug_skip_loads(True)
+    try:
+        api.forge_linear_bwd_step(prob.X[0].cuda(), prob.dY[0].cuda(), g["W"], "sgd", prob.hp, 1, 1,
+                                  dX=dX)
+        with pytest.raises(api.ForgeError) as e:
+            api.forge_get_device_status()
+        assert e.value.status == 4
+    finally:
+        api.forge_debug_skip_loads(False)
+        api.forge_set_wait_limit_ns(200_000_000)
+    api.forge_get_device_status()  # cleared
+    gpu, gdx = prob.run_gpu(want_dx=True)
+    ref, rdx, _ = prob.run_oracle(want_dx=True)
+    _compare_exact(prob, gpu, ref)
+    assert_dx_close(gdx[0], to_bits(prob.dY[0]), prob.state0["W"], "dX")
