@@ -133,6 +133,29 @@ FORGE_API forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const 
                                      int32_t opt_kind, const forge_hparams_t* hp,
                                      int64_t step, uint64_t seed, void* stream);
 
+/* forge_linear_bwd_step computing the same bits, with the one-launch form's
+ * scratch in a fixed, static device array of this library instead of the
+ * array that forge_linear_bwd_step uses: the dX-completion counters of the
+ * one launch, one 32-bit word per 256-column block of W, 1024 words.  The
+ * pages have no counterpart of this entry point; it exists so that a caller
+ * can keep such steps off the scratch that forge_linear_bwd_step uses.
+ *   - No allocation, ever; the array's device address is looked up once per
+ *     device (cudaGetSymbolAddress, checked) and the counters this call uses
+ *     are cleared (set to zero) on `stream` before its launch.
+ *   - Requests the one launch applies to (bf16 weights, dX requested, T > 0,
+ *     N and K multiples of 64) with K > 262144 return FORGE_ERR_UNSUPPORTED
+ *     before any CUDA call.  Other requests need no scratch and run exactly
+ *     as forge_linear_bwd_step's two-launch form.
+ *   - Races: every call on a device uses the same array.  Two calls whose
+ *     launches overlap in time (different streams, no ordering between them)
+ *     corrupt each other's counters; order them on one stream or with events.
+ *     Calls of this entry point and of forge_linear_bwd_step do not share
+ *     scratch. */
+FORGE_API forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin,
+                                                      const forge_state_t* state, int32_t opt_kind,
+                                                      const forge_hparams_t* hp, int64_t step,
+                                                      uint64_t seed, void* stream);
+
 /* Whether forge_linear_bwd_step may run dX and the FORGE step in one launch
  * (non-zero, the default) or always uses two launches (0).  Process-wide. */
 FORGE_API void forge_set_step_fusion(int32_t enable);

@@ -61,6 +61,9 @@ _SIGNATURES = {
     "forge_linear_bwd_step": (c_int32, [ctypes.POINTER(ForgeLinear), ctypes.POINTER(ForgeState),
                                         c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
                                         c_void_p]),
+    "forge_linear_bwd_step_static": (c_int32, [ctypes.POINTER(ForgeLinear), ctypes.POINTER(ForgeState),
+                                               c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
+                                               c_void_p]),
     "forge_linear_dgrad": (c_int32, [ctypes.POINTER(ForgeLinear), c_void_p, c_int32, c_void_p]),
     "forge_unfused_wgrad": (c_int32, [ctypes.POINTER(ForgeLinear), c_void_p, c_void_p]),
     "forge_unfused_opt_step": (c_int32, [c_void_p, ctypes.POINTER(ForgeState), c_int64, c_int64,
@@ -183,6 +186,23 @@ def forge_linear_bwd_step(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1
     _check(lib().forge_linear_bwd_step(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
                                        ctypes.byref(hparams(**hp)), int(step),
                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def forge_linear_bwd_step_static(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1=None,
+                                 s2=None, s1_scale=None, s2_scale=None, dX=None, stream=None):
+    """forge_linear_bwd_step with its one-launch scratch in the library's own
+    static device array (no allocation; calls on one device must not overlap)."""
+    T, K = X.shape
+    N = W.shape[0]
+    _need(X, "X", torch.bfloat16, (T, K))
+    _need(dY, "dY", torch.bfloat16, (T, N))
+    if dX is not None:
+        _need(dX, "dX", torch.bfloat16, (T, K))
+    st = make_state(W, s1, s2, s1_scale, s2_scale)
+    lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), _ptr(dX))
+    _check(lib().forge_linear_bwd_step_static(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
+                                              ctypes.byref(hparams(**hp)), int(step),
+                                              int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
 def forge_linear_dgrad(dY, W, dX, stream=None):

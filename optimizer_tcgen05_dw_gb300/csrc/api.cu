@@ -31,6 +31,14 @@ __device__ uint32_t g_device_status;
 // steps on one device ordered (forge.h, forge_set_step_fusion).
 __device__ uint32_t g_dx_done[kMaxDxBlocks];
 
+// Scratch of forge_linear_bwd_step_static alone: that entry point's own
+// dX-completion counters for the one-launch step, one word per 256-column
+// block of W (1024 words: K up to 262144).  Static device memory, so the
+// entry point never allocates; cleared on the caller's stream before each
+// launch that uses it.
+constexpr int kStaticScratchWords = 1024;
+static __device__ __align__(256) uint32_t g_static_scratch[kStaticScratchWords];
+
 namespace {
 
 thread_local char g_msg[512] = "";
@@ -59,6 +67,7 @@ struct DeviceInfo {
   int num_sms = 0;
   uint32_t* status = nullptr;
   uint32_t* dx_done = nullptr;
+  uint32_t* static_scratch = nullptr;  // g_static_scratch on this device
   int step_pairs[2] = {0, 0};  // resident one-launch-step pairs, fp32 / INT8 states
   int cc_major = 0, cc_minor = 0;
 };
@@ -86,6 +95,9 @@ forge_status_t device_info(DeviceInfo* out) {
     if ((e = cudaGetSymbolAddress(&sym, g_dx_done)) != cudaSuccess)
       return cuda_fail(e, "cudaGetSymbolAddress(dX counters)");
     d.dx_done = static_cast<uint32_t*>(sym);
+    if ((e = cudaGetSymbolAddress(&sym, g_static_scratch)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    d.static_scratch = static_cast<uint32_t*>(sym);
     if (d.cc_major == 10 && d.cc_minor == 3) {
       d.step_pairs[0] = step_max_pairs(kSFp32);
       d.step_pairs[1] = step_max_pairs(kSInt8);
@@ -397,7 +409,7 @@ forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_
 // tiles over (N, K) reducing over T.
 forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state, int32_t opt_kind,
                            const OptScalars& sc, int64_t step, uint64_t seed, cudaStream_t s,
-                           const DeviceInfo& d) {
+                           const DeviceInfo& d, uint32_t* counters = nullptr) {
   const int64_t T = lin->T, N = lin->N, K = lin->K;
   forge_status_t st;
   CUtensorMap ma, mb, mda, mdb, m1, m2;
@@ -421,10 +433,10 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   p.dx_tiles = p.dx_tiles_m * p.tiles_n;
   p.dx_num_kb = static_cast<int32_t>((N + kFusedBlockK - 1) / kFusedBlockK);
   p.dx_out = lin->dX;
-  p.dx_done = d.dx_done;
+  p.dx_done = counters != nullptr ? counters : d.dx_done;
   p.dx_target = static_cast<uint32_t>(2 * p.dx_tiles_m);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(d.dx_done, 0, static_cast<size_t>(p.tiles_n) * sizeof(uint32_t), s)) != cudaSuccess)
+  if ((e = cudaMemsetAsync(p.dx_done, 0, static_cast<size_t>(p.tiles_n) * sizeof(uint32_t), s)) != cudaSuccess)
     return cuda_fail(e, "clearing the dX counters");
   // Every pair must be resident at once (dW tiles wait for other pairs' dX
   // tiles): at most the occupancy limit, at most one pair per tile.
@@ -508,6 +520,31 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
       cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
+}
+
+forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const forge_state_t* state,
+                                            int32_t opt_kind, const forge_hparams_t* hp,
+                                            int64_t step, uint64_t seed, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if ((st = check_linear(lin, true)) != FORGE_OK) return st;
+  if ((st = check_hp(opt_kind, hp, step)) != FORGE_OK) return st;
+  if ((st = check_state(state, opt_kind, lin->N, lin->K)) != FORGE_OK) return st;
+  const bool one_launch = lin->dX != nullptr && lin->T > 0 && lin->N > 0 && lin->K > 0 &&
+                          state->w_dtype == FORGE_W_BF16_SR && lin->N % 64 == 0 && lin->K % 64 == 0;
+  if (!one_launch)  // no scratch needed: the regular entry point's two-launch form
+    return forge_linear_bwd_step(lin, state, opt_kind, hp, step, seed, stream);
+  const int64_t blocks = (lin->K + kTileN - 1) / kTileN;
+  if (blocks > kStaticScratchWords)
+    return fail(FORGE_ERR_UNSUPPORTED, "K = %lld needs %lld scratch counters; the static scratch holds %d",
+                static_cast<long long>(lin->K), static_cast<long long>(blocks), kStaticScratchWords);
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  if ((st = check_device(d)) != FORGE_OK) return st;
+  if (d.step_pairs[state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0] <= 0)
+    return fail(FORGE_ERR_UNSUPPORTED, "the one-launch step cannot be resident on this device");
+  return launch_step(lin, state, opt_kind, make_scalars(opt_kind, *hp, step), step, seed,
+                     static_cast<cudaStream_t>(stream), d, d.static_scratch);
 }
 
 void forge_set_step_fusion(int32_t enable) { g_step_fusion.store(enable != 0 ? 1 : 0); }
