@@ -412,13 +412,14 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
                            const DeviceInfo& d, uint32_t* counters = nullptr) {
   const int64_t T = lin->T, N = lin->N, K = lin->K;
   forge_status_t st;
-  CUtensorMap ma, mb, mda, mdb, m1, m2;
+  CUtensorMap ma, mb, mda, mdb, m1, m2, mdx;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   if ((st = wgrad_maps(lin, kFusedBlockK, &ma, &mb, &p.op3d)) != FORGE_OK) return st;
   if ((st = bf16_map(&mda, lin->dY, N, T, 64, kTileM)) != FORGE_OK) return st;
   if ((st = mn_major_3d_map(&mdb, state->W, K, N, kFusedBlockK, kTileN / 2 / 64)) != FORGE_OK) return st;
   if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
+  if ((st = bf16_map(&mdx, lin->dX, K, T, 64, kTileM)) != FORGE_OK) return st;
   fill_tiles(p, N, K, T, kFusedBlockK);
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
@@ -432,7 +433,6 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   p.dx_tiles_m = static_cast<int32_t>((T + 2 * kTileM - 1) / (2 * kTileM));
   p.dx_tiles = p.dx_tiles_m * p.tiles_n;
   p.dx_num_kb = static_cast<int32_t>((N + kFusedBlockK - 1) / kFusedBlockK);
-  p.dx_out = lin->dX;
   p.dx_done = counters != nullptr ? counters : d.dx_done;
   p.dx_target = static_cast<uint32_t>(2 * p.dx_tiles_m);
   cudaError_t e;
@@ -443,7 +443,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   const int sdt = state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0;
   const int pairs = std::min(d.num_sms / 2, d.step_pairs[sdt]);
   const int tiles = p.num_tiles + p.dx_tiles;
-  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, p, 2 * std::min(tiles, pairs), s)) !=
+  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, p, 2 * std::min(tiles, pairs), s)) !=
       cudaSuccess)
     return cuda_fail(e, "one-launch step");
   return FORGE_OK;

@@ -111,7 +111,6 @@ struct GemmParams {
   int32_t dx_tiles_m;        // 256-row pair tiles over T
   int32_t dx_tiles;          // dx_tiles_m * tiles_n
   int32_t dx_num_kb;         // reduction blocks of 64 over M
-  void* dx_out;              // bf16 [dx_rows x Ncols]
   uint32_t* dx_done;         // [tiles_n], zero at launch
   uint32_t dx_target;        // 2 * dx_tiles_m
 };

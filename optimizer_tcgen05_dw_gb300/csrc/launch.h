@@ -31,10 +31,12 @@ cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtens
                             const CUtensorMap& s1, const CUtensorMap& s2, const GemmParams& p,
                             int grid, cudaStream_t s);
 // tc_step.cu: dX and the FORGE step in one launch (mode kModeStep, bf16
-// weights): a, b the dW operands, da, db the dX operands (dY K-major, W).
+// weights): a, b the dW operands, da, db the dX operands (dY K-major, W),
+// dx the dX output (bf16, 64-column x 128-row boxes, 128-byte swizzle).
 cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
-                           const CUtensorMap& s2, const GemmParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p,
+                           int grid, cudaStream_t s);
 // CTA pairs of the one-launch step that can be resident at once (its dW tiles
 // wait for dX tiles of other pairs, so its grid must not exceed this); 0 if
 // the query fails.

@@ -11,7 +11,7 @@ static cudaError_t run_fused(const CUtensorMap& a, const CUtensorMap& b, const C
   constexpr int smem = KCfg<kModeFusedOpt, WDT>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pair(k, grid, KCfg<kModeFusedOpt, WDT>::kThreads, smem, s, a, b, a, b, s1, s2, p);
+  return launch_pair(k, grid, KCfg<kModeFusedOpt, WDT>::kThreads, smem, s, a, b, a, b, s1, s2, a, p);
 }
 
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,

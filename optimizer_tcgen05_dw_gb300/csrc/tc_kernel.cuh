@@ -809,28 +809,23 @@ __device__ __forceinline__ bool bounded_wait_count(const uint32_t* cnt, uint32_t
 }
 
 // One dX tile of the one-launch step, by a compute warp: 64 columns
-// (sub*64..) of TMEM lane row r, rounded to bf16 (nearest even) and stored
-// to dX row `row`, columns col0.. (whole groups of 8 inside the K columns).
-__device__ __forceinline__ void epi_dx_store(uint32_t taddr, int64_t row, int col0,
-                                             const GemmParams& p) {
-  const bool row_ok = row < p.dx_rows;
-  uint16_t* out = static_cast<uint16_t*>(p.dx_out) + row * static_cast<int64_t>(p.Ncols);
+// (sub*64..) of TMEM lane row r, rounded to bf16 (nearest even) and written
+// to row r of `box`, a 128-row x 64-column bf16 box in shared memory laid out
+// with the 128-byte swizzle, from where the I/O thread stores it with TMA.
+__device__ __forceinline__ void epi_dx_stage(uint32_t taddr, uint8_t* box, int r) {
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     float g[32];
     ptx::tmem_ld_32x32b_x32(taddr + c * 32, g);
-    if (!row_ok) continue;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int col = col0 + c * 32 + q * 8;
-      if (col >= p.Ncols) continue;
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const __nv_bfloat162 h = __floats2bfloat162_rn(g[8 * q + 2 * j], g[8 * q + 2 * j + 1]);
         o[j] = *reinterpret_cast<const uint32_t*>(&h);
       }
-      *reinterpret_cast<uint4*>(out + col) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(box + sw128(r, 4 * c + q)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
@@ -849,8 +844,8 @@ __device__ __forceinline__ void epi_dx_store(uint32_t taddr, int64_t row, int co
 // counted, so no weight is written while a dX tile may still read it.
 template <int KIND, int SDT, bool STEP>
 __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
-                                 const GemmParams& p, SharedState* ss, uint8_t* epi, int lane,
-                                 uint32_t rank) {
+                                 const CUtensorMap* mDX, const GemmParams& p, SharedState* ss,
+                                 uint8_t* epi, int lane, uint32_t rank) {
   using G = StagedGeom<KIND, SDT>;
   TileWalk<G::kChunks> walk;
   walk.init(p, rank);
@@ -877,28 +872,40 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
     ptx::bulk_commit_group();
   };
   int issued = 0, consumed = 0, local = -1;
-  if (io && total > 0) {
-    issue(0);
-    issued = 1;
-  }
   bool aborted = false;
-  if (STEP) {
+  if (STEP) {  // the dX tiles: staged in both epilogue buffers, stored with TMA
     const int ndx = my_dx_tiles(p);
     for (int i = 0; i < ndx; ++i) {
       ++local;
       bool ok = true;
-      if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
-      if (io && ok) {
-        int tm, tn;
-        dx_tile_coords(i, p, tm, tn);
-        ptx::red_release_gpu_add(p.dx_done + tn, 1u);
+      int tm, tn;
+      dx_tile_coords(i, p, tm, tn);
+      if (io) {
+        ptx::bulk_wait_group_read0();  // the previous dX tile's stores have read the staging
+        ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
       }
+      if (io && ok) ptx::red_release_gpu_add(p.dx_done + tn, 1u);
       if (ptx::bar_red_or(kEpiBarrier, G::kNB, !ok)) {
         aborted = true;
         break;
       }
-      ptx::bar_sync(kEpiBarrier, G::kNB);  // the compute warps have stored the tile
+      ptx::bar_sync(kEpiBarrier, G::kNB);  // the compute warps have staged the tile
+      if (io) {
+        const int row0 = tm * kPairM + static_cast<int>(rank) * kTileM;
+        const int col0 = tn * kTileN;
+        if (row0 < p.dx_rows) {
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (col0 + 64 * b < p.Ncols) ptx::tma_store_2d(mDX, epi + b * 16384, col0 + 64 * b, row0);
+        }
+        ptx::bulk_commit_group();
+      }
     }
+    if (io) ptx::bulk_wait_group_read0();  // the buffers are free for the weight tiles' states
+  }
+  if (io && total > 0 && !aborted) {
+    issue(0);
+    issued = 1;
   }
   const int first = local + 1;  // accumulator index of the first dW tile
   for (int j = 0; j < total && !aborted; ++j) {
@@ -972,19 +979,17 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   uint4 wnext[kWPerThread / 8];
   float o1next = 0.f, o2next = 0.f;  // old INT8 scales of the next chunk
   int local = -1;
-  if (STEP) {  // the pair's dX tiles: 64 columns per warp, straight to global memory
+  if (STEP) {  // the pair's dX tiles: 64 columns per warp into the staging boxes
     const int ndx = my_dx_tiles(p);
     for (int i = 0; i < ndx; ++i) {
       ++local;
       if (ptx::bar_red_or(kEpiBarrier, G::kNB, false)) return;  // the I/O warp's verdict
       ptx::tc_fence_after();
-      int tm, tn;
-      dx_tile_coords(i, p, tm, tn);
       const int acc = local & 1;
       const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                              static_cast<uint32_t>(acc * kTileN + sub * 64);
-      epi_dx_store(taddr, static_cast<int64_t>(tm) * kPairM + static_cast<int>(rank) * kTileM + r,
-                   tn * kTileN + sub * 64, p);
+      epi_dx_stage(taddr, epi + sub * 16384, r);
+      ptx::fence_proxy_async_smem();  // the staged values, visible to the TMA store
       ptx::tc_fence_before();
       ptx::bar_sync(kEpiBarrier, G::kNB);
       if (lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
@@ -1040,28 +1045,29 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 
 template <int KIND, int SDT, bool STEP>
 __device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CUtensorMap* mS2,
-                                                const GemmParams& p, SharedState* ss, uint8_t* epi,
-                                                int warp, int lane, uint32_t rank) {
+                                                const CUtensorMap* mDX, const GemmParams& p,
+                                                SharedState* ss, uint8_t* epi, int warp, int lane,
+                                                uint32_t rank) {
   if (warp == 2 + kNumEpiWarpsStaged)
-    epilogue_io_role<KIND, SDT, STEP>(mS1, mS2, p, ss, epi, lane, rank);
+    epilogue_io_role<KIND, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, lane, rank);
   else
     epilogue_compute_role<KIND, SDT, STEP>(p, ss, epi, warp, lane, rank);
 }
 
 template <int SDT, bool STEP>
 __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, const CUtensorMap* mS2,
-                                                      const GemmParams& p, SharedState* ss,
-                                                      uint8_t* epi, int warp, int lane,
-                                                      uint32_t rank) {
+                                                      const CUtensorMap* mDX, const GemmParams& p,
+                                                      SharedState* ss, uint8_t* epi, int warp,
+                                                      int lane, uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_staged<kAdamW, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kNAdam: epilogue_staged<kNAdam, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kRAdam: epilogue_staged<kRAdam, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kLion: epilogue_staged<kLion, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kRMSprop: epilogue_staged<kRMSprop, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    case kSGD: epilogue_staged<kSGD, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
-    default: epilogue_staged<kSGDMomentum, SDT, STEP>(mS1, mS2, p, ss, epi, warp, lane, rank); break;
+    case kAdamW: epilogue_staged<kAdamW, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_staged<kNAdam, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_staged<kRAdam, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_staged<kLion, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_staged<kRMSprop, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_staged<kSGD, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_staged<kSGDMomentum, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
   }
 }
 
@@ -1072,7 +1078,8 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ CUtensorMap mapDA, const __grid_constant__ CUtensorMap mapDB,
               const __grid_constant__ CUtensorMap mapS1,
-              const __grid_constant__ CUtensorMap mapS2, const GemmParams p) {
+              const __grid_constant__ CUtensorMap mapS2, const __grid_constant__ CUtensorMap mapDX,
+              const GemmParams p) {
   using Cfg = KCfg<MODE, WDT>;
   constexpr int STG = Cfg::kStg;
   extern __shared__ uint8_t smem_raw[];
@@ -1124,7 +1131,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT, MODE == kModeStep>(&mapS1, &mapS2, p, ss, epi, warp, lane, rank);
+      epilogue_tma_dispatch<SDT, MODE == kModeStep>(&mapS1, &mapS2, &mapDX, p, ss, epi, warp, lane, rank);
     else
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
@@ -1144,7 +1151,7 @@ template <typename Kernel>
 inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaStream_t s,
                                const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
                                const CUtensorMap& db, const CUtensorMap& s1,
-                               const CUtensorMap& s2, const GemmParams& p) {
+                               const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
@@ -1157,7 +1164,7 @@ inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaSt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, da, db, s1, s2, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, da, db, s1, s2, dx, p);
 }
 
 }  // namespace forge

@@ -9,12 +9,12 @@ namespace forge {
 template <int SDT>
 static cudaError_t run_step(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
                             const CUtensorMap& db, const CUtensorMap& s1, const CUtensorMap& s2,
-                            const GemmParams& p, int grid, cudaStream_t s) {
+                            const CUtensorMap& dx, const GemmParams& p, int grid, cudaStream_t s) {
   auto* k = tc_kernel<kModeStep, kWBf16, SDT>;
   constexpr int smem = KCfg<kModeStep, kWBf16>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pair(k, grid, KCfg<kModeStep, kWBf16>::kThreads, smem, s, a, b, da, db, s1, s2, p);
+  return launch_pair(k, grid, KCfg<kModeStep, kWBf16>::kThreads, smem, s, a, b, da, db, s1, s2, dx, p);
 }
 
 template <int SDT>
@@ -42,9 +42,10 @@ int step_max_pairs(int sdt) { return sdt == kSInt8 ? step_pairs<kSInt8>() : step
 
 cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
-                           const CUtensorMap& s2, const GemmParams& p, int grid, cudaStream_t s) {
-  return sdt == kSInt8 ? run_step<kSInt8>(a, b, da, db, s1, s2, p, grid, s)
-                       : run_step<kSFp32>(a, b, da, db, s1, s2, p, grid, s);
+                           const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p,
+                           int grid, cudaStream_t s) {
+  return sdt == kSInt8 ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, p, grid, s)
+                       : run_step<kSFp32>(a, b, da, db, s1, s2, dx, p, grid, s);
 }
 
 }  // namespace forge
