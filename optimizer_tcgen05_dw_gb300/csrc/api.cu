@@ -404,6 +404,40 @@ forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_
   return FORGE_OK;
 }
 
+// Deal the one-launch step's dX tiles over `pairs` so that the largest
+// per-pair work (dX tiles plus dW tiles) is smallest.  dW tiles go
+// round-robin: the first num_tiles % pairs pairs get one more ("heavy").  A
+// dW tile costs about c = 1.1 T / N dX tiles (reductions over T and N, plus
+// its optimizer epilogue).  The kernel deals dx_rounds rounds to every pair
+// and the rest round-robin to the pairs from dx_heavy on.  Candidates: all
+// full rounds with the few left-over tiles on the last pairs (away from the
+// heavy ones), or fewer rounds with the rest on the light pairs; the
+// smallest modelled maximum wins.
+void balance_dx(GemmParams& p, int pairs, int64_t T, int64_t N) {
+  const int D = p.dx_tiles, F = p.num_tiles;
+  const int heavy = F % pairs, fl = F / pairs;
+  const double c = 1.1 * static_cast<double>(T) / static_cast<double>(N);
+  const int full = D / pairs, ex = D % pairs;
+  // full rounds; the ex left-over tiles on pairs pairs-ex .. pairs-1
+  double best = full + fl * c;
+  if (ex > 0) best = std::max(best, full + 1 + fl * c);
+  if (heavy > 0) best = std::max(best, full + (fl + 1) * c);
+  if (ex > 0 && heavy > pairs - ex) best = std::max(best, full + 1 + (fl + 1) * c);
+  p.dx_rounds = full;
+  p.dx_heavy = pairs - ex;
+  if (heavy == 0) return;
+  const int nl = pairs - heavy;
+  for (int r = full; r >= 0; --r) {  // r rounds, the rest on the light pairs
+    const int rem = D - r * pairs;
+    const double load = std::max(r + (rem + nl - 1) / nl + fl * c, r + (fl + 1) * c);
+    if (load + 1e-9 < best) {
+      best = load;
+      p.dx_rounds = r;
+      p.dx_heavy = heavy;
+    }
+  }
+}
+
 // dX and the FORGE step in one persistent launch (bf16 weights; N and K
 // multiples of 64; T > 0): dX tiles over (T, K) reducing over N, then dW
 // tiles over (N, K) reducing over T.
@@ -441,9 +475,9 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   // Every pair must be resident at once (dW tiles wait for other pairs' dX
   // tiles): at most the occupancy limit, at most one pair per tile.
   const int sdt = state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0;
-  const int pairs = std::min(d.num_sms / 2, d.step_pairs[sdt]);
-  const int tiles = p.num_tiles + p.dx_tiles;
-  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, p, 2 * std::min(tiles, pairs), s)) !=
+  const int pairs = std::min(std::min(d.num_sms / 2, d.step_pairs[sdt]), p.num_tiles + p.dx_tiles);
+  balance_dx(p, pairs, T, N);
+  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, p, 2 * pairs, s)) !=
       cudaSuccess)
     return cuda_fail(e, "one-launch step");
   return FORGE_OK;

@@ -113,6 +113,11 @@ struct GemmParams {
   int32_t dx_num_kb;         // reduction blocks of 64 over M
   uint32_t* dx_done;         // [tiles_n], zero at launch
   uint32_t dx_target;        // 2 * dx_tiles_m
+  // How the dX tiles are dealt (balancing the pairs' total work): every pair
+  // takes one per round for dx_rounds rounds; the rest go round-robin to the
+  // pairs from dx_heavy on, those without an extra dW tile.
+  int32_t dx_rounds;
+  int32_t dx_heavy;
 };
 
 }  // namespace forge

@@ -129,15 +129,26 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
 __device__ __forceinline__ int pair_id() { return static_cast<int>(blockIdx.x) >> 1; }
 __device__ __forceinline__ int num_pairs() { return static_cast<int>(gridDim.x) >> 1; }
 
-// One-launch step: a pair first runs its dX tiles, dealt round-robin from
-// the last pair down (so the pairs that get an extra dW tile get one dX tile
-// fewer), then its dW tiles pair_id(), pair_id() + num_pairs(), ...
+// One-launch step: a pair first runs its dX tiles, then its dW tiles
+// pair_id(), pair_id() + num_pairs(), ...  The dX tiles are dealt in rounds,
+// one per pair for the first dx_rounds rounds, then round-robin over the
+// pairs from dx_heavy on (those with one dW tile fewer), so the pairs' work
+// comes out about even; consecutive tiles run side by side in every round.
 __device__ __forceinline__ int my_dx_tiles(const GemmParams& p) {
-  const int rp = num_pairs() - 1 - pair_id();
-  return p.dx_tiles > rp ? (p.dx_tiles - 1 - rp) / num_pairs() + 1 : 0;
+  int n = p.dx_rounds;
+  if (pair_id() >= p.dx_heavy) {
+    const int nl = num_pairs() - p.dx_heavy, lr = pair_id() - p.dx_heavy;
+    const int rem = p.dx_tiles - p.dx_rounds * num_pairs();
+    n += rem > lr ? (rem - 1 - lr) / nl + 1 : 0;
+  }
+  return n;
 }
 __device__ __forceinline__ void dx_tile_coords(int i, const GemmParams& p, int& tm, int& tn) {
-  tile_coords_of(num_pairs() - 1 - pair_id() + i * num_pairs(), p.dx_tiles_m, p.tiles_n, tm, tn);
+  const int d = i < p.dx_rounds
+                    ? i * num_pairs() + pair_id()
+                    : p.dx_rounds * num_pairs() + (i - p.dx_rounds) * (num_pairs() - p.dx_heavy) +
+                          (pair_id() - p.dx_heavy);
+  tile_coords_of(d, p.dx_tiles_m, p.tiles_n, tm, tn);
 }
 
 template <int MODE, int STG, int BK>
