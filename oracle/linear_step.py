@@ -21,8 +21,9 @@ Per element the order is: dequantise states -> rule (float32) -> requantise
 states (new block absmax) and round the weight.
 
 Layouts (row-major): X [T, K] bf16, dY [T, N] bf16, W [N, K] (float32 master or
-bf16), states [N, K] (float32, or int8/uint8 codes with float32 absmax
-[N, K / 64]), dX [T, K] bf16.  bf16 tensors are numpy uint16 bit patterns.
+bf16), states [N, K] (float32; int8/uint8 codes with float32 absmax
+[N, K / 64]; or bf16 rounded to nearest even), dX [T, K] bf16.  bf16 tensors
+are numpy uint16 bit patterns.
 
 TEST INFRASTRUCTURE ONLY (see oracle/__init__.py).
 """
@@ -88,12 +89,15 @@ def weights_for_dx(W, w_dtype: str) -> np.ndarray:
 # ----------------------------------------------------------------------------
 
 def update_block(kind, hp, step, seed, g, W, w_dtype, s1=None, s2=None,
-                 s1_scale=None, s2_scale=None, s_dtype="fp32", n0=0, k0=0, K=None):
+                 s1_scale=None, s2_scale=None, s_dtype="fp32", n0=0, k0=0, K=None,
+                 block=64):
     """Apply one optimizer step to the block W[n0:n0+R, k0:k0+C] given its gradient g.
 
     K is the full row length of W (for the element index n*K + k that keys the
-    stochastic rounding).  Returns a dict with W, s1, s2, s1_scale, s2_scale for
-    the block (None where unused)."""
+    stochastic rounding).  s_dtype: 'fp32', 'int8' (codes with an absmax per
+    `block` row elements; 64 is the method's) or 'bf16' (moments stored as
+    bf16, rounded to nearest even after the FP32 update).  Returns a dict with
+    W, s1, s2, s1_scale, s2_scale for the block (None where unused)."""
     g = np.asarray(g, dtype=np.float32)
     R, C = g.shape
     if K is None:
@@ -103,8 +107,11 @@ def update_block(kind, hp, step, seed, g, W, w_dtype, s1=None, s2=None,
     wf = bf16_bits_to_f32(W) if w_dtype == "bf16" else np.asarray(W, dtype=np.float32)
     # dequantise states
     if s_dtype == "int8":
-        m = dequantize_blocks(s1, s1_scale, signed=True) if uses1 else None
-        v = dequantize_blocks(s2, s2_scale, signed=False) if uses2 else None
+        m = dequantize_blocks(s1, s1_scale, signed=True, block=block) if uses1 else None
+        v = dequantize_blocks(s2, s2_scale, signed=False, block=block) if uses2 else None
+    elif s_dtype == "bf16":
+        m = bf16_bits_to_f32(s1) if uses1 else None
+        v = bf16_bits_to_f32(s2) if uses2 else None
     else:
         m = np.asarray(s1, dtype=np.float32) if uses1 else None
         v = np.asarray(s2, dtype=np.float32) if uses2 else None
@@ -120,9 +127,12 @@ def update_block(kind, hp, step, seed, g, W, w_dtype, s1=None, s2=None,
         out["W"] = w_new.astype(np.float32)
     if s_dtype == "int8":
         if uses1:
-            out["s1"], out["s1_scale"] = quantize_blocks(m_new, signed=True)
+            out["s1"], out["s1_scale"] = quantize_blocks(m_new, signed=True, block=block)
         if uses2:
-            out["s2"], out["s2_scale"] = quantize_blocks(v_new, signed=False)
+            out["s2"], out["s2_scale"] = quantize_blocks(v_new, signed=False, block=block)
+    elif s_dtype == "bf16":
+        out["s1"] = bf16_bits_rne(m_new) if uses1 else None
+        out["s2"] = bf16_bits_rne(v_new) if uses2 else None
     else:
         out["s1"] = m_new.astype(np.float32) if uses1 else None
         out["s2"] = v_new.astype(np.float32) if uses2 else None
@@ -138,7 +148,7 @@ def linear_bwd_step(X_bits, dY_bits, state: dict, kind: int, hp, step: int, seed
     """One full step on one layer.
 
     state: dict with W (float32 or uint16 bf16 bits), w_dtype ('fp32' | 'bf16'),
-    s_dtype ('fp32' | 'int8'), s1, s2, s1_scale, s2_scale.  Returns a new dict of
+    s_dtype ('fp32' | 'int8' | 'bf16'), s1, s2, s1_scale, s2_scale.  Returns a new dict of
     the same form plus 'dX' (bf16 bits) when want_dx."""
     W = state["W"]
     w_dtype, s_dtype = state["w_dtype"], state["s_dtype"]

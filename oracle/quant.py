@@ -28,15 +28,16 @@ def _levels(signed: bool) -> np.float32:
     return np.float32(127.0) if signed else np.float32(255.0)
 
 
-def quantize_blocks(x, signed: bool):
-    """x: float32 [rows, cols] with cols % 64 == 0.
+def quantize_blocks(x, signed: bool, block: int = BLOCK):
+    """x: float32 [rows, cols] with cols % block == 0 (block 64 is the method's;
+    other sizes serve the block-size comparison).
 
     Returns (codes, absmax): codes int8 (signed) or uint8 (unsigned) [rows, cols],
-    absmax float32 [rows, cols // 64]."""
+    absmax float32 [rows, cols // block]."""
     x = np.asarray(x, dtype=np.float32)
     rows, cols = x.shape
-    assert cols % BLOCK == 0
-    xb = x.reshape(rows, cols // BLOCK, BLOCK)
+    assert cols % block == 0
+    xb = x.reshape(rows, cols // block, block)
     ax = np.abs(xb)
     # NaN never wins the maximum (it compares false), matching a running max
     # that only replaces on a strictly larger value.
@@ -53,10 +54,10 @@ def quantize_blocks(x, signed: bool):
     return codes, absmax
 
 
-def dequantize_blocks(codes, absmax, signed: bool) -> np.ndarray:
+def dequantize_blocks(codes, absmax, signed: bool, block: int = BLOCK) -> np.ndarray:
     codes = np.asarray(codes)
     rows, cols = codes.shape
-    absmax = np.asarray(absmax, dtype=np.float32).reshape(rows, cols // BLOCK)
+    absmax = np.asarray(absmax, dtype=np.float32).reshape(rows, cols // block)
     s = (absmax / _levels(signed)).astype(np.float32)
-    qf = codes.astype(np.float32).reshape(rows, cols // BLOCK, BLOCK)
+    qf = codes.astype(np.float32).reshape(rows, cols // block, block)
     return (qf * s[..., None]).astype(np.float32).reshape(rows, cols)
