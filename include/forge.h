@@ -80,7 +80,13 @@ typedef enum forge_wdtype { FORGE_W_FP32 = 0, FORGE_W_BF16_SR = 1 } forge_wdtype
  * block.  s1 (may be negative) is int8 with codes -127..127 and value
  * code * (absmax/127); s2 (never negative) is uint8 with codes 0..255 and value
  * code * (absmax/255).  Scale arrays are [N x K/64] FP32. */
-typedef enum forge_sdtype { FORGE_STATE_FP32 = 0, FORGE_STATE_INT8_B64 = 1 } forge_sdtype_t;
+typedef enum forge_sdtype {
+  FORGE_STATE_FP32 = 0,      /* float32 moments                                           */
+  FORGE_STATE_INT8_B64 = 1,  /* int8 / uint8 codes, float32 absmax per 64 row elements     */
+  FORGE_STATE_BF16 = 2       /* bf16 moments, rounded to nearest even after the FP32 rule; */
+                             /* with fp32 weights only the optimizer-only entry points and */
+                             /* T = 0 accept them (the fused kernels stage bf16 weights)    */
+} forge_sdtype_t;
 
 /* The activations of one linear layer. */
 typedef struct forge_linear {

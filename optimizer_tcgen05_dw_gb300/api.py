@@ -21,7 +21,7 @@ c_int32, c_int64, c_uint64, c_float, c_void_p = (ctypes.c_int32, ctypes.c_int64,
 OPT_KINDS = {"adamw": 0, "nadam": 1, "radam": 2, "lion": 3, "rmsprop": 4, "adagrad": 5,
              "sgd": 6, "sgd_momentum": 7}
 W_FP32, W_BF16_SR = 0, 1
-STATE_FP32, STATE_INT8_B64 = 0, 1
+STATE_FP32, STATE_INT8_B64, STATE_BF16 = 0, 1, 2
 USES_S1 = {"adamw", "nadam", "radam", "lion", "sgd_momentum"}
 USES_S2 = {"adamw", "nadam", "radam", "rmsprop", "adagrad"}
 
@@ -156,6 +156,12 @@ def make_state(W, s1=None, s2=None, s1_scale=None, s2_scale=None) -> ForgeState:
         raise TypeError(f"W must be float32 or bfloat16, got {W.dtype}")
     _need(W, "W", W.dtype, (N, K))
     int8 = any(t is not None and t.dtype in (torch.int8, torch.uint8) for t in (s1, s2))
+    bf16 = any(t is not None and t.dtype == torch.bfloat16 for t in (s1, s2))
+    if bf16:
+        for t, nm in ((s1, "s1"), (s2, "s2")):
+            if t is not None:
+                _need(t, nm, torch.bfloat16, (N, K))
+        return ForgeState(_ptr(W), wdt, STATE_BF16, _ptr(s1), _ptr(s2), None, None)
     if int8:
         if s1 is not None:
             _need(s1, "s1", torch.int8, (N, K))

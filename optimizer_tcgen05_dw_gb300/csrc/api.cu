@@ -68,7 +68,7 @@ struct DeviceInfo {
   uint32_t* status = nullptr;
   uint32_t* dx_done = nullptr;
   uint32_t* static_scratch = nullptr;  // g_static_scratch on this device
-  int step_pairs[2] = {0, 0};  // resident one-launch-step pairs, fp32 / INT8 states
+  int step_pairs[3] = {0, 0, 0};  // resident one-launch-step pairs, by state dtype
   int cc_major = 0, cc_minor = 0;
 };
 
@@ -99,8 +99,9 @@ forge_status_t device_info(DeviceInfo* out) {
       return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
     d.static_scratch = static_cast<uint32_t*>(sym);
     if (d.cc_major == 10 && d.cc_minor == 3) {
-      d.step_pairs[0] = step_max_pairs(kSFp32);
-      d.step_pairs[1] = step_max_pairs(kSInt8);
+      d.step_pairs[kSFp32] = step_max_pairs(kSFp32);
+      d.step_pairs[kSInt8] = step_max_pairs(kSInt8);
+      d.step_pairs[kSBf16] = step_max_pairs(kSBf16);
     }
     g_dev[dev] = d;
     g_dev_ready[dev] = true;
@@ -206,8 +207,8 @@ forge_status_t wgrad_maps(const forge_linear_t* lin, int bk, CUtensorMap* ma, CU
 
 // Maps of the state tiles the bf16-weight epilogue stages through shared
 // memory: fp32 states in 32-column boxes (128-byte rows, 128-byte swizzle),
-// INT8 codes in 64-column boxes (64-byte rows, 64-byte swizzle); 128 rows
-// each.  A rule that keeps no such state gets a copy of `other` (unused).
+// INT8 codes in 64-column boxes and bf16 states in 32-column boxes (64-byte
+// rows, 64-byte swizzle); 128 rows each.  A rule that keeps no such state gets a copy of `other` (unused).
 forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t K,
                           const CUtensorMap& other, CUtensorMap* m1, CUtensorMap* m2) {
   *m1 = other;
@@ -220,6 +221,9 @@ forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t 
     if (!used[i]) continue;
     forge_status_t r =
         int8 ? tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, K, N, 64, kTileM,
+                          CU_TENSOR_MAP_SWIZZLE_64B)
+        : st->s_dtype == FORGE_STATE_BF16
+             ? tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, 32, kTileM,
                           CU_TENSOR_MAP_SWIZZLE_64B)
              : tensor_map(maps[i], bufs[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, K, N, 32, kTileM,
                           CU_TENSOR_MAP_SWIZZLE_128B);
@@ -307,7 +311,8 @@ forge_status_t check_state(const forge_state_t* st, int kind, int64_t N, int64_t
   if (st == nullptr) return fail(FORGE_ERR_INVALID_ARG, "state is NULL");
   if (st->w_dtype != FORGE_W_FP32 && st->w_dtype != FORGE_W_BF16_SR)
     return fail(FORGE_ERR_INVALID_ARG, "w_dtype %d", st->w_dtype);
-  if (st->s_dtype != FORGE_STATE_FP32 && st->s_dtype != FORGE_STATE_INT8_B64)
+  if (st->s_dtype != FORGE_STATE_FP32 && st->s_dtype != FORGE_STATE_INT8_B64 &&
+      st->s_dtype != FORGE_STATE_BF16)
     return fail(FORGE_ERR_INVALID_ARG, "s_dtype %d", st->s_dtype);
   if (N * K > 0 && (st->W == nullptr || !aligned16(st->W)))
     return fail(FORGE_ERR_INVALID_ARG, "W must be a non-NULL 16-byte aligned device pointer");
@@ -474,8 +479,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
     return cuda_fail(e, "clearing the dX counters");
   // Every pair must be resident at once (dW tiles wait for other pairs' dX
   // tiles): at most the occupancy limit, at most one pair per tile.
-  const int sdt = state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0;
-  const int pairs = std::min(std::min(d.num_sms / 2, d.step_pairs[sdt]), p.num_tiles + p.dx_tiles);
+  const int pairs = std::min(std::min(d.num_sms / 2, d.step_pairs[state->s_dtype]), p.num_tiles + p.dx_tiles);
   balance_dx(p, pairs, T, N);
   if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, p, 2 * pairs, s)) !=
       cudaSuccess)
@@ -505,6 +509,8 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   if ((st = check_hp(opt_kind, hp, step)) != FORGE_OK) return st;
   if ((st = check_state(state, opt_kind, lin->N, lin->K)) != FORGE_OK) return st;
   if (lin->N == 0 || lin->K == 0) return FORGE_OK;
+  if (state->s_dtype == FORGE_STATE_BF16 && state->w_dtype == FORGE_W_FP32 && lin->T > 0)
+    return fail(FORGE_ERR_UNSUPPORTED, "bf16 moments need bf16 weights in the fused step");
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
   if ((st = check_device(d)) != FORGE_OK) return st;
@@ -515,7 +521,7 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   // weights.
   if (lin->dX != nullptr && lin->T > 0 && state->w_dtype == FORGE_W_BF16_SR && lin->N % 64 == 0 &&
       lin->K % 64 == 0 && (lin->K + kTileN - 1) / kTileN <= kMaxDxBlocks && g_step_fusion.load() &&
-      d.step_pairs[state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0] > 0)
+      d.step_pairs[state->s_dtype] > 0)
     return launch_step(lin, state, opt_kind, sc, step, seed, s, d);
   // 1. dX from the pre-update weights, enqueued first on the same stream.
   if (lin->dX != nullptr && (st = launch_dgrad(lin, state->W, state->w_dtype, s, d)) != FORGE_OK) return st;
@@ -575,7 +581,7 @@ forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const for
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
   if ((st = check_device(d)) != FORGE_OK) return st;
-  if (d.step_pairs[state->s_dtype == FORGE_STATE_INT8_B64 ? 1 : 0] <= 0)
+  if (d.step_pairs[state->s_dtype] <= 0)
     return fail(FORGE_ERR_UNSUPPORTED, "the one-launch step cannot be resident on this device");
   return launch_step(lin, state, opt_kind, make_scalars(opt_kind, *hp, step), step, seed,
                      static_cast<cudaStream_t>(stream), d, d.static_scratch);

@@ -11,7 +11,7 @@ enum OptKind : int32_t {
   kRMSprop = 4, kAdaGrad = 5, kSGD = 6, kSGDMomentum = 7
 };
 enum WDtype : int32_t { kWFp32 = 0, kWBf16 = 1 };
-enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1 };
+enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1, kSBf16 = 2 };
 
 // Device-side status codes (values match forge_status_t).
 enum DeviceStatus : uint32_t { kStatusOk = 0, kStatusTimeout = 4 };

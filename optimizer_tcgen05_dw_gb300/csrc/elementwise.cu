@@ -62,6 +62,23 @@ __device__ __forceinline__ void store_codes8(void* base, int64_t e0, float a, co
   *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + e0) = make_uint2(w[0], w[1]);
 }
 
+__device__ __forceinline__ void load_bf16x8(const void* base, int64_t e0, float (&v)[8]) {
+  const uint4 b = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + e0);
+  const uint32_t w[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    v[2 * j] = dev::bf16_to_f32(w[j] & 0xFFFFu);
+    v[2 * j + 1] = dev::bf16_to_f32(w[j] >> 16);
+  }
+}
+
+__device__ __forceinline__ void store_bf16x8_rne(void* base, int64_t e0, const float (&v)[8]) {
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) o[j] = dev::bf16_rne(v[2 * j]) | (dev::bf16_rne(v[2 * j + 1]) << 16);
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + e0) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <int KIND, int WDT, int SDT>
 __device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemParams& p) {
   const int64_t e0 = gid * 8;
@@ -85,6 +102,9 @@ __device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemPa
     if (SDT == kSInt8) {
       if (uses_s1(KIND)) load_codes8<true>(p.s1, e0, p.s1_scale[sidx], s1);
       if (uses_s2(KIND)) load_codes8<false>(p.s2, e0, p.s2_scale[sidx], s2);
+    } else if (SDT == kSBf16) {
+      if (uses_s1(KIND)) load_bf16x8(p.s1, e0, s1);
+      if (uses_s2(KIND)) load_bf16x8(p.s2, e0, s2);
     } else {
       if (uses_s1(KIND)) load8(static_cast<const float*>(p.s1) + e0, s1);
       if (uses_s2(KIND)) load8(static_cast<const float*>(p.s2) + e0, s2);
@@ -105,6 +125,9 @@ __device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemPa
     if (SDT == kSFp32) {
       if (uses_s1(KIND)) store8(static_cast<float*>(p.s1) + e0, s1);
       if (uses_s2(KIND)) store8(static_cast<float*>(p.s2) + e0, s2);
+    } else if (SDT == kSBf16) {
+      if (uses_s1(KIND)) store_bf16x8_rne(p.s1, e0, s1);
+      if (uses_s2(KIND)) store_bf16x8_rne(p.s2, e0, s2);
     }
   }
   if (SDT == kSInt8) {
@@ -247,9 +270,11 @@ cudaError_t launch_opt_step(int wdt, int sdt, const ElemParams& p, int num_sms, 
   const int grid = elem_grid(p.N * p.K / 8, num_sms);
   if (wdt == kWBf16) {
     if (sdt == kSInt8) opt_step_kernel<kWBf16, kSInt8><<<grid, kElemThreads, 0, s>>>(p);
+    else if (sdt == kSBf16) opt_step_kernel<kWBf16, kSBf16><<<grid, kElemThreads, 0, s>>>(p);
     else opt_step_kernel<kWBf16, kSFp32><<<grid, kElemThreads, 0, s>>>(p);
   } else {
     if (sdt == kSInt8) opt_step_kernel<kWFp32, kSInt8><<<grid, kElemThreads, 0, s>>>(p);
+    else if (sdt == kSBf16) opt_step_kernel<kWFp32, kSBf16><<<grid, kElemThreads, 0, s>>>(p);
     else opt_step_kernel<kWFp32, kSFp32><<<grid, kElemThreads, 0, s>>>(p);
   }
   return cudaGetLastError();

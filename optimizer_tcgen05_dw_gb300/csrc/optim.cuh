@@ -139,6 +139,14 @@ __device__ __forceinline__ uint32_t bf16_sr(float x, uint32_t r16) {
 
 __device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
 
+// fp32 -> bf16 bits, round to nearest, ties to even (BF16 moments).  NaN ->
+// 0x7FC0; a value past the largest finite bf16 rounds to Inf.
+__device__ __forceinline__ uint32_t bf16_rne(float x) {
+  const uint32_t u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
+  return (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;  // no wrap: at most 0xFF800000 + 0x8000
+}
+
 // ------------------------------------------------------------------ INT8 code
 
 // Value of one code of a block with absmax `a`: code * (a / 127) or (a / 255).

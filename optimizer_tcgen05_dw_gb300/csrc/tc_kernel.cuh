@@ -688,6 +688,39 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
   }
 }
 
+// bf16 states: a chunk is 128 rows x 32 columns (m and v 8 KiB each in
+// shared memory, 64-byte rows with the 64-byte swizzle); this thread owns 8
+// columns of row r (16 bytes of each state), starting at element e0.  The
+// rule runs on the widened moments; the new ones are rounded to nearest even.
+template <int KIND>
+__device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, int r, int sub,
+                                                int64_t e0, uint4& wv, const GemmParams& p) {
+  constexpr int kOffS1 = 0, kOffS2 = 8192;
+  float g[8], w[8], s1[8], s2[8];
+  ptx::tmem_ld_32x32b_x8(taddr, g);
+  unpack_bf16x8(wv, w);
+  if (uses_s1(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub)), s1);
+  if (uses_s2(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub)), s2);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (!uses_s1(KIND)) s1[j] = 0.f;
+    if (!uses_s2(KIND)) s2[j] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+  wv = pack_sr_bf16x8(w, dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step));
+  uint32_t o1[4], o2[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    o1[j] = dev::bf16_rne(s1[2 * j]) | (dev::bf16_rne(s1[2 * j + 1]) << 16);
+    o2[j] = dev::bf16_rne(s2[2 * j]) | (dev::bf16_rne(s2[2 * j + 1]) << 16);
+  }
+  if (uses_s1(KIND))
+    *reinterpret_cast<uint4*>(buf + kOffS1 + sw64(r, sub)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+  if (uses_s2(KIND))
+    *reinterpret_cast<uint4*>(buf + kOffS2 + sw64(r, sub)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+}
+
 // INT8 states: a chunk is 128 rows x 64 columns (one code block per row;
 // codes 8 KiB per state in shared memory); this thread owns 16 columns (a
 // quarter block) of row r, its 16 bf16 weights in registers (`wv`).  The new
@@ -750,17 +783,19 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 
 // Chunk geometry of the staged FORGE epilogue for one state dtype.  A chunk
 // is 128 rows x kCC columns of the CTA's 128 x 256 half of a pair tile:
-// fp32 states 32 columns (m and v 16 KiB each in shared memory), INT8 states
-// 64 columns (one code block per row; 8 KiB of codes per state).
+// fp32 states 32 columns (m and v 16 KiB each in shared memory), bf16 states
+// 32 columns (8 KiB each), INT8 states 64 columns (one code block per row;
+// 8 KiB of codes per state).
 template <int KIND, int SDT>
 struct StagedGeom {
   static constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
   static constexpr bool I8 = (SDT == kSInt8);
+  static constexpr bool BF = (SDT == kSBf16);
   static constexpr int kCC = I8 ? 64 : 32;
   static constexpr int kChunks = kTileN / kCC;
   static constexpr int kOffS1 = 0;
-  static constexpr int kOffS2 = I8 ? 8192 : 16384;
-  static constexpr uint32_t kStateBytes = I8 ? 8192u : 16384u;
+  static constexpr int kOffS2 = (I8 || BF) ? 8192 : 16384;
+  static constexpr uint32_t kStateBytes = (I8 || BF) ? 8192u : 16384u;
   static constexpr uint32_t kTx = (U1 ? kStateBytes : 0u) + (U2 ? kStateBytes : 0u);
   static constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
   static constexpr int kNC = 32 * kNumEpiWarpsStaged;  // compute threads
@@ -1039,6 +1074,8 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
         if (G::U1) p.s1_scale[sidx] = n1;
         if (G::U2) p.s2_scale[sidx] = n2;
       }
+    } else if (G::BF) {
+      epi_chunk_bf16s<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
     } else {
       epi_chunk_fp32<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
     }

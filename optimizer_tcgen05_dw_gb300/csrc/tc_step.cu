@@ -38,14 +38,17 @@ static int step_pairs() {
   return n;
 }
 
-int step_max_pairs(int sdt) { return sdt == kSInt8 ? step_pairs<kSInt8>() : step_pairs<kSFp32>(); }
+int step_max_pairs(int sdt) {
+  return sdt == kSInt8 ? step_pairs<kSInt8>() : sdt == kSBf16 ? step_pairs<kSBf16>() : step_pairs<kSFp32>();
+}
 
 cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
                            const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p,
                            int grid, cudaStream_t s) {
-  return sdt == kSInt8 ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, p, grid, s)
-                       : run_step<kSFp32>(a, b, da, db, s1, s2, dx, p, grid, s);
+  return sdt == kSInt8   ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, p, grid, s)
+         : sdt == kSBf16 ? run_step<kSBf16>(a, b, da, db, s1, s2, dx, p, grid, s)
+                         : run_step<kSFp32>(a, b, da, db, s1, s2, dx, p, grid, s);
 }
 
 }  // namespace forge

@@ -68,26 +68,22 @@ class Problem:
         if opt.USES_S1[self.kind]:
             if s_dtype == "int8":
                 st["s1"], st["s1_scale"] = quant.quantize_blocks(m.numpy(), signed=True)
+            elif s_dtype == "bf16":
+                st["s1"] = rounding.bf16_bits_rne(m.numpy())
             else:
                 st["s1"] = m.numpy()
         if opt.USES_S2[self.kind]:
             if s_dtype == "int8":
                 st["s2"], st["s2_scale"] = quant.quantize_blocks(v.numpy(), signed=False)
+            elif s_dtype == "bf16":
+                st["s2"] = rounding.bf16_bits_rne(v.numpy())
             else:
                 st["s2"] = v.numpy()
         self.state0 = st
 
     # ---- GPU side
     def gpu_state(self):
-        st = self.state0
-        dev = "cuda"
-        W = (torch.from_numpy(st["W"].copy()) if self.w_dtype == "fp32"
-             else inputs.bits_to_bf16(st["W"])).to(dev)
-        out = {"W": W}
-        for k in ("s1", "s2", "s1_scale", "s2_scale"):
-            if st.get(k) is not None:
-                out[k] = torch.from_numpy(np.ascontiguousarray(st[k])).to(dev)
-        return out
+        return self.upload(self.state0)
 
     def run_gpu(self, fused=True, want_dx=False, state=None):
         from optimizer_tcgen05_dw_gb300 import api
@@ -120,7 +116,10 @@ class Problem:
         out = {"W": W}
         for k in ("s1", "s2", "s1_scale", "s2_scale"):
             if st.get(k) is not None:
-                out[k] = torch.from_numpy(np.ascontiguousarray(st[k])).to(dev)
+                if self.s_dtype == "bf16" and k in ("s1", "s2"):
+                    out[k] = inputs.bits_to_bf16(st[k]).to(dev)
+                else:
+                    out[k] = torch.from_numpy(np.ascontiguousarray(st[k])).to(dev)
         return out
 
     def per_step_from_common_state(self):
@@ -166,8 +165,12 @@ class Problem:
         bound = SUM_ERR * (np.abs(dY).T @ np.abs(X)) + 1e-30
         mask = np.abs(g) <= bound
         if self.kind == opt.LION and st.get("s1") is not None:
-            m = st["s1"] if self.s_dtype == "fp32" else quant.dequantize_blocks(
-                st["s1"], st["s1_scale"], True)
+            if self.s_dtype == "fp32":
+                m = st["s1"]
+            elif self.s_dtype == "bf16":
+                m = rounding.bf16_bits_to_f32(st["s1"])
+            else:
+                m = quant.dequantize_blocks(st["s1"], st["s1_scale"], True)
             b1 = np.float32(self.hp.get("beta1", 0.9))
             c = b1 * m.astype(np.float64) + (1 - b1) * g
             mask |= np.abs(c) <= bound
@@ -300,6 +303,9 @@ def oracle_interval(kind, hp, step, seed, g, st_block, w_dtype, s_dtype, n0, k0,
     if s_dtype == "int8":
         m0 = quant.dequantize_blocks(st_block["s1"], st_block["s1_scale"], True) if uses1 else None
         v0 = quant.dequantize_blocks(st_block["s2"], st_block["s2_scale"], False) if uses2 else None
+    elif s_dtype == "bf16":
+        m0 = rounding.bf16_bits_to_f32(st_block["s1"]) if uses1 else None
+        v0 = rounding.bf16_bits_to_f32(st_block["s2"]) if uses2 else None
     else:
         m0, v0 = st_block.get("s1"), st_block.get("s2")
     sc = opt.step_scalars(kind, hp, step)
@@ -348,6 +354,13 @@ def assert_in_interval(gpu_state, interval, w_dtype, s_dtype, what):
             continue
         g = gpu_np(gpu_state[key])
         lo, hi = _hull([f[key] for f in fp32])          # float32 moment, per element
+        if s_dtype == "bf16":  # nearest-even bf16 of a value in the hull: within 1 ULP of it
+            gf = rounding.bf16_bits_to_f32(g).astype(np.float64)
+            ok = (gf >= lo - _ulp_at(np.abs(lo))) & (gf <= hi + _ulp_at(np.abs(hi)))
+            bad = np.argwhere(~ok)
+            assert bad.size == 0, f"{what} {key}: {len(bad)} of {g.size} outside the interval; " \
+                f"first {bad[:3].tolist()}: gpu={gf[tuple(bad[0])]} [{lo[tuple(bad[0])]}, {hi[tuple(bad[0])]}]"
+            continue
         if s_dtype != "int8":
             gf = g.astype(np.float64)
             ok = _fp32_in(gf, lo, hi)

@@ -90,6 +90,14 @@ def test_invalid_arguments_rejected_on_host(L, case):
     assert L.forge_last_error_message().decode() != ""
 
 
+def test_bf16_moments_with_fp32_weights_unsupported_in_the_fused_step(L):
+    hp = api.hparams()
+    st = _state(wdt=api.W_FP32, sdt=api.STATE_BF16)
+    rc = L.forge_linear_bwd_step(ctypes.byref(_lin()), ctypes.byref(st), 0, ctypes.byref(hp), 1, 0, None)
+    assert rc == 2, (rc, L.forge_last_error_message())
+    assert b"bf16 moments" in L.forge_last_error_message()
+
+
 def test_other_entry_points_validate(L):
     assert L.forge_unfused_opt_step(None, None, 8, 8, 0, None, 1, 0, None) == 1
     assert L.forge_quantize_state(None, None, None, 4, 100, 1, None) == 1  # cols % 64

@@ -24,7 +24,7 @@ from _helpers import (Problem, assert_bf16_close, assert_bitexact, assert_dx_clo
 pytestmark = pytest.mark.gpu
 
 OPTS = list(opt.NAMES)
-DTYPES = [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "int8")]
+DTYPES = [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "int8"), ("bf16", "bf16")]
 RAGGED = dict(T=200, N=264, K=320)     # dX as its own launch (N % 64 != 0)
 RAGGED64 = dict(T=200, N=320, K=384)   # dX and the step in one launch
 
@@ -136,6 +136,15 @@ def test_optimizer_sweep_realistic(opt_name):
     assert_bf16_close(gpu["W"], ref["W"], "W (3 free-running steps)", exclude=sens, free_running=True)
 
 
+@pytest.mark.parametrize("opt_name", ["adamw", "nadam", "lion", "rmsprop"])
+def test_bf16_moments_realistic(opt_name):
+    """bf16 weights and bf16 moments (nearest even), realistic data, 3 steps
+    each inside the oracle's interval from a common state."""
+    prob = Problem(T=576, N=384, K=512, w_dtype="bf16", s_dtype="bf16", opt_name=opt_name,
+                   hp=inputs.SWEEP_HPARAMS[opt_name], seed=4100 + OPTS.index(opt_name), steps=3)
+    prob.per_step_from_common_state()
+
+
 def test_int8_states_realistic():
     """bf16 weights, INT8 block-64 AdamW moments pre-warmed from N(0,1e-4) and
     |N(0,1e-6)|, the Llama hyper-parameters, 3 steps."""
@@ -227,7 +236,7 @@ def test_edge_shapes(shape):
     assert_dx_close(gdx[0], to_bits(prob.dY[0]), prob.state0["W"], "dX")
 
 
-@pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
+@pytest.mark.parametrize("s_dtype", ["fp32", "int8", "bf16"])
 @pytest.mark.parametrize("opt_name", ["adamw", "lion", "sgd"])
 def test_one_launch_step_equals_two_launches(opt_name, s_dtype):
     """dX and the step in one launch compute the same bits as the dX launch

@@ -139,13 +139,16 @@ def _state(N, K, w_dtype, s_dtype, kind, seed=0):
             continue
         if s_dtype == "int8":
             st[key], st[key + "_scale"] = quant.quantize_blocks(arr, signed)
+        elif s_dtype == "bf16":
+            st[key] = rounding.bf16_bits_rne(arr)
         else:
             st[key] = arr
     return st
 
 
 @pytest.mark.parametrize("kind", range(8), ids=opt.NAMES)
-@pytest.mark.parametrize("w_dtype,s_dtype", [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "int8")])
+@pytest.mark.parametrize("w_dtype,s_dtype", [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "int8"),
+                                             ("bf16", "bf16")])
 def test_tiled_update_equals_full_gradient_update(kind, w_dtype, s_dtype):
     """§2 "Exactness": with integer-grid inputs every sum is exact, so the
     tile-by-tile step must equal the full-matrix step bit for bit."""

@@ -29,11 +29,15 @@ def _case(kind, s_dtype, seed=5, T=2048, N=128, K=128):
     if opt.USES_S1[kind]:
         if s_dtype == "int8":
             st["s1"], st["s1_scale"] = quant.quantize_blocks(m, True)
+        elif s_dtype == "bf16":
+            st["s1"] = rounding.bf16_bits_rne(m)
         else:
             st["s1"] = m
     if opt.USES_S2[kind]:
         if s_dtype == "int8":
             st["s2"], st["s2_scale"] = quant.quantize_blocks(v, False)
+        elif s_dtype == "bf16":
+            st["s2"] = rounding.bf16_bits_rne(v)
         else:
             st["s2"] = v
     g = ls.weight_gradient(X, dY)
@@ -51,7 +55,7 @@ def _case(kind, s_dtype, seed=5, T=2048, N=128, K=128):
 
 
 @pytest.mark.parametrize("kind", range(8), ids=opt.NAMES)
-@pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
+@pytest.mark.parametrize("s_dtype", ["fp32", "int8", "bf16"])
 def test_perturbed_gradient_passes(kind, s_dtype):
     iv, sim = _case(kind, s_dtype)
     assert_in_interval(sim, iv, "bf16", s_dtype, "simulated")
@@ -64,6 +68,15 @@ def test_planted_weight_error_fails():
     sim["W"] = inputs.bits_to_bf16(bits.astype(np.uint16))
     with pytest.raises(AssertionError):
         assert_in_interval(sim, iv, "bf16", "fp32", "planted")
+
+
+def test_planted_bf16_state_error_fails():
+    iv, sim = _case(opt.ADAMW, "bf16")
+    bits = sim["s2"].numpy().astype(np.int32)
+    bits[2, 9] += 3
+    with pytest.raises(AssertionError):
+        assert_in_interval(dict(sim, s2=torch.from_numpy(bits.astype(np.uint16))), iv, "bf16", "bf16",
+                           "planted bf16 v")
 
 
 def test_planted_state_errors_fail():
