@@ -56,9 +56,10 @@ __device__ __forceinline__ void load_codes8(const void* base, int64_t e0, float 
 template <bool SIGNED>
 __device__ __forceinline__ void store_codes8(void* base, int64_t e0, float a, const float (&v)[8]) {
   uint32_t w[2] = {0u, 0u};
+  const float st = dev::dvd(a, SIGNED ? 127.f : 255.f), inv = dev::dvd(1.f, st);
 #pragma unroll
   for (int j = 0; j < 8; ++j)
-    w[j >> 2] |= (static_cast<uint32_t>(dev::quant<SIGNED>(v[j], a)) & 0xFFu) << (8 * (j & 3));
+    w[j >> 2] |= (static_cast<uint32_t>(dev::quant_recip<SIGNED>(v[j], a, st, inv)) & 0xFFu) << (8 * (j & 3));
   *reinterpret_cast<uint2*>(static_cast<uint8_t*>(base) + e0) = make_uint2(w[0], w[1]);
 }
 

@@ -169,6 +169,26 @@ __device__ __forceinline__ int quant(float x, float a) {
   return static_cast<int>(q);
 }
 
+// quant<SIGNED>(x, a) with the block's step s = a/127 (or a/255) and its
+// reciprocal inv = RN(1/s) formed once per block: the same code, mostly
+// without the division.  y = RN(x * inv) = (x/s)(1 + e1)(1 + e2) with
+// |e1|, |e2| <= 2^-24, so |y - x/s| <= 2^-23 (1 + 2^-25) |x/s| < 1.6e-5 for
+// |x/s| <= 128, and RN(x/s) lies within 2^-24 * 128 < 7.7e-6 of x/s: y and
+// RN(x/s) round to the same integer unless a half-integer lies within
+// 2.4e-5 of y.  There (and whenever inv is not finite) the quotient is
+// formed exactly as in quant; elsewhere rint(y) is the code.
+template <bool SIGNED>
+__device__ __forceinline__ int quant_recip(float x, float a, float s, float inv) {
+  if (a == 0.f) return 0;
+  const float y = mul(x, inv);
+  const float fr = __fsub_rn(y, floorf(y));  // exact for |y| < 2^23
+  const float r = (fabsf(__fsub_rn(fr, 0.5f)) <= 3.0e-5f || !(fabsf(inv) <= 3.0e38f)) ? dvd(x, s) : y;
+  if (r != r) return 0;
+  float q = rintf(r);
+  q = fminf(fmaxf(q, SIGNED ? -127.f : 0.f), SIGNED ? 127.f : 255.f);
+  return static_cast<int>(q);
+}
+
 // Running absmax that never takes a NaN (NaN > a is false).
 __device__ __forceinline__ float absmax_acc(float a, float x) {
   const float ax = fabsf(x);

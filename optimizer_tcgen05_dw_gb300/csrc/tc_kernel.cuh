@@ -768,10 +768,14 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
     n2 = fmaxf(n2, amax[(1 * 4 + o) * 128 + r]);
   }
   uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
+  const float st1 = dev::dvd(n1, 127.f), st2 = dev::dvd(n2, 255.f);  // code steps
+  const float iv1 = dev::dvd(1.f, st1), iv2 = dev::dvd(1.f, st2);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    if (uses_s1(KIND)) o1[j >> 2] |= (static_cast<uint32_t>(dev::quant<true>(m[j], n1)) & 0xFFu) << (8 * (j & 3));
-    if (uses_s2(KIND)) o2[j >> 2] |= (static_cast<uint32_t>(dev::quant<false>(v[j], n2)) & 0xFFu) << (8 * (j & 3));
+    if (uses_s1(KIND))
+      o1[j >> 2] |= (static_cast<uint32_t>(dev::quant_recip<true>(m[j], n1, st1, iv1)) & 0xFFu) << (8 * (j & 3));
+    if (uses_s2(KIND))
+      o2[j >> 2] |= (static_cast<uint32_t>(dev::quant_recip<false>(v[j], n2, st2, iv2)) & 0xFFu) << (8 * (j & 3));
   }
   if (uses_s1(KIND))
     *reinterpret_cast<uint4*>(buf + kOffS1 + sw64(r, sub)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
