@@ -1,4 +1,5 @@
-// The tensor-core kernel behind the fused step, the unfused wgrad pass and dX.
+// The tensor-core kernel behind the fused step (alone, or in one launch with
+// dX), the unfused wgrad pass and dX.
 //
 // FORGE (gist.science explainer), Technical Summary §2 "Core Mechanism": for
 // each tile of W the partial products of dY and X are accumulated in FP32,
@@ -18,11 +19,16 @@
 //               so the MMAs of tile i+1 overlap the epilogue of tile i, and
 //               multicasts its commits to both CTAs' "empty" / "tmem full"
 //               barriers;
-//   warps 2..9  the epilogue of each CTA: tcgen05.ld pulls its 128 rows of
+//   warps 2..   the epilogue of each CTA: tcgen05.ld pulls its 128 rows of
 //               the finished fp32 tile into registers (one TMEM lane = one
 //               output row), then runs the optimizer on it (FORGE), or stores
-//               it as fp32 (unfused pass 1) or bf16 (dX); the eight warps of
-//               both CTAs release the accumulator on the leader's barrier.
+//               it as fp32 (unfused pass 1) or bf16 (dX); the epilogue warps
+//               of both CTAs release the accumulator on the leader's barrier.
+//               Plain modes and fp32 weights: warps 2..9 (direct stores).
+//               The FORGE step with bf16 weights: warps 2..17 compute, warp
+//               18 stages the optimizer states through shared memory with
+//               TMA (and, in the one-launch step, stores the dX tiles that
+//               run first in the same launch).
 // Operand layouts (all 128-byte swizzled atoms of 8 rows x 128 bytes):
 //   wgrad  A = dY^T tile [128 n x BK t] per CTA: dY is [T x N] with n
 //          contiguous, so A is MN-major: two 64-wide column atoms BK*128
