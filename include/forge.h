@@ -162,6 +162,39 @@ FORGE_API forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin,
                                                       const forge_hparams_t* hp, int64_t step,
                                                       uint64_t seed, void* stream);
 
+/* The weight-gradient operands of one linear layer in FP8 (E4M3: 1 sign,
+ * 4 exponent bits with bias 7, 3 mantissa bits; no infinity; the two codes
+ * 0x7F / 0xFF are NaN; largest finite 448), one float scale per tensor:
+ * X = decode(Xt)^T * x_scale, dY = decode(dYt)^T * dy_scale.  Both are stored
+ * token-contiguous (transposed), T % 16 == 0 so that rows are 16-byte
+ * multiples. */
+typedef struct forge_linear_fp8 {
+  int64_t T, N, K;     /* tokens, out-features, in-features                    */
+  const void* Xt;      /* E4M3 codes [K x T] (the input activation, transposed) */
+  const void* dYt;     /* E4M3 codes [N x T] (the upstream gradient, transposed) */
+  float x_scale;       /* dequantisation scale of Xt                           */
+  float dy_scale;      /* dequantisation scale of dYt                          */
+} forge_linear_fp8_t;
+
+/* The FORGE step (step 2 of forge_linear_bwd_step) from FP8 operands
+ * (Technical Summary §4 "Composability": FORGE composes with FP8
+ * quantisation; the pages give no format or scale recipe, so this is one
+ * plain reading).  For every W tile, S = sum over tokens of the products of
+ * the decoded codes is accumulated in FP32 in tensor memory (tcgen05 E4M3 x
+ * E4M3 -> FP32), the gradient is g = S * c with c = x_scale * dy_scale
+ * formed in double and rounded once to float, and the rule `opt_kind` is
+ * applied exactly as in forge_linear_bwd_step.  BF16 weights (stochastic
+ * rounding) only: FP32 weights return FORGE_ERR_UNSUPPORTED.  States: FP32,
+ * INT8 blocks of 64 or BF16.  No dX is computed: call forge_linear_dgrad
+ * first on the same stream (it reads the weights before this call updates
+ * them).  T == 0 applies the rule to a zero gradient.  Requirements as in
+ * the shared conventions plus T % 16 == 0 and finite scales; NaN codes
+ * propagate into the updated weights.  Nothing is allocated. */
+FORGE_API forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin,
+                                                   const forge_state_t* state, int32_t opt_kind,
+                                                   const forge_hparams_t* hp, int64_t step,
+                                                   uint64_t seed, void* stream);
+
 /* Whether forge_linear_bwd_step may run dX and the FORGE step in one launch
  * (non-zero, the default) or always uses two launches (0).  Process-wide. */
 FORGE_API void forge_set_step_fusion(int32_t enable);

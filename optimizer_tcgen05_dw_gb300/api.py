@@ -34,6 +34,11 @@ class ForgeLinear(ctypes.Structure):
                 ("X", c_void_p), ("dY", c_void_p), ("dX", c_void_p)]
 
 
+class ForgeLinearFp8(ctypes.Structure):
+    _fields_ = [("T", c_int64), ("N", c_int64), ("K", c_int64),
+                ("Xt", c_void_p), ("dYt", c_void_p), ("x_scale", c_float), ("dy_scale", c_float)]
+
+
 class ForgeState(ctypes.Structure):
     _fields_ = [("W", c_void_p), ("w_dtype", c_int32), ("s_dtype", c_int32),
                 ("s1", c_void_p), ("s2", c_void_p), ("s1_scale", c_void_p), ("s2_scale", c_void_p)]
@@ -64,6 +69,9 @@ _SIGNATURES = {
     "forge_linear_bwd_step_static": (c_int32, [ctypes.POINTER(ForgeLinear), ctypes.POINTER(ForgeState),
                                                c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
                                                c_void_p]),
+    "forge_linear_bwd_step_fp8": (c_int32, [ctypes.POINTER(ForgeLinearFp8), ctypes.POINTER(ForgeState),
+                                            c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
+                                            c_void_p]),
     "forge_linear_dgrad": (c_int32, [ctypes.POINTER(ForgeLinear), c_void_p, c_int32, c_void_p]),
     "forge_unfused_wgrad": (c_int32, [ctypes.POINTER(ForgeLinear), c_void_p, c_void_p]),
     "forge_unfused_opt_step": (c_int32, [c_void_p, ctypes.POINTER(ForgeState), c_int64, c_int64,
@@ -209,6 +217,23 @@ def forge_linear_bwd_step_static(X, dY, W, opt: str, hp: dict, step: int, seed: 
     _check(lib().forge_linear_bwd_step_static(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
                                               ctypes.byref(hparams(**hp)), int(step),
                                               int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def forge_linear_bwd_step_fp8(Xt, dYt, x_scale: float, dy_scale: float, W, opt: str, hp: dict,
+                              step: int, seed: int, s1=None, s2=None, s1_scale=None, s2_scale=None,
+                              stream=None):
+    """The FORGE step from E4M3 operands: Xt [K, T] and dYt [N, T] codes
+    (torch.float8_e4m3fn or uint8), token-contiguous, with one scale each;
+    updates the bf16 W and the states in place (no dX)."""
+    K, T = Xt.shape
+    N = W.shape[0]
+    for t, name, shape in ((Xt, "Xt", (K, T)), (dYt, "dYt", (N, T))):
+        _need(t, name, t.dtype if t.dtype in (torch.uint8, torch.float8_e4m3fn) else torch.uint8, shape)
+    st = make_state(W, s1, s2, s1_scale, s2_scale)
+    lin = ForgeLinearFp8(T, N, K, _ptr(Xt), _ptr(dYt), float(x_scale), float(dy_scale))
+    _check(lib().forge_linear_bwd_step_fp8(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
+                                           ctypes.byref(hparams(**hp)), int(step),
+                                           int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
 def forge_linear_dgrad(dY, W, dX, stream=None):

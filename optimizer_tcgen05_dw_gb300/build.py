@@ -26,7 +26,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I" + CSRC, "-I" + INCLUDE]
 
 LIBS = {
-    "libforge.so": ["api.cu", "tc_fused.cu", "tc_step.cu", "tc_plain.cu", "elementwise.cu"],
+    "libforge.so": ["api.cu", "tc_fused.cu", "tc_step.cu", "tc_fp8.cu", "tc_plain.cu", "elementwise.cu"],
     "libforge_testkit.so": ["testkit.cu"],
 }
 HEADERS = ["common.h", "launch.h", "optim.cuh", "ptx.cuh", "tc_kernel.cuh"]

@@ -587,6 +587,77 @@ forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const for
                      static_cast<cudaStream_t>(stream), d, d.static_scratch);
 }
 
+forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const forge_state_t* state,
+                                         int32_t opt_kind, const forge_hparams_t* hp, int64_t step,
+                                         uint64_t seed, void* stream) {
+  g_msg[0] = '\0';
+  forge_status_t st;
+  if (lin == nullptr) return fail(FORGE_ERR_INVALID_ARG, "lin is NULL");
+  const int64_t T = lin->T, N = lin->N, K = lin->K;
+  if (T < 0 || N < 0 || K < 0)
+    return fail(FORGE_ERR_INVALID_ARG, "negative shape T=%lld N=%lld K=%lld", (long long)T, (long long)N,
+                (long long)K);
+  if (N % 8 != 0 || K % 8 != 0)
+    return fail(FORGE_ERR_INVALID_ARG, "N and K must be multiples of 8 (N=%lld K=%lld)", (long long)N,
+                (long long)K);
+  if (T % 16 != 0) return fail(FORGE_ERR_INVALID_ARG, "FP8 operands need T %% 16 == 0 (T=%lld)", (long long)T);
+  if (T > (int64_t{1} << 31) - 1 || N > (int64_t{1} << 31) - 1 || K > (int64_t{1} << 31) - 1)
+    return fail(FORGE_ERR_UNSUPPORTED, "dimensions must fit in 31 bits");
+  if (T > 0 && N > 0 && K > 0) {
+    if (lin->Xt == nullptr || !aligned16(lin->Xt)) return fail(FORGE_ERR_INVALID_ARG, "Xt must be 16-byte aligned");
+    if (lin->dYt == nullptr || !aligned16(lin->dYt)) return fail(FORGE_ERR_INVALID_ARG, "dYt must be 16-byte aligned");
+  }
+  const double c = static_cast<double>(lin->x_scale) * static_cast<double>(lin->dy_scale);
+  if (!std::isfinite(lin->x_scale) || !std::isfinite(lin->dy_scale) || !std::isfinite(static_cast<float>(c)))
+    return fail(FORGE_ERR_INVALID_ARG, "FP8 scales and their product must be finite floats");
+  if ((st = check_hp(opt_kind, hp, step)) != FORGE_OK) return st;
+  if ((st = check_state(state, opt_kind, N, K)) != FORGE_OK) return st;
+  if (state->w_dtype != FORGE_W_BF16_SR)
+    return fail(FORGE_ERR_UNSUPPORTED, "the FP8 step stages bf16 weights (w_dtype must be FORGE_W_BF16_SR)");
+  if (N == 0 || K == 0) return FORGE_OK;
+  DeviceInfo d;
+  if ((st = device_info(&d)) != FORGE_OK) return st;
+  if ((st = check_device(d)) != FORGE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const OptScalars sc = make_scalars(opt_kind, *hp, step);
+  cudaError_t e;
+  if (T == 0) {  // no tokens: the rule on a zero gradient
+    ElemParams ep;
+    std::memset(&ep, 0, sizeof(ep));
+    ep.W = state->W; ep.s1 = state->s1; ep.s2 = state->s2;
+    ep.s1_scale = state->s1_scale; ep.s2_scale = state->s2_scale;
+    ep.N = N; ep.K = K; ep.sc = sc; ep.seed = seed; ep.step = static_cast<uint64_t>(step);
+    if ((e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, s)) != cudaSuccess)
+      return cuda_fail(e, "optimizer launch (T = 0)");
+    return FORGE_OK;
+  }
+  // A = dY^T [N x T] and B = X^T [K x T], token-contiguous: K-major operands,
+  // 128 tokens (bytes) by 128 rows per box.
+  CUtensorMap ma, mb, m1, m2;
+  if ((st = tensor_map(&ma, lin->dYt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, T, N, kFp8BlockK, kTileM,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FORGE_OK)
+    return st;
+  if ((st = tensor_map(&mb, lin->Xt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, T, K, kFp8BlockK, kTileN / 2,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FORGE_OK)
+    return st;
+  if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  fill_tiles(p, N, K, T, kFp8BlockK);
+  p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
+  p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
+  p.sc = sc;
+  p.seed = seed;
+  p.step = static_cast<uint64_t>(step);
+  p.status = d.status;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.skip_loads = g_skip_loads.load();
+  p.gscale = static_cast<float>(c);
+  if ((e = launch_tc_fp8(state->s_dtype, ma, mb, m1, m2, p, grid_for(p, d), s)) != cudaSuccess)
+    return cuda_fail(e, "FP8 step launch");
+  return FORGE_OK;
+}
+
 void forge_set_step_fusion(int32_t enable) { g_step_fusion.store(enable != 0 ? 1 : 0); }
 
 forge_status_t forge_linear_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype, void* stream) {

@@ -66,6 +66,7 @@ constexpr int kStages = 6;
 #endif
 constexpr int kFusedBlockK = FORGE_FUSED_BK;
 constexpr int kWgradBlockK = FORGE_WGRAD_BK;      // unfused weight-gradient pass
+constexpr int kFp8BlockK = 128;                   // tokens per stage with E4M3 operands (128-byte rows)
 constexpr int kWgradStages = FORGE_WGRAD_STAGES;
 constexpr int kFusedStages = FORGE_FUSED_STAGES;
 constexpr int kNumEpiWarps = 8;                          // epilogue warps, plain epilogues
@@ -76,7 +77,8 @@ enum GemmMode : int32_t {
   kModeFusedOpt = 0,   // dW tile -> optimizer epilogue (the FORGE step)
   kModeWgradStore = 1, // dW tile -> fp32 store (unfused pass 1)
   kModeDgrad = 2,      // dX tile -> bf16 store
-  kModeStep = 3        // one launch: the dX tiles, then the dW tiles -> optimizer epilogue
+  kModeStep = 3,       // one launch: the dX tiles, then the dW tiles -> optimizer epilogue
+  kModeFusedFp8 = 4    // the FORGE step from E4M3 operands (token-contiguous, scaled)
 };
 
 // Column blocks (of kTileN) whose dX-completion counters the one-launch step
@@ -118,6 +120,9 @@ struct GemmParams {
   // pairs from dx_heavy on, those without an extra dW tile.
   int32_t dx_rounds;
   int32_t dx_heavy;
+  // kModeFusedFp8: the accumulated sum of code products times gscale
+  // (= x_scale * dy_scale) is the gradient.
+  float gscale;
 };
 
 }  // namespace forge

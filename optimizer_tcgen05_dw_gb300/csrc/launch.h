@@ -41,6 +41,11 @@ cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
 // wait for dX tiles of other pairs, so its grid must not exceed this); 0 if
 // the query fails.
 int step_max_pairs(int sdt);
+// tc_fp8.cu: the FORGE step from E4M3 operands (mode kModeFusedFp8, bf16
+// weights): a = dY^T codes [N x T], b = X^T codes [K x T], 128 x 128-byte
+// boxes with the 128-byte swizzle; p.gscale the product of the scales.
+cudaError_t launch_tc_fp8(int sdt, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& s1,
+                          const CUtensorMap& s2, const GemmParams& p, int grid, cudaStream_t s);
 // tc_plain.cu: unfused pass 1 (kModeWgradStore) or dX (kModeDgrad).
 cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t s);

@@ -72,13 +72,17 @@ constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 
 template <int MODE, int WDT>
 struct KCfg {
-  static constexpr bool kTmaEpi = ((MODE == kModeFusedOpt || MODE == kModeStep) && WDT == kWBf16);
+  static constexpr bool kFp8 = (MODE == kModeFusedFp8);
+  static constexpr bool kTmaEpi =
+      ((MODE == kModeFusedOpt || MODE == kModeStep || kFp8) && WDT == kWBf16);
   static constexpr int kBK =
-      kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK);  // tokens per stage
+      kFp8 ? kFp8BlockK
+           : (kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK));  // tokens per stage
   static constexpr int kStg =
       kTmaEpi ? kFusedStages : (MODE == kModeWgradStore ? kWgradStages : kStages);
-  static constexpr int kA = kTileM * kBK * 2;       // bytes of A per stage (this CTA's 128 rows)
-  static constexpr int kB = (kTileN / 2) * kBK * 2; // bytes of B per stage (this CTA's 128 columns)
+  static constexpr int kEsz = kFp8 ? 1 : 2;           // operand element bytes
+  static constexpr int kA = kTileM * kBK * kEsz;       // bytes of A per stage (this CTA's 128 rows)
+  static constexpr int kB = (kTileN / 2) * kBK * kEsz; // bytes of B per stage (this CTA's 128 columns)
   static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBufBytes : 0;
   static constexpr int kSmem = kStg * (kA + kB) + kEpiBytes + 512 + 1024;
   // TMA warp, MMA warp, epilogue warps (four per 32-lane quarter of TMEM in the
@@ -92,6 +96,7 @@ static_assert(KCfg<kModeFusedOpt, kWBf16>::kStg <= 8 && KCfg<kModeWgradStore, kW
 static_assert(KCfg<kModeWgradStore, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeFusedOpt, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeDgrad, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeFusedFp8, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -161,7 +166,8 @@ template <int MODE, int STG, int BK>
 __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, const CUtensorMap* mDA,
                               const CUtensorMap* mDB, const GemmParams& p, uint8_t* smA,
                               uint8_t* smB, SharedState* ss, uint32_t rank) {
-  constexpr int kA = kTileM * BK * 2, kB = (kTileN / 2) * BK * 2;
+  constexpr int kEsz = MODE == kModeFusedFp8 ? 1 : 2;
+  constexpr int kA = kTileM * BK * kEsz, kB = (kTileN / 2) * BK * kEsz;
   uint32_t it = 0;
   uint32_t issued_mask = 0;
   uint32_t last_parity = 0;  // bit s: parity of the last phase armed on full[s]
@@ -200,6 +206,13 @@ __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, cons
         if (rank == 0) ptx::mbar_arrive_expect_tx(&ss->full[s], 2u * (kA + kB));
         uint8_t* a = smA + s * kA;
         uint8_t* b = smB + s * kB;
+        if (MODE == kModeFusedFp8) {  // dY^T and X^T, token-contiguous: one 128 x 128-byte box each
+          ptx::tma_load_2d_pair(mA, bar, a, kb * BK, m0);
+          ptx::tma_load_2d_pair(mB, bar, b, kb * BK, n0);
+          issued_mask |= 1u << s;
+          last_parity = (last_parity & ~(1u << s)) | (ph << s);
+          continue;
+        }
         if (MODE == kModeDgrad) {
           ptx::tma_load_2d_pair(mA, bar, a, kb * BK, m0);
         } else if (p.op3d) {  // [2 column blocks][BK rows][64 columns] in one copy
@@ -232,7 +245,8 @@ drain:
 // Leader CTA only.
 template <int MODE, int STG, int BK>
 __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, SharedState* ss) {
-  constexpr int kA = kTileM * BK * 2, kB = (kTileN / 2) * BK * 2;
+  constexpr bool kFp8 = MODE == kModeFusedFp8;
+  constexpr int kA = kTileM * BK * (kFp8 ? 1 : 2), kB = (kTileN / 2) * BK * (kFp8 ? 1 : 2);
   uint32_t it = 0;
   int local = 0;
   // One tile into accumulator local & 1: num_kb stages; A K-major (dX: dY) or
@@ -242,8 +256,9 @@ __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, Shared
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
     if (!bounded_wait(&ss->tmem_empty[acc], aph ^ 1u, p, ss)) return false;
     ptx::tc_fence_after();
-    const uint32_t idesc = a_kmajor ? ptx::idesc_bf16_f32(kPairM, kTileN, false, true)
-                                    : ptx::idesc_bf16_f32(kPairM, kTileN, true, true);
+    const uint32_t idesc = kFp8       ? ptx::idesc_e4m3_f32(kPairM, kTileN)
+                           : a_kmajor ? ptx::idesc_bf16_f32(kPairM, kTileN, false, true)
+                                      : ptx::idesc_bf16_f32(kPairM, kTileN, true, true);
     const uint32_t d_tmem = ss->tmem_base + static_cast<uint32_t>(acc * kTileN);
     for (int kb = 0; kb < num_kb; ++kb, ++it) {
       const int s = static_cast<int>(it % STG);
@@ -252,6 +267,17 @@ __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, Shared
       ptx::tc_fence_after();
       const uint32_t a0 = ptx::smem_addr(smA + s * kA);
       const uint32_t b0 = ptx::smem_addr(smB + s * kB);
+      if constexpr (kFp8) {
+        // Both operands K-major: 32 E4M3 = 32 B of each 128-byte swizzle row
+        // per instruction, 8-row groups 1 KiB apart.
+#pragma unroll
+        for (int kk = 0; kk < BK / 32; ++kk)
+          ptx::mma_e4m3_pair(d_tmem, ptx::smem_desc_sw128(a0 + kk * 32, 16, 1024),
+                             ptx::smem_desc_sw128(b0 + kk * 32, 16, 1024), idesc,
+                             (kb | kk) != 0 ? 1u : 0u);
+        ptx::mma_commit_pair_multicast(&ss->empty[s], 0x3);
+        continue;
+      }
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
         // MN-major: 16 reduction rows = two 8-row groups of 128 B -> +2 KiB;
@@ -654,16 +680,24 @@ __device__ __forceinline__ uint4 pack_sr_bf16x8(const float* w, uint4 rnd) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// FP8 operands: the accumulated sum of E4M3 code products times the product
+// of the two per-tensor scales is the gradient.
+__device__ __forceinline__ void scale_grad(float (&g)[8], const GemmParams& p) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) g[j] = __fmul_rn(g[j], p.gscale);
+}
+
 // fp32 states: a chunk is 128 rows x 32 columns (m and v 16 KiB each in
 // shared memory); this thread owns 8 columns of row r (two 16-byte chunks of
 // each state), starting at element e0.  Its 8 bf16 weights come in and go out
 // in registers (`wv`).
-template <int KIND>
+template <int KIND, bool SCALE>
 __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int r, int sub,
                                                int64_t e0, uint4& wv, const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 16384;
   float g[8], w[8], s1[8], s2[8];
   ptx::tmem_ld_32x32b_x8(taddr, g);
+  if (SCALE) scale_grad(g, p);
   unpack_bf16x8(wv, w);
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -698,12 +732,13 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
 // shared memory, 64-byte rows with the 64-byte swizzle); this thread owns 8
 // columns of row r (16 bytes of each state), starting at element e0.  The
 // rule runs on the widened moments; the new ones are rounded to nearest even.
-template <int KIND>
+template <int KIND, bool SCALE>
 __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, int r, int sub,
                                                 int64_t e0, uint4& wv, const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 8192;
   float g[8], w[8], s1[8], s2[8];
   ptx::tmem_ld_32x32b_x8(taddr, g);
+  if (SCALE) scale_grad(g, p);
   unpack_bf16x8(wv, w);
   if (uses_s1(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub)), s1);
   if (uses_s2(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub)), s2);
@@ -733,7 +768,7 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
 // block absmax combines the four quarters through shared memory; the weights
 // use the new float32 moments, then the moments are quantised with the new
 // absmax.
-template <int KIND>
+template <int KIND, bool SCALE>
 __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int r, int sub,
                                                int64_t e0, uint4 (&wv)[2], float a1, float a2,
                                                float* n1_out, float* n2_out, int nthreads,
@@ -750,6 +785,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   for (int h = 0; h < 2; ++h) {  // two halves of 8 columns: gradient and weights
     float g[8], w[8];
     ptx::tmem_ld_32x32b_x8(taddr + 8 * h, g);
+    if (SCALE) scale_grad(g, p);
     unpack_bf16x8(wv[h], w);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -898,11 +934,12 @@ __device__ __forceinline__ void epi_dx_stage(uint32_t taddr, uint8_t* box, int r
 // MMAs, and so its reads of the weights, are complete); before a dW tile's
 // first chunk it waits until all dX tiles of the tile's column block are
 // counted, so no weight is written while a dX tile may still read it.
-template <int KIND, int SDT, bool STEP>
+template <int KIND, int SDT, int MODE>
 __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                  const CUtensorMap* mDX, const GemmParams& p, SharedState* ss,
                                  uint8_t* epi, int lane, uint32_t rank) {
   using G = StagedGeom<KIND, SDT>;
+  constexpr bool STEP = MODE == kModeStep;
   TileWalk<G::kChunks> walk;
   walk.init(p, rank);
   const int total = walk.my_tiles * G::kChunks;
@@ -997,10 +1034,11 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
 // lanes 32*(w%4).. (its rows) and a quarter of each chunk's columns; its bf16
 // weights (and old INT8 scales) come straight from global memory one chunk
 // ahead, its states from the staged chunk in shared memory.
-template <int KIND, int SDT, bool STEP>
+template <int KIND, int SDT, int MODE>
 __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint8_t* epi,
                                       int warp, int lane, uint32_t rank) {
   using G = StagedGeom<KIND, SDT>;
+  constexpr bool STEP = MODE == kModeStep, SCALE = MODE == kModeFusedFp8;
   constexpr int kCC = G::kCC, kChunks = G::kChunks, kWPerThread = G::kWPerThread;
   const int quarter = warp & 3, sub = (warp - 2) >> 2;  // TMEM lane quarter, column quarter
   const int r = quarter * 32 + lane;
@@ -1077,7 +1115,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     const int64_t e0 = row * K + col;
     if (G::I8) {
       float n1, n2;
-      epi_chunk_int8<KIND>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
+      epi_chunk_int8<KIND, SCALE>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
                            &n1, &n2, G::kNC, p);
       if (sub == 0 && row < p.M && col0 < K) {
         const int64_t sidx = row * (K / 64) + col0 / 64;
@@ -1085,9 +1123,9 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
         if (G::U2) p.s2_scale[sidx] = n2;
       }
     } else if (G::BF) {
-      epi_chunk_bf16s<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
+      epi_chunk_bf16s<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     } else {
-      epi_chunk_fp32<KIND>(taddr, buf, r, sub, e0, wcur[0], p);
+      epi_chunk_fp32<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     }
     if (row < p.M && col < K) {
       uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
@@ -1101,31 +1139,31 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   }
 }
 
-template <int KIND, int SDT, bool STEP>
+template <int KIND, int SDT, int MODE>
 __device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                                 const CUtensorMap* mDX, const GemmParams& p,
                                                 SharedState* ss, uint8_t* epi, int warp, int lane,
                                                 uint32_t rank) {
   if (warp == 2 + kNumEpiWarpsStaged)
-    epilogue_io_role<KIND, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, lane, rank);
+    epilogue_io_role<KIND, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, lane, rank);
   else
-    epilogue_compute_role<KIND, SDT, STEP>(p, ss, epi, warp, lane, rank);
+    epilogue_compute_role<KIND, SDT, MODE>(p, ss, epi, warp, lane, rank);
 }
 
-template <int SDT, bool STEP>
+template <int SDT, int MODE>
 __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                                       const CUtensorMap* mDX, const GemmParams& p,
                                                       SharedState* ss, uint8_t* epi, int warp,
                                                       int lane, uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_staged<kAdamW, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kNAdam: epilogue_staged<kNAdam, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kRAdam: epilogue_staged<kRAdam, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kLion: epilogue_staged<kLion, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kRMSprop: epilogue_staged<kRMSprop, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kSGD: epilogue_staged<kSGD, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    default: epilogue_staged<kSGDMomentum, SDT, STEP>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kAdamW: epilogue_staged<kAdamW, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_staged<kNAdam, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_staged<kRAdam, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_staged<kLion, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_staged<kRMSprop, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_staged<kSGD, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_staged<kSGDMomentum, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
   }
 }
 
@@ -1189,7 +1227,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT, MODE == kModeStep>(&mapS1, &mapS2, &mapDX, p, ss, epi, warp, lane, rank);
+      epilogue_tma_dispatch<SDT, MODE>(&mapS1, &mapS2, &mapDX, p, ss, epi, warp, lane, rank);
     else
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }

@@ -122,6 +122,23 @@ def integer_grid(shape, lo: int, hi: int, pow2_scale: int, seed: int,
     return (t.to(torch.float32) * (2.0 ** pow2_scale)).to(dtype)
 
 
+def e4m3_integer_grid(shape, lo: int, hi: int, seed: int, device="cpu") -> torch.Tensor:
+    """E4M3 codes (uint8) of integers uniform in [lo, hi] (exact for |x| <= 16)."""
+    t = torch.randint(lo, hi + 1, tuple(shape), generator=_gen(seed, device), device=device,
+                      dtype=torch.int32)
+    return t.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def e4m3_normal(shape, std: float, seed: int, device="cpu"):
+    """N(0, std) drawn in float32, divided by a power-of-two per-tensor scale
+    that brings the largest magnitude to at most 448 (the largest finite E4M3
+    value), and cast to E4M3 (nearest even).  Returns (codes as uint8, scale)."""
+    t = torch.randn(*shape, generator=_gen(seed, device), device=device, dtype=torch.float32) * std
+    amax = float(t.abs().max()) if t.numel() else 0.0
+    scale = 2.0 ** int(np.ceil(np.log2(amax / 448.0))) if amax > 0 else 1.0
+    return (t / scale).to(torch.float8_e4m3fn).view(torch.uint8), scale
+
+
 def bf16_to_bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (on the CPU)."""
     assert t.dtype == torch.bfloat16

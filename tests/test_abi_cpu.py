@@ -120,3 +120,46 @@ def test_valid_call_without_a_gpu_reports_cuda_error(L):
     rc = L.forge_linear_bwd_step(ctypes.byref(_lin()), ctypes.byref(_state()), 0,
                                  ctypes.byref(hp), 1, 0, None)
     assert rc == 3
+
+
+def _lin8(T=128, N=256, K=256, x=16, dy=32, sx=1.0, sdy=1.0):
+    return api.ForgeLinearFp8(T, N, K, ctypes.c_void_p(x), ctypes.c_void_p(dy), sx, sdy)
+
+
+@pytest.mark.parametrize("case,rc", [
+    ("null_lin", 1), ("t_not_mult16", 1), ("k_not_mult8", 1), ("misaligned_xt", 1), ("null_dyt", 1),
+    ("nan_scale", 1), ("scale_product_overflows", 1), ("bad_kind", 1), ("fp32_weights", 2),
+    ("negative_t", 1)])
+def test_fp8_step_arguments_checked_on_host(L, case, rc):
+    hp = api.hparams()
+    lin, st, kind = _lin8(), _state(), 0
+    if case == "null_lin":
+        lin = None
+    elif case == "t_not_mult16":
+        lin = _lin8(T=120)
+    elif case == "k_not_mult8":
+        lin = _lin8(K=100)
+    elif case == "misaligned_xt":
+        lin = _lin8(x=24)
+    elif case == "null_dyt":
+        lin = api.ForgeLinearFp8(128, 256, 256, ctypes.c_void_p(16), None, 1.0, 1.0)
+    elif case == "nan_scale":
+        lin = _lin8(sx=float("nan"))
+    elif case == "scale_product_overflows":
+        lin = _lin8(sx=1e30, sdy=1e30)
+    elif case == "bad_kind":
+        kind = 11
+    elif case == "fp32_weights":
+        st = _state(wdt=api.W_FP32)
+    elif case == "negative_t":
+        lin = _lin8(T=-16)
+    got = L.forge_linear_bwd_step_fp8(None if lin is None else ctypes.byref(lin), ctypes.byref(st),
+                                      kind, ctypes.byref(hp), 1, 0, None)
+    assert got == rc, (case, got, L.forge_last_error_message())
+    assert L.forge_last_error_message().decode() != ""
+
+
+def test_fp8_step_empty_problem_is_a_no_op(L):
+    hp = api.hparams()
+    assert L.forge_linear_bwd_step_fp8(ctypes.byref(_lin8(N=0)), ctypes.byref(_state()), 0,
+                                       ctypes.byref(hp), 1, 0, None) == 0
