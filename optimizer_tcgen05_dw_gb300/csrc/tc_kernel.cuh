@@ -15,7 +15,8 @@
 //               complete on the leader CTA's "full" mbarrier;
 //   warp 1      allocates 512 tensor-memory columns (collectively with the
 //               peer); in the leader one lane issues tcgen05.mma (M=256,
-//               N=256, K=16, bf16 -> fp32) into one of two TMEM accumulators,
+//               N=256, K=16, bf16 -> fp32; K=32 for E4M3) into one of two
+//               TMEM accumulators,
 //               so the MMAs of tile i+1 overlap the epilogue of tile i, and
 //               multicasts its commits to both CTAs' "empty" / "tmem full"
 //               barriers;
@@ -36,6 +37,11 @@
 //          B = X tile [128 k x BK t] per CTA, MN-major, two atoms.
 //   dgrad  A = dY tile [128 t x 64 n], K-major (n contiguous); B = W tile
 //          [128 k x 64 n] per CTA, MN-major.
+//   FP8    the FORGE step from E4M3 codes stored token-contiguous: A = dY^T
+//          tile [128 n x 128 t], B = X^T tile [128 k x 128 t] per CTA, both
+//          K-major (one 128-byte row per output row and stage); tcgen05
+//          kind::f8f6f4, K = 32 per instruction; the epilogue multiplies the
+//          FP32 sum by the product of the two per-tensor scales.
 // Every wait is bounded (GemmParams::wait_limit_ns): on expiry the CTA records
 // a timeout in the status word, all roles stop, in-flight copies and MMAs are
 // drained (again bounded), tensor memory is released and the CTA returns.
