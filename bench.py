@@ -22,7 +22,10 @@ and dY (token-contiguous, one power-of-two scale per tensor; dX stays a bf16
 launch) against the bf16 peak times the nominal FP8/BF16 tensor-rate ratio 2.
 
 ``--impl reference`` times the CPU oracle on a bounded sample of the same
-workload instead (no GPU work).
+workload instead (no GPU work).  ``--workload KEY`` prints one line for another
+measured configuration instead of the headline one (marked ``"secondary"``):
+the fp32-master 256x256 layer, the Llama set with INT8 moments, the 4096x4096
+optimizer sweep, or the 40-layer Qwen3-14B sweep at T = 4096.
 """
 
 import argparse
@@ -530,6 +533,8 @@ def run_ours(args):
                 "frac": round(fp8_tflops / (2 * peak_sust), 4),
                 "fused_per_layer_tflops": fp8_per_layer},
         "hbm_bytes_per_param_algorithmic": round(bytes_step / params, 3),
+        "hbm_bytes_per_param_measured": (None if _profiled_traffic() is None else
+                                         round(_profiled_traffic() * len(layers) / params, 3)),
         "gpu_launches": len(layers) * args.steps,
         "clocks": ck,
     }
@@ -545,6 +550,165 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ----------------------------------------------------------------------------
+# Secondary workloads (`--workload`): the other measured configurations
+# ----------------------------------------------------------------------------
+
+SECONDARY = ("single_256", "llama8b_bf16_int8state", "sweep_4096", "qwen14b_int8")
+QWEN_ACT = {"q_proj": "x_attn", "k_proj": "x_attn", "v_proj": "x_attn", "o_proj": "x_o",
+            "gate_proj": "x_mlp", "up_proj": "x_mlp", "down_proj": "x_down"}
+
+
+class _SLayer:
+    """One linear of a secondary workload: bf16 or fp32 W, fp32 or INT8 AdamW-
+    style states (INT8 codes made by the library's own quantiser), its dY and dX."""
+
+    def __init__(self, api, name, N, K, T, dev, seed, w, want_dx=True):
+        self.name, self.N, self.K, self.T, self.seed = name, N, K, T, seed
+        wdt = torch.float32 if w.w_dtype == "fp32" else torch.bfloat16
+        self.W = inputs.normal((N, K), w.w_std, seed, wdt, dev)
+        self.dY = inputs.normal((T, N), w.dy_std, seed + 1, torch.bfloat16, dev)
+        self.dX = torch.empty((T, K), dtype=torch.bfloat16, device=dev) if want_dx else None
+        if w.s_dtype == "int8":
+            self.m = torch.empty((N, K), dtype=torch.int8, device=dev)
+            self.v = torch.empty((N, K), dtype=torch.uint8, device=dev)
+            self.ms = torch.empty((N, K // 64), dtype=torch.float32, device=dev)
+            self.vs = torch.empty((N, K // 64), dtype=torch.float32, device=dev)
+            api.forge_quantize_state(inputs.normal((N, K), w.m_init_std, seed + 2, torch.float32, dev),
+                                     self.m, self.ms, True)
+            api.forge_quantize_state(inputs.abs_normal((N, K), w.v_init_std, seed + 3, torch.float32, dev),
+                                     self.v, self.vs, False)
+        else:
+            self.m = torch.zeros((N, K), dtype=torch.float32, device=dev)
+            self.v = torch.zeros((N, K), dtype=torch.float32, device=dev)
+            self.ms = self.vs = None
+        self.state_bytes = 2 * N * K * (1 if w.s_dtype == "int8" else 4) + \
+            (2 * 4 * N * (K // 64) if w.s_dtype == "int8" else 0)
+
+
+def run_workload(args):
+    """One JSON line for a secondary workload: its step timed with CUDA events
+    between synchronisations (W warm-up steps, then K), the step launches' own
+    rate against the sustained bf16 peak, peak device memory and the
+    algorithmic HBM bytes per parameter."""
+    from optimizer_tcgen05_dw_gb300 import api
+    from optimizer_tcgen05_dw_gb300.build import build
+
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    build()
+    api.lib()
+    dev = torch.device("cuda", local)
+    w = inputs.WORKLOADS[args.workload]
+    T = w.T
+    stream = torch.cuda.current_stream()
+    torch.cuda.reset_peak_memory_stats(dev)
+    hbm_gbs, peak_burst, peak_sust, peak_src = _peaks()
+    sweep = args.workload == "sweep_4096"
+    opts = list(inputs.SWEEP_HPARAMS) if sweep else [w.opt]
+    # layers: (layer index, name, N, K); activations per layer
+    if args.workload == "qwen14b_int8":
+        shapes = [(li, n, N, K) for li in range(w.layers) for n, N, K in inputs.QWEN3_14B_LINEARS]
+        acts = {"x_attn": 5120, "x_o": 5120, "x_mlp": 5120, "x_down": 17408}
+        act_of = QWEN_ACT
+    elif args.workload == "llama8b_bf16_int8state":
+        shapes = [(0, n, N, K) for n, N, K in sorted(inputs.LLAMA31_8B_LINEARS, key=lambda x: ORDER.index(x[0]))]
+        acts = {"x_attn": 4096, "x_o": 4096, "x_mlp": 4096, "x_down": 14336}
+        act_of = ACT
+    else:  # one linear
+        (n0, N0, K0), = w.linears
+        shapes = [(0, n0, N0, K0)]
+        acts = {"x": K0}
+        act_of = {n0: "x"}
+    want_dx = not sweep
+    X = {(li, a): inputs.normal((T, k), w.x_std, inputs.layer_seed(7, li, 0, 50 + j), torch.bfloat16, dev)
+         for li in sorted({s[0] for s in shapes}) for j, (a, k) in enumerate(acts.items())}
+    layers = [(li, _SLayer(api, n, N, K, T, dev, inputs.layer_seed(7, li, 0, 10 * (1 + i)), w, want_dx))
+              for i, (li, n, N, K) in enumerate(shapes)]
+    torch.cuda.synchronize()
+    flops_dw = sum(2.0 * L.N * L.K * T for _, L in layers)
+    flops_step = flops_dw * (2.0 if want_dx else 1.0)
+    params = sum(L.N * L.K for _, L in layers)
+    w_bytes = 2 * (4 if w.w_dtype == "fp32" else 2)
+    bytes_step = sum(2 * (L.T * L.K + L.T * L.N) + (2 * L.T * L.K if want_dx else 0) for _, L in layers) + \
+        params * w_bytes + sum(L.state_bytes for _, L in layers)
+    results = {}
+    s_no = 1
+    for opt_name in opts:
+        hp = inputs.SWEEP_HPARAMS[opt_name] if sweep else w.hparams
+        ev = []
+
+        def step(s, record=False):
+            for li, L in layers:
+                if record:
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                s1 = L.m if opt_name in api.USES_S1 else None
+                s2 = L.v if opt_name in api.USES_S2 else None
+                api.forge_linear_bwd_step(X[(li, act_of[L.name])], L.dY, L.W, opt_name, hp, s, L.seed,
+                                          s1, s2, L.ms if s1 is not None else None,
+                                          L.vs if s2 is not None else None, dX=L.dX)
+                if record:
+                    b.record(stream)
+                    ev.append((a, b))
+
+        for _ in range(args.warmup):
+            step(s_no)
+            s_no += 1
+        api.forge_get_device_status()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            for _ in range(args.steps):
+                step(s_no, record=True)
+                s_no += 1
+            end.record(stream)
+            torch.cuda.synchronize()
+        api.forge_get_device_status()
+        ms = start.elapsed_time(end) / args.steps
+        kern_ms = sum(a.elapsed_time(b) for a, b in ev)
+        results[opt_name] = {"ms_per_step": round(ms, 4),
+                             "value": round(flops_step / (ms * 1e-3) / 1e12, 2),
+                             "kernel_tflops": round(flops_step * args.steps / (kern_ms * 1e-3) / 1e12, 2),
+                             "clocks": clk.summary()}
+    tot_ms = sum(r["ms_per_step"] for r in results.values())
+    value = flops_step * len(opts) / (tot_ms * 1e-3) / 1e12
+    kern = statistics.mean(r["kernel_tflops"] for r in results.values())
+    t_flop = flops_step / (peak_sust * 1e12)
+    t_byte = bytes_step / (hbm_gbs * 1e9)
+    bound = "tensor" if t_flop >= t_byte else "hbm"
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_ms / len(opts), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.w_dtype == "bf16" else "fp32", "data": "synthetic",
+        "secondary": True,
+        "config": {"workload": w.name, "key": args.workload, "T": T, "linears": len(layers),
+                   "flops_counted": "2NKT (dW)" + (" + 2NKT (dX)" if want_dx else "") + " per linear",
+                   "w_dtype": w.w_dtype, "s_dtype": w.s_dtype, "optimizers": opts},
+        "roofline": {"bound": bound, "achieved": round(kern, 2), "unit": "TFLOP/s",
+                     "peak": peak_sust, "peak_kind": f"bf16 sustained, {peak_src}",
+                     "frac": round(kern / peak_sust, 4),
+                     "frac_of_slower_roofline": round(max(t_flop, t_byte) * 1e3 / (tot_ms / len(opts)), 4),
+                     "algorithmic_bytes_per_step": bytes_step},
+        "hbm_bytes_per_param_algorithmic": round(bytes_step / params, 3),
+        "params": params,
+        "peak_device_memory_bytes": torch.cuda.max_memory_allocated(dev),
+        "per_optimizer": results if sweep else None,
+        "clocks": results[opts[-1]]["clocks"],
+        "gpu_launches": sum(1 if (not want_dx or (w.w_dtype == "bf16" and L.N % 64 == 0 and L.K % 64 == 0))
+                            else 2 for _, L in layers) * args.steps * len(opts),
+        "note": "inputs are drawn once per linear and reused by every timed step (timing does "
+                "not depend on their values); parity for this configuration is in the tests",
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -556,11 +720,16 @@ def main():
                     help="restrict to some linears (profiling); the bench line uses all seven")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the step only (profiling runs): no e2e, unfused or CPU legs")
+    ap.add_argument("--workload", default=WORKLOAD_KEY, choices=(WORKLOAD_KEY,) + SECONDARY,
+                    help="a secondary measured configuration instead of the headline one "
+                         "(its own JSON line, marked \"secondary\")")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != WORKLOAD_KEY:
+        run_workload(args)
     else:
         run_ours(args)
 
