@@ -189,6 +189,33 @@ __device__ __forceinline__ int quant_recip(float x, float a, float s, float inv)
   return static_cast<int>(q);
 }
 
+// The fused epilogue's INT8 arithmetic, written to keep off the conversion
+// unit (int <-> float casts and floor/rint run there at a fraction of the FP32
+// rate); every function gives the same values as the definitions above.
+//
+// Code k (0..3) of a word of four packed codes, as a float: the byte placed
+// under the exponent of 2^23 (bit pattern 0x4B0000cc) is 2^23 + c exactly, so
+// one subtraction gives c.  Signed codes are flipped to c + 128 first.
+template <bool SIGNED>
+__device__ __forceinline__ float code_f32(uint32_t word, int k) {
+  const uint32_t biased = __byte_perm(SIGNED ? (word ^ 0x80808080u) : word, 0x4B000000u, 0x7440u | k);
+  return __fsub_rn(__uint_as_float(biased), SIGNED ? 8388736.f : 8388608.f);
+}
+
+// clamp(rint(y)) as an integer, NaN -> 0: adding 1.5 * 2^23 rounds any |y| <
+// 2^22 to an integer (nearest even) held in the low mantissa bits.  `near`
+// reports a y within 3e-5 of a half-integer (see quant_recip), where the
+// rounding of y and of the exact quotient may differ.
+constexpr float kShifter = 12582912.f;
+template <bool SIGNED>
+__device__ __forceinline__ int code_round(float y, bool& near) {
+  const float yc = fminf(fmaxf(y, SIGNED ? -127.f : 0.f), SIGNED ? 127.f : 255.f);
+  const float t = __fadd_rn(yc, kShifter);
+  near = fabsf(__fsub_rn(yc, __fsub_rn(t, kShifter))) >= 0.49997f;
+  const int k = static_cast<int>(__float_as_uint(t) - 0x4B400000u);
+  return (y == y) ? k : 0;
+}
+
 // Running absmax that never takes a NaN (NaN > a is false).
 __device__ __forceinline__ float absmax_acc(float a, float x) {
   const float ax = fabsf(x);

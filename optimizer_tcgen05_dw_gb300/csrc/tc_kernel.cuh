@@ -49,6 +49,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.h"
 #include "optim.cuh"
 #include "ptx.cuh"
@@ -786,6 +788,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   const uint4 c2 = uses_s2(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub))
                                  : make_uint4(0, 0, 0, 0);
   const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
+  const float sd1 = dev::dvd(a1, 127.f), sd2 = dev::dvd(a2, 255.f);  // old code steps
   float n1 = 0.f, n2 = 0.f;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {  // two halves of 8 columns: gradient and weights
@@ -796,13 +799,11 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int j = 8 * h + i;
-      const uint32_t b1 = (q1[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      const uint32_t b2 = (q2[j >> 2] >> (8 * (j & 3))) & 0xFFu;
-      m[j] = uses_s1(KIND) ? dev::dequant<true>(static_cast<int>(static_cast<int8_t>(b1)), a1) : 0.f;
-      v[j] = uses_s2(KIND) ? dev::dequant<false>(static_cast<int>(b2), a2) : 0.f;
+      m[j] = uses_s1(KIND) ? dev::mul(dev::code_f32<true>(q1[j >> 2], j & 3), sd1) : 0.f;
+      v[j] = uses_s2(KIND) ? dev::mul(dev::code_f32<false>(q2[j >> 2], j & 3), sd2) : 0.f;
       dev::rule<KIND>(w[i], g[i], m[j], v[j], p.sc);
-      if (uses_s1(KIND)) n1 = dev::absmax_acc(n1, m[j]);
-      if (uses_s2(KIND)) n2 = dev::absmax_acc(n2, v[j]);
+      if (uses_s1(KIND)) n1 = fmaxf(n1, fabsf(m[j]));  // = absmax_acc: n1 is never NaN
+      if (uses_s2(KIND)) n2 = fmaxf(n2, fabsf(v[j]));
     }
     wv[h] = pack_sr_bf16x8(w, dev::sr_words((static_cast<uint64_t>(e0) >> 3) + h, p.seed, p.step));
   }
@@ -815,16 +816,32 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
     n1 = fmaxf(n1, amax[(0 * 4 + o) * 128 + r]);
     n2 = fmaxf(n2, amax[(1 * 4 + o) * 128 + r]);
   }
+  // New codes (dev::quant_recip's rule): round x * (1/s) with the shifter;
+  // the few near a half-integer, and every code of a block whose reciprocal
+  // is not finite, are redone from the exact quotient x / s (a branch that is
+  // rarely taken).
   uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
   const float st1 = dev::dvd(n1, 127.f), st2 = dev::dvd(n2, 255.f);  // code steps
   const float iv1 = dev::dvd(1.f, st1), iv2 = dev::dvd(1.f, st2);
+  const bool bad1 = !(fabsf(iv1) <= 3.0e38f), bad2 = !(fabsf(iv2) <= 3.0e38f);
+  auto codes = [&](const float (&x)[16], float st, float inv, bool bad, uint32_t (&o)[4], auto sgn) {
+    constexpr bool S = decltype(sgn)::value;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    if (uses_s1(KIND))
-      o1[j >> 2] |= (static_cast<uint32_t>(dev::quant_recip<true>(m[j], n1, st1, iv1)) & 0xFFu) << (8 * (j & 3));
-    if (uses_s2(KIND))
-      o2[j >> 2] |= (static_cast<uint32_t>(dev::quant_recip<false>(v[j], n2, st2, iv2)) & 0xFFu) << (8 * (j & 3));
-  }
+    for (int q = 0; q < 4; ++q) {  // four codes per word, byte i = code 4q + i
+      int k[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        bool nr;
+        k[i] = dev::code_round<S>(dev::mul(x[4 * q + i], inv), nr);
+        if (nr || bad) k[i] = dev::code_round<S>(dev::dvd(x[4 * q + i], st), nr);
+      }
+      o[q] = __byte_perm(__byte_perm(k[0], k[1], 0x0040u), __byte_perm(k[2], k[3], 0x0040u), 0x5410u);
+    }
+  };
+  if (uses_s1(KIND)) codes(m, st1, iv1, bad1, o1, std::true_type{});
+  if (uses_s2(KIND)) codes(v, st2, iv2, bad2, o2, std::false_type{});
+  if (n1 == 0.f) o1[0] = o1[1] = o1[2] = o1[3] = 0u;  // a zero block keeps zero codes
+  if (n2 == 0.f) o2[0] = o2[1] = o2[2] = o2[3] = 0u;
   if (uses_s1(KIND))
     *reinterpret_cast<uint4*>(buf + kOffS1 + sw64(r, sub)) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
   if (uses_s2(KIND))

@@ -354,3 +354,35 @@ def test_one_launch_step_timeout_reports_and_context_survives():
     ref, rdx, _ = prob.run_oracle(want_dx=True)
     _compare_exact(prob, gpu, ref)
     assert_dx_close(gdx[0], to_bits(prob.dY[0]), prob.state0["W"], "dX")
+
+
+def test_int8_requantisation_ties_and_zero_blocks_bitexact():
+    """The fused epilogue's INT8 requantisation on exact ties: SGD-momentum
+    with momentum 0 stores g itself in the signed code buffer; one token
+    makes g the outer product dY[0] X[0], with X[0] holding 127 and the
+    half-integers 0.5 .. 62.5 (alternating signs, times 2^-6) in every block
+    of 64, so g / (absmax / 127) lands exactly on half-integers (ties to even
+    on both the reciprocal and the exact-division path); a zero row of dY
+    leaves zero blocks (scale 0, codes 0)."""
+    T, N, K = 16, 256, 320
+    blk = np.array([127.0] + [(j + 0.5) * (-1) ** j for j in range(63)]) * 2.0 ** -6
+    x = np.zeros((T, K), np.float32)
+    x[0] = np.tile(blk, K // 64)
+    dy = np.zeros((T, N), np.float32)
+    dy[0] = np.where(np.arange(N) % 3 == 1, 0.0, np.where(np.arange(N) % 3 == 2, -1.0, 1.0))
+    X = torch.from_numpy(x).to(torch.bfloat16)
+    dY = torch.from_numpy(dy).to(torch.bfloat16)
+    hp = dict(lr=1e-2, momentum=0.0)
+    prob = Problem(T=T, N=N, K=K, w_dtype="bf16", s_dtype="int8", opt_name="sgd_momentum", hp=hp,
+                   grid=True, steps=1, seed=31)
+    prob.X, prob.dY = [X], [dY]
+    st0 = dict(prob.state0)
+    st0["s1"] = np.zeros((N, K), np.int8)
+    st0["s1_scale"] = np.zeros((N, K // 64), np.float32)
+    prob.state0 = st0
+    gpu, _ = prob.run_gpu(fused=True)
+    ref, _, _ = prob.run_oracle()
+    _compare_exact(prob, gpu, ref)
+    codes = ref["s1"].astype(np.int64)
+    assert (codes[0, 1:64] % 2 == 0).all() and np.abs(codes[0, 1:64]).max() > 60  # ties went to even
+    assert (ref["s1_scale"][1::3] == 0).all() and (codes[1::3] == 0).all()          # zero blocks
