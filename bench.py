@@ -610,11 +610,14 @@ def run_workload(args):
     opts = list(inputs.SWEEP_HPARAMS) if sweep else [w.opt]
     # layers: (layer index, name, N, K); activations per layer
     if args.workload == "qwen14b_int8":
-        shapes = [(li, n, N, K) for li in range(w.layers) for n, N, K in inputs.QWEN3_14B_LINEARS]
+        n_layers = w.layers if args.num_layers is None else args.num_layers
+        shapes = [(li, n, N, K) for li in range(n_layers) for n, N, K in inputs.QWEN3_14B_LINEARS
+                  if not args.layers or n in args.layers]
         acts = {"x_attn": 5120, "x_o": 5120, "x_mlp": 5120, "x_down": 17408}
         act_of = QWEN_ACT
     elif args.workload == "llama8b_bf16_int8state":
-        shapes = [(0, n, N, K) for n, N, K in sorted(inputs.LLAMA31_8B_LINEARS, key=lambda x: ORDER.index(x[0]))]
+        shapes = [(0, n, N, K) for n, N, K in sorted(inputs.LLAMA31_8B_LINEARS, key=lambda x: ORDER.index(x[0]))
+                  if not args.layers or n in args.layers]
         acts = {"x_attn": 4096, "x_o": 4096, "x_mlp": 4096, "x_down": 14336}
         act_of = ACT
     else:  # one linear
@@ -622,7 +625,7 @@ def run_workload(args):
         shapes = [(0, n0, N0, K0)]
         acts = {"x": K0}
         act_of = {n0: "x"}
-    want_dx = not sweep
+    want_dx = not sweep and not args.no_dx
     X = {(li, a): inputs.normal((T, k), w.x_std, inputs.layer_seed(7, li, 0, 50 + j), torch.bfloat16, dev)
          for li in sorted({s[0] for s in shapes}) for j, (a, k) in enumerate(acts.items())}
     layers = [(li, _SLayer(api, n, N, K, T, dev, inputs.layer_seed(7, li, 0, 10 * (1 + i)), w, want_dx))
@@ -690,7 +693,8 @@ def run_workload(args):
         "secondary": True,
         "config": {"workload": w.name, "key": args.workload, "T": T, "linears": len(layers),
                    "flops_counted": "2NKT (dW)" + (" + 2NKT (dX)" if want_dx else "") + " per linear",
-                   "w_dtype": w.w_dtype, "s_dtype": w.s_dtype, "optimizers": opts},
+                   "w_dtype": w.w_dtype, "s_dtype": w.s_dtype, "optimizers": opts,
+                   "partial": bool(args.layers or args.num_layers is not None or args.no_dx)},
         "roofline": {"bound": bound, "achieved": round(kern, 2), "unit": "TFLOP/s",
                      "peak": peak_sust, "peak_kind": f"bf16 sustained, {peak_src}",
                      "frac": round(kern / peak_sust, 4),
@@ -720,6 +724,10 @@ def main():
                     help="restrict to some linears (profiling); the bench line uses all seven")
     ap.add_argument("--no-extras", action="store_true",
                     help="time the step only (profiling runs): no e2e, unfused or CPU legs")
+    ap.add_argument("--num-layers", type=int, default=None,
+                    help="with --workload qwen14b_int8: decoder layers to sweep (profiling; default 40)")
+    ap.add_argument("--no-dx", action="store_true",
+                    help="with --workload: the weight step alone, without dX (profiling)")
     ap.add_argument("--workload", default=WORKLOAD_KEY, choices=(WORKLOAD_KEY,) + SECONDARY,
                     help="a secondary measured configuration instead of the headline one "
                          "(its own JSON line, marked \"secondary\")")

@@ -205,11 +205,14 @@ __device__ __forceinline__ float code_f32(uint32_t word, int k) {
 // clamp(rint(y)) as an integer, NaN -> 0: adding 1.5 * 2^23 rounds any |y| <
 // 2^22 to an integer (nearest even) held in the low mantissa bits.  `near`
 // reports a y within 3e-5 of a half-integer (see quant_recip), where the
-// rounding of y and of the exact quotient may differ.
+// rounding of y and of the exact quotient may differ.  CLAMP = false is for
+// y = x * RN(1/s) with a finite reciprocal and |x| <= absmax: then s >=
+// 3.3e-39, whose relative spacing is below 5e-7, so |y| <= 127.0001 (255.0002
+// unsigned, where x >= 0) and the clamp would never change the rounded code.
 constexpr float kShifter = 12582912.f;
-template <bool SIGNED>
+template <bool SIGNED, bool CLAMP = true>
 __device__ __forceinline__ int code_round(float y, bool& near) {
-  const float yc = fminf(fmaxf(y, SIGNED ? -127.f : 0.f), SIGNED ? 127.f : 255.f);
+  const float yc = CLAMP ? fminf(fmaxf(y, SIGNED ? -127.f : 0.f), SIGNED ? 127.f : 255.f) : y;
   const float t = __fadd_rn(yc, kShifter);
   near = fabsf(__fsub_rn(yc, __fsub_rn(t, kShifter))) >= 0.49997f;
   const int k = static_cast<int>(__float_as_uint(t) - 0x4B400000u);

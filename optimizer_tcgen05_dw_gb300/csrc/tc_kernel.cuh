@@ -704,8 +704,8 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
                                                int64_t e0, uint4& wv, const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 16384;
   float g[8], w[8], s1[8], s2[8];
-  ptx::tmem_ld_32x32b_x8(taddr, g);
-  if (SCALE) scale_grad(g, p);
+  uint32_t gr[8];
+  ptx::tmem_ld_issue(taddr, gr);  // the gradient arrives while the states are read
   unpack_bf16x8(wv, w);
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -722,6 +722,10 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
       s2[4 * i] = s2[4 * i + 1] = s2[4 * i + 2] = s2[4 * i + 3] = 0.f;
     }
   }
+  ptx::tmem_wait_ld(gr);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
+  if (SCALE) scale_grad(g, p);
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
   wv = pack_sr_bf16x8(w, dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step));
@@ -745,11 +749,15 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
                                                 int64_t e0, uint4& wv, const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 8192;
   float g[8], w[8], s1[8], s2[8];
-  ptx::tmem_ld_32x32b_x8(taddr, g);
-  if (SCALE) scale_grad(g, p);
+  uint32_t gr[8];
+  ptx::tmem_ld_issue(taddr, gr);  // the gradient arrives while the states are read
   unpack_bf16x8(wv, w);
   if (uses_s1(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub)), s1);
   if (uses_s2(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub)), s2);
+  ptx::tmem_wait_ld(gr);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
+  if (SCALE) scale_grad(g, p);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if (!uses_s1(KIND)) s1[j] = 0.f;
@@ -783,6 +791,8 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
                                                const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 8192, kOffAmax = 16384;
   float m[16], v[16];  // the new moments stay live until the block absmax is known
+  uint32_t gr[16];
+  ptx::tmem_ld_issue(taddr, gr);  // the gradient arrives while the codes are read
   const uint4 c1 = uses_s1(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub))
                                  : make_uint4(0, 0, 0, 0);
   const uint4 c2 = uses_s2(KIND) ? *reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub))
@@ -790,10 +800,12 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
   const float sd1 = dev::dvd(a1, 127.f), sd2 = dev::dvd(a2, 255.f);  // old code steps
   float n1 = 0.f, n2 = 0.f;
+  ptx::tmem_wait_ld(gr);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {  // two halves of 8 columns: gradient and weights
     float g[8], w[8];
-    ptx::tmem_ld_32x32b_x8(taddr + 8 * h, g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) g[i] = __uint_as_float(gr[8 * h + i]);
     if (SCALE) scale_grad(g, p);
     unpack_bf16x8(wv[h], w);
 #pragma unroll
@@ -832,7 +844,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         bool nr;
-        k[i] = dev::code_round<S>(dev::mul(x[4 * q + i], inv), nr);
+        k[i] = dev::code_round<S, false>(dev::mul(x[4 * q + i], inv), nr);
         if (nr || bad) k[i] = dev::code_round<S>(dev::dvd(x[4 * q + i], st), nr);
       }
       o[q] = __byte_perm(__byte_perm(k[0], k[1], 0x0040u), __byte_perm(k[2], k[3], 0x0040u), 0x5410u);
