@@ -991,9 +991,7 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
     if (G::U1) ptx::tma_load_2d_hint(mS1, bar, buf + G::kOffS1, col0, row0, pol);
     if (G::U2) ptx::tma_load_2d_hint(mS2, bar, buf + G::kOffS2, col0, row0, pol);
   };
-  auto store = [&](int j) {
-    int row0, col0;
-    walk.where(j, G::kCC, row0, col0);
+  auto store_at = [&](int j, int row0, int col0) {
     const uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
     if (G::U1) ptx::tma_store_2d_hint(mS1, buf + G::kOffS1, col0, row0, pol);
     if (G::U2) ptx::tma_store_2d_hint(mS2, buf + G::kOffS2, col0, row0, pol);
@@ -1031,32 +1029,52 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
     }
     if (io) ptx::bulk_wait_group_read0();  // the buffers are free for the weight tiles' states
   }
-  if (io && total > 0 && !aborted) {
-    issue(0);
-    issued = 1;
-  }
   const int first = local + 1;  // accumulator index of the first dW tile
-  for (int j = 0; j < total && !aborted; ++j) {
-    const int c = j % G::kChunks;
+  // Waits until chunk j may start: its tile's accumulator (first chunk of a
+  // tile) and its staged states.  False if a wait failed.
+  auto ready = [&](int j) -> bool {
     bool ok = true;
-    if (c == 0) {
+    if (j % G::kChunks == 0) {
       ++local;
       if (local > first) walk.advance(local - first, p, rank);
       if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
       if (STEP && io && ok) ok = bounded_wait_count(p.dx_done + walk.cur_col0 / kTileN, p.dx_target, p, ss);
     }
     if (io && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
-    // Releases the compute warps into chunk j (ordering their tensor- and
-    // shared-memory reads after the waits above), or stops everyone.
-    if (ptx::bar_red_or(kEpiBarrier, G::kNB, !ok)) break;
-    consumed = j + 1;
-    if (io && j + 1 < total) {
+    return ok;
+  };
+  // The barriers release the compute warps into a chunk (ordering their
+  // tensor- and shared-memory reads after the waits above) or stop everyone;
+  // inside a tile one barrier both ends chunk j and starts chunk j + 1.  At
+  // the end of a tile the compute warps free the accumulator between two
+  // barriers, so the next tile's MMAs never wait for the tile after it.
+  bool stop = aborted || total == 0;
+  if (!stop) {
+    if (io) {
+      issue(0);
+      issued = 1;
+    }
+    stop = ptx::bar_red_or(kEpiBarrier, G::kNB, !ready(0));
+    if (!stop) consumed = 1;
+  }
+  for (int j = 0; j < total && !stop; ++j) {
+    int srow, scol;
+    walk.where(j, G::kCC, srow, scol);  // chunk j's origin, before the walk moves on
+    const bool more = j + 1 < total;
+    if (io && more) {
       ptx::bulk_wait_group_read0();  // chunk j-1's stores have read buffer (j+1)&1
       issue(j + 1);
       issued = j + 2;
     }
-    ptx::bar_sync(kEpiBarrier, G::kNB);  // chunk j is back in shared memory
-    if (io) store(j);
+    if (more && (j + 1) % G::kChunks != 0) {
+      stop = ptx::bar_red_or(kEpiBarrier, G::kNB, !ready(j + 1));
+      if (io) store_at(j, srow, scol);
+    } else {
+      ptx::bar_sync(kEpiBarrier, G::kNB);  // chunk j is back in shared memory
+      if (io) store_at(j, srow, scol);
+      if (more) stop = ptx::bar_red_or(kEpiBarrier, G::kNB, !ready(j + 1));
+    }
+    if (!stop && more) consumed = j + 2;
   }
   if (io) {
     ptx::bulk_wait_group0();
@@ -1125,14 +1143,20 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     }
   }
   const int first = local + 1;  // accumulator index of the first dW tile
-  if (total > 0) prefetch(0, wnext, o1next, o2next);
-  for (int j = 0; j < total; ++j) {
-    const int c = j % kChunks;
-    if (c == 0) {
+  auto begin = [&](int j) {  // chunk j is about to start: the walk follows its tile
+    if (j % kChunks == 0) {
       ++local;
       if (local > first) walk.advance(local - first, p, rank);
     }
-    if (ptx::bar_red_or(kEpiBarrier, G::kNB, false)) break;  // the I/O warp's verdict
+  };
+  bool stop = total == 0;
+  if (!stop) {
+    prefetch(0, wnext, o1next, o2next);
+    begin(0);
+    stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);  // the I/O warp's verdict
+  }
+  for (int j = 0; j < total && !stop; ++j) {
+    const int c = j % kChunks;
     int row0, col0;
     walk.where(j, kCC, row0, col0);
     const int64_t row = static_cast<int64_t>(row0) + r;
@@ -1169,8 +1193,18 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     }
     if (c == kChunks - 1) ptx::tc_fence_before();
     ptx::fence_proxy_async_smem();
-    ptx::bar_sync(kEpiBarrier, G::kNB);
-    if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
+    const bool more = j + 1 < total;
+    if (more && c != kChunks - 1) {  // end of chunk j = start of chunk j + 1 (same tile)
+      begin(j + 1);
+      stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);
+    } else {
+      ptx::bar_sync(kEpiBarrier, G::kNB);
+      if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
+      if (more) {
+        begin(j + 1);
+        stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);
+      }
+    }
   }
 }
 
