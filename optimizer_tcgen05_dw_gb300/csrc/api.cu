@@ -232,6 +232,16 @@ forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t 
   return FORGE_OK;
 }
 
+// The bf16 weights in 64-column x 128-row boxes (128-byte swizzle): the
+// epilogue stages them with INT8 states.  Otherwise a copy of `other` (unused).
+forge_status_t weight_map(const forge_state_t* st, int64_t N, int64_t K, const CUtensorMap& other,
+                          CUtensorMap* mw) {
+  *mw = other;
+  if (st->w_dtype == FORGE_W_BF16_SR && st->s_dtype == FORGE_STATE_INT8_B64)
+    return bf16_map(mw, st->W, K, N, 64, kTileM);
+  return FORGE_OK;
+}
+
 // ---------------------------------------------------------------- scalars
 
 // Per-step scalars of each rule, in double from the float hyper-parameters,
@@ -451,7 +461,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
                            const DeviceInfo& d, uint32_t* counters = nullptr) {
   const int64_t T = lin->T, N = lin->N, K = lin->K;
   forge_status_t st;
-  CUtensorMap ma, mb, mda, mdb, m1, m2, mdx;
+  CUtensorMap ma, mb, mda, mdb, m1, m2, mdx, mw;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   if ((st = wgrad_maps(lin, kFusedBlockK, &ma, &mb, &p.op3d)) != FORGE_OK) return st;
@@ -459,6 +469,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   if ((st = mn_major_3d_map(&mdb, state->W, K, N, kFusedBlockK, kTileN / 2 / 64)) != FORGE_OK) return st;
   if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
   if ((st = bf16_map(&mdx, lin->dX, K, T, 64, kTileM)) != FORGE_OK) return st;
+  if ((st = weight_map(state, N, K, ma, &mw)) != FORGE_OK) return st;
   fill_tiles(p, N, K, T, kFusedBlockK);
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
@@ -481,7 +492,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   // tiles): at most the occupancy limit, at most one pair per tile.
   const int pairs = std::min(std::min(d.num_sms / 2, d.step_pairs[state->s_dtype]), p.num_tiles + p.dx_tiles);
   balance_dx(p, pairs, T, N);
-  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, p, 2 * pairs, s)) !=
+  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, mw, p, 2 * pairs, s)) !=
       cudaSuccess)
     return cuda_fail(e, "one-launch step");
   return FORGE_OK;
@@ -552,11 +563,12 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
-  CUtensorMap m1 = ma, m2 = ma;
+  CUtensorMap m1 = ma, m2 = ma, mw = ma;
   if (state->w_dtype == FORGE_W_BF16_SR &&
-      (st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK)
+      ((st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK ||
+       (st = weight_map(state, lin->N, lin->K, ma, &mw)) != FORGE_OK))
     return st;
-  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, m1, m2, p, grid_for(p, d), s)) !=
+  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, m1, m2, mw, p, grid_for(p, d), s)) !=
       cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
@@ -633,7 +645,7 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   }
   // A = dY^T [N x T] and B = X^T [K x T], token-contiguous: K-major operands,
   // 128 tokens (bytes) by 128 rows per box.
-  CUtensorMap ma, mb, m1, m2;
+  CUtensorMap ma, mb, m1, m2, mw;
   if ((st = tensor_map(&ma, lin->dYt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, T, N, kFp8BlockK, kTileM,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FORGE_OK)
     return st;
@@ -641,6 +653,7 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FORGE_OK)
     return st;
   if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
+  if ((st = weight_map(state, N, K, ma, &mw)) != FORGE_OK) return st;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   fill_tiles(p, N, K, T, kFp8BlockK);
@@ -653,7 +666,7 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
   p.gscale = static_cast<float>(c);
-  if ((e = launch_tc_fp8(state->s_dtype, ma, mb, m1, m2, p, grid_for(p, d), s)) != cudaSuccess)
+  if ((e = launch_tc_fp8(state->s_dtype, ma, mb, m1, m2, mw, p, grid_for(p, d), s)) != cudaSuccess)
     return cuda_fail(e, "FP8 step launch");
   return FORGE_OK;
 }

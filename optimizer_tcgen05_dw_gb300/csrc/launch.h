@@ -26,17 +26,18 @@ struct ElemParams {
 // tc_fused.cu: the FORGE step (mode kModeFusedOpt) for one (W dtype, state dtype).
 // s1, s2: tensor maps of the state tiles the bf16-weight epilogue stages
 // through shared memory (unused, any valid map, for fp32 weights or for
-// states the rule does not keep).
+// states the rule does not keep); w: bf16 W in 64-column x 128-row boxes
+// (128-byte swizzle), staged with INT8 states (else any valid map).
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
-                            const CUtensorMap& s1, const CUtensorMap& s2, const GemmParams& p,
-                            int grid, cudaStream_t s);
+                            const CUtensorMap& s1, const CUtensorMap& s2, const CUtensorMap& w,
+                            const GemmParams& p, int grid, cudaStream_t s);
 // tc_step.cu: dX and the FORGE step in one launch (mode kModeStep, bf16
 // weights): a, b the dW operands, da, db the dX operands (dY K-major, W),
 // dx the dX output (bf16, 64-column x 128-row boxes, 128-byte swizzle).
 cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
-                           const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p,
-                           int grid, cudaStream_t s);
+                           const CUtensorMap& s2, const CUtensorMap& dx, const CUtensorMap& w,
+                           const GemmParams& p, int grid, cudaStream_t s);
 // CTA pairs of the one-launch step that can be resident at once (its dW tiles
 // wait for dX tiles of other pairs, so its grid must not exceed this); 0 if
 // the query fails.
@@ -45,7 +46,8 @@ int step_max_pairs(int sdt);
 // weights): a = dY^T codes [N x T], b = X^T codes [K x T], 128 x 128-byte
 // boxes with the 128-byte swizzle; p.gscale the product of the scales.
 cudaError_t launch_tc_fp8(int sdt, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& s1,
-                          const CUtensorMap& s2, const GemmParams& p, int grid, cudaStream_t s);
+                          const CUtensorMap& s2, const CUtensorMap& w, const GemmParams& p, int grid,
+                          cudaStream_t s);
 // tc_plain.cu: unfused pass 1 (kModeWgradStore) or dX (kModeDgrad).
 cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t s);

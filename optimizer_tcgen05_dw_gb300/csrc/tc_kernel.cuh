@@ -74,24 +74,31 @@ struct SharedState {
 // deeper ring.  A stage holds 128 rows of A and 128 columns of B (half of the
 // pair's 256): 32 KiB at 64 tokens.
 constexpr int kEpiBufBytes = 32768;
+// INT8 states stage the bf16 weight chunk too (see StagedGeom): a larger
+// buffer, and one operand stage fewer to make room.
+constexpr int kEpiBufBytesW = 37888;
+__host__ __device__ constexpr bool stages_weights(int sdt) { return sdt == kSInt8; }
 constexpr int kEpiBarrier = 1;       // named barrier of the epilogue warps
 constexpr int kEpiInnerBarrier = 2;  // the staged epilogue's compute warps only
 constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 
-template <int MODE, int WDT>
+template <int MODE, int WDT, int SDT = kSFp32>
 struct KCfg {
   static constexpr bool kFp8 = (MODE == kModeFusedFp8);
   static constexpr bool kTmaEpi =
       ((MODE == kModeFusedOpt || MODE == kModeStep || kFp8) && WDT == kWBf16);
+  static constexpr bool kStageW = kTmaEpi && stages_weights(SDT);
   static constexpr int kBK =
       kFp8 ? kFp8BlockK
            : (kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK));  // tokens per stage
   static constexpr int kStg =
-      kTmaEpi ? kFusedStages : (MODE == kModeWgradStore ? kWgradStages : kStages);
+      kTmaEpi ? (kStageW ? kFusedStages - 1 : kFusedStages)
+              : (MODE == kModeWgradStore ? kWgradStages : kStages);
   static constexpr int kEsz = kFp8 ? 1 : 2;           // operand element bytes
   static constexpr int kA = kTileM * kBK * kEsz;       // bytes of A per stage (this CTA's 128 rows)
   static constexpr int kB = (kTileN / 2) * kBK * kEsz; // bytes of B per stage (this CTA's 128 columns)
-  static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBufBytes : 0;
+  static constexpr int kEpiBuf = kStageW ? kEpiBufBytesW : kEpiBufBytes;
+  static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBuf : 0;
   static constexpr int kSmem = kStg * (kA + kB) + kEpiBytes + 512 + 1024;
   // TMA warp, MMA warp, epilogue warps (four per 32-lane quarter of TMEM in the
   // staged epilogue, two in the plain ones).
@@ -105,6 +112,8 @@ static_assert(KCfg<kModeWgradStore, kWBf16>::kSmem <= 232448, "dynamic shared me
 static_assert(KCfg<kModeFusedOpt, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeDgrad, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeFusedFp8, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeStep, kWBf16, kSInt8>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeFusedFp8, kWBf16, kSInt8>::kSmem <= 232448, "dynamic shared memory limit");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -879,6 +888,13 @@ struct StagedGeom {
   static constexpr uint32_t kStateBytes = (I8 || BF) ? 8192u : 16384u;
   static constexpr uint32_t kTx = (U1 ? kStateBytes : 0u) + (U2 ? kStateBytes : 0u);
   static constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
+  // INT8: the chunk's bf16 weights (128 rows x 128 bytes, 128-byte swizzle)
+  // are staged by TMA as well, and the old scales of the next chunk are
+  // handed from the quarter that loads them to the other three.
+  static constexpr bool WST = stages_weights(SDT);
+  static constexpr int kOffAmax = 16384, kOffOld = 20480, kOffW = 21504;
+  static constexpr int kBuf = WST ? kEpiBufBytesW : kEpiBufBytes;
+  static constexpr uint32_t kTxAll = kTx + (WST ? 16384u : 0u);
   static constexpr int kNC = 32 * kNumEpiWarpsStaged;  // compute threads
   static constexpr int kNB = kNC + 32;                 // compute threads + the I/O warp
 };
@@ -971,8 +987,8 @@ __device__ __forceinline__ void epi_dx_stage(uint32_t taddr, uint8_t* box, int r
 // counted, so no weight is written while a dX tile may still read it.
 template <int KIND, int SDT, int MODE>
 __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
-                                 const CUtensorMap* mDX, const GemmParams& p, SharedState* ss,
-                                 uint8_t* epi, int lane, uint32_t rank) {
+                                 const CUtensorMap* mDX, const CUtensorMap* mW, const GemmParams& p,
+                                 SharedState* ss, uint8_t* epi, int lane, uint32_t rank) {
   using G = StagedGeom<KIND, SDT>;
   constexpr bool STEP = MODE == kModeStep;
   TileWalk<G::kChunks> walk;
@@ -985,16 +1001,18 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
   auto issue = [&](int j) {
     int row0, col0;
     walk.where(j, G::kCC, row0, col0);
-    uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
+    uint8_t* buf = epi + (j & 1) * G::kBuf;
     uint64_t* bar = &ss->epi_full[j & 1];
-    ptx::mbar_arrive_expect_tx(bar, G::kTx);
+    ptx::mbar_arrive_expect_tx(bar, G::kTxAll);
     if (G::U1) ptx::tma_load_2d_hint(mS1, bar, buf + G::kOffS1, col0, row0, pol);
     if (G::U2) ptx::tma_load_2d_hint(mS2, bar, buf + G::kOffS2, col0, row0, pol);
+    if (G::WST) ptx::tma_load_2d_hint(mW, bar, buf + G::kOffW, col0, row0, pol);
   };
   auto store_at = [&](int j, int row0, int col0) {
-    const uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
+    const uint8_t* buf = epi + (j & 1) * G::kBuf;
     if (G::U1) ptx::tma_store_2d_hint(mS1, buf + G::kOffS1, col0, row0, pol);
     if (G::U2) ptx::tma_store_2d_hint(mS2, buf + G::kOffS2, col0, row0, pol);
+    if (G::WST) ptx::tma_store_2d_hint(mW, buf + G::kOffW, col0, row0, pol);
     ptx::bulk_commit_group();
   };
   int issued = 0, consumed = 0, local = -1;
@@ -1113,9 +1131,11 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     const int col = col0 + sub * kWPerThread;
     const bool ok = row < p.M && col < K;
     const uint16_t* q = static_cast<const uint16_t*>(p.W) + row * K + col;
+    if (!G::WST) {
 #pragma unroll
-    for (int h = 0; h < kWPerThread / 8; ++h)
-      v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
+      for (int h = 0; h < kWPerThread / 8; ++h)
+        v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
+    }
     if (G::I8) {  // one code block per chunk
       const bool okb = row < p.M && col0 < K;
       const int64_t sidx = row * (K / 64) + col0 / 64;
@@ -1161,13 +1181,25 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     walk.where(j, kCC, row0, col0);
     const int64_t row = static_cast<int64_t>(row0) + r;
     uint4 wcur[kWPerThread / 8];
+    uint8_t* buf = epi + (j & 1) * G::kBuf;
+    float o1 = o1next, o2 = o2next;
+    if (G::WST) {  // staged weights; old scales from the quarter that loaded them
 #pragma unroll
-    for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
-    const float o1 = o1next, o2 = o2next;
-    if (j + 1 < total) prefetch(j + 1, wnext, o1next, o2next);
+      for (int h = 0; h < kWPerThread / 8; ++h)
+        wcur[h] = *reinterpret_cast<const uint4*>(buf + G::kOffW + sw128(r, 2 * sub + h));
+      if (j > 0) {
+        const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
+        o1 = old[r];
+        o2 = old[128 + r];
+      }
+      if (j + 1 < total && sub == 0) prefetch(j + 1, wnext, o1next, o2next);
+    } else {
+#pragma unroll
+      for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
+      if (j + 1 < total) prefetch(j + 1, wnext, o1next, o2next);
+    }
     ptx::tc_fence_after();
     const int acc = local & 1;
-    uint8_t* buf = epi + (j & 1) * kEpiBufBytes;
     const int col = col0 + sub * kWPerThread;
     const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(acc * kTileN + c * kCC + sub * kWPerThread);
@@ -1186,7 +1218,16 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     } else {
       epi_chunk_fp32<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     }
-    if (row < p.M && col < K) {
+    if (G::WST) {  // back to the staged chunk (TMA-stored); the next chunk's old scales
+#pragma unroll
+      for (int h = 0; h < kWPerThread / 8; ++h)
+        *reinterpret_cast<uint4*>(buf + G::kOffW + sw128(r, 2 * sub + h)) = wcur[h];
+      if (j + 1 < total && sub == 0) {
+        float* nold = reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffOld);
+        nold[r] = o1next;
+        nold[128 + r] = o2next;
+      }
+    } else if (row < p.M && col < K) {
       uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
@@ -1210,42 +1251,44 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 
 template <int KIND, int SDT, int MODE>
 __device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CUtensorMap* mS2,
-                                                const CUtensorMap* mDX, const GemmParams& p,
+                                                const CUtensorMap* mDX, const CUtensorMap* mW,
+                                                const GemmParams& p,
                                                 SharedState* ss, uint8_t* epi, int warp, int lane,
                                                 uint32_t rank) {
   if (warp == 2 + kNumEpiWarpsStaged)
-    epilogue_io_role<KIND, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, lane, rank);
+    epilogue_io_role<KIND, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, lane, rank);
   else
     epilogue_compute_role<KIND, SDT, MODE>(p, ss, epi, warp, lane, rank);
 }
 
 template <int SDT, int MODE>
 __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, const CUtensorMap* mS2,
-                                                      const CUtensorMap* mDX, const GemmParams& p,
+                                                      const CUtensorMap* mDX, const CUtensorMap* mW,
+                                                      const GemmParams& p,
                                                       SharedState* ss, uint8_t* epi, int warp,
                                                       int lane, uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_staged<kAdamW, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kNAdam: epilogue_staged<kNAdam, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kRAdam: epilogue_staged<kRAdam, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kLion: epilogue_staged<kLion, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kRMSprop: epilogue_staged<kRMSprop, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    case kSGD: epilogue_staged<kSGD, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
-    default: epilogue_staged<kSGDMomentum, SDT, MODE>(mS1, mS2, mDX, p, ss, epi, warp, lane, rank); break;
+    case kAdamW: epilogue_staged<kAdamW, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_staged<kNAdam, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_staged<kRAdam, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_staged<kLion, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_staged<kRMSprop, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_staged<kSGD, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_staged<kSGDMomentum, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
   }
 }
 
 // ------------------------------------------------------------------ kernel
 
 template <int MODE, int WDT, int SDT>
-__global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
+__global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
               const __grid_constant__ CUtensorMap mapDA, const __grid_constant__ CUtensorMap mapDB,
               const __grid_constant__ CUtensorMap mapS1,
               const __grid_constant__ CUtensorMap mapS2, const __grid_constant__ CUtensorMap mapDX,
-              const GemmParams p) {
-  using Cfg = KCfg<MODE, WDT>;
+              const __grid_constant__ CUtensorMap mapW, const GemmParams p) {
+  using Cfg = KCfg<MODE, WDT, SDT>;
   constexpr int STG = Cfg::kStg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -1296,7 +1339,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT>::kThreads, 1)
     if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT, MODE>(&mapS1, &mapS2, &mapDX, p, ss, epi, warp, lane, rank);
+      epilogue_tma_dispatch<SDT, MODE>(&mapS1, &mapS2, &mapDX, &mapW, p, ss, epi, warp, lane, rank);
     else
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
@@ -1316,7 +1359,8 @@ template <typename Kernel>
 inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaStream_t s,
                                const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
                                const CUtensorMap& db, const CUtensorMap& s1,
-                               const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p) {
+                               const CUtensorMap& s2, const CUtensorMap& dx, const CUtensorMap& w,
+                               const GemmParams& p) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
@@ -1329,7 +1373,7 @@ inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaSt
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, b, da, db, s1, s2, dx, p);
+  return cudaLaunchKernelEx(&cfg, k, a, b, da, db, s1, s2, dx, w, p);
 }
 
 }  // namespace forge

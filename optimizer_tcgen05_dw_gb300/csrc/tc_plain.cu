@@ -12,7 +12,7 @@ static cudaError_t run_plain(const CUtensorMap& a, const CUtensorMap& b, const G
   constexpr int smem = KCfg<MODE, kWBf16>::kSmem;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pair(k, grid, KCfg<MODE, kWBf16>::kThreads, smem, s, a, b, a, b, a, a, a, p);  // only a, b used
+  return launch_pair(k, grid, KCfg<MODE, kWBf16>::kThreads, smem, s, a, b, a, b, a, a, a, a, p);  // only a, b used
 }
 
 cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,

@@ -9,22 +9,23 @@ namespace forge {
 template <int SDT>
 static cudaError_t run_step(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
                             const CUtensorMap& db, const CUtensorMap& s1, const CUtensorMap& s2,
-                            const CUtensorMap& dx, const GemmParams& p, int grid, cudaStream_t s) {
+                            const CUtensorMap& dx, const CUtensorMap& w, const GemmParams& p, int grid,
+                            cudaStream_t s) {
   auto* k = tc_kernel<kModeStep, kWBf16, SDT>;
-  constexpr int smem = KCfg<kModeStep, kWBf16>::kSmem;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  using Cfg = KCfg<kModeStep, kWBf16, SDT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
   if (e != cudaSuccess) return e;
-  return launch_pair(k, grid, KCfg<kModeStep, kWBf16>::kThreads, smem, s, a, b, da, db, s1, s2, dx, p);
+  return launch_pair(k, grid, Cfg::kThreads, Cfg::kSmem, s, a, b, da, db, s1, s2, dx, w, p);
 }
 
 template <int SDT>
 static int step_pairs() {
   auto* k = tc_kernel<kModeStep, kWBf16, SDT>;
-  constexpr int smem = KCfg<kModeStep, kWBf16>::kSmem;
+  constexpr int smem = KCfg<kModeStep, kWBf16, SDT>::kSmem;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(KCfg<kModeStep, kWBf16>::kThreads, 1, 1);
+  cfg.blockDim = dim3(KCfg<kModeStep, kWBf16, SDT>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -44,11 +45,11 @@ int step_max_pairs(int sdt) {
 
 cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
-                           const CUtensorMap& s2, const CUtensorMap& dx, const GemmParams& p,
-                           int grid, cudaStream_t s) {
-  return sdt == kSInt8   ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, p, grid, s)
-         : sdt == kSBf16 ? run_step<kSBf16>(a, b, da, db, s1, s2, dx, p, grid, s)
-                         : run_step<kSFp32>(a, b, da, db, s1, s2, dx, p, grid, s);
+                           const CUtensorMap& s2, const CUtensorMap& dx, const CUtensorMap& w,
+                           const GemmParams& p, int grid, cudaStream_t s) {
+  return sdt == kSInt8   ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+         : sdt == kSBf16 ? run_step<kSBf16>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+                         : run_step<kSFp32>(a, b, da, db, s1, s2, dx, w, p, grid, s);
 }
 
 }  // namespace forge
