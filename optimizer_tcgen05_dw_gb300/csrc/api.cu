@@ -68,7 +68,7 @@ struct DeviceInfo {
   uint32_t* status = nullptr;
   uint32_t* dx_done = nullptr;
   uint32_t* static_scratch = nullptr;  // g_static_scratch on this device
-  int step_pairs[3] = {0, 0, 0};  // resident one-launch-step pairs, by state dtype
+  int step_pairs[4] = {0, 0, 0, 0};  // resident one-launch-step pairs, by kernel state dtype
   int cc_major = 0, cc_minor = 0;
 };
 
@@ -102,6 +102,7 @@ forge_status_t device_info(DeviceInfo* out) {
       d.step_pairs[kSFp32] = step_max_pairs(kSFp32);
       d.step_pairs[kSInt8] = step_max_pairs(kSInt8);
       d.step_pairs[kSBf16] = step_max_pairs(kSBf16);
+      d.step_pairs[kSInt8W] = step_max_pairs(kSInt8W);
     }
     g_dev[dev] = d;
     g_dev_ready[dev] = true;
@@ -232,13 +233,21 @@ forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t 
   return FORGE_OK;
 }
 
-// The bf16 weights in 64-column x 128-row boxes (128-byte swizzle): the
-// epilogue stages them with INT8 states.  Otherwise a copy of `other` (unused).
-forge_status_t weight_map(const forge_state_t* st, int64_t N, int64_t K, const CUtensorMap& other,
+// The state dtype the tensor-core kernel is instantiated for: INT8 states
+// over a short reduction (T <= kStageWeightsMaxT) with bf16 weights take the
+// epilogue that stages the weights too.
+int kernel_sdt(const forge_state_t* st, int64_t T) {
+  if (st->s_dtype == FORGE_STATE_INT8_B64 && st->w_dtype == FORGE_W_BF16_SR && T <= kStageWeightsMaxT)
+    return kSInt8W;
+  return st->s_dtype;
+}
+
+// The bf16 weights in 64-column x 128-row boxes (128-byte swizzle), for the
+// kSInt8W epilogue.  Otherwise a copy of `other` (unused).
+forge_status_t weight_map(const forge_state_t* st, int sdt, int64_t N, int64_t K, const CUtensorMap& other,
                           CUtensorMap* mw) {
   *mw = other;
-  if (st->w_dtype == FORGE_W_BF16_SR && st->s_dtype == FORGE_STATE_INT8_B64)
-    return bf16_map(mw, st->W, K, N, 64, kTileM);
+  if (sdt == kSInt8W) return bf16_map(mw, st->W, K, N, 64, kTileM);
   return FORGE_OK;
 }
 
@@ -469,7 +478,8 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   if ((st = mn_major_3d_map(&mdb, state->W, K, N, kFusedBlockK, kTileN / 2 / 64)) != FORGE_OK) return st;
   if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
   if ((st = bf16_map(&mdx, lin->dX, K, T, 64, kTileM)) != FORGE_OK) return st;
-  if ((st = weight_map(state, N, K, ma, &mw)) != FORGE_OK) return st;
+  const int sdt = kernel_sdt(state, T);
+  if ((st = weight_map(state, sdt, N, K, ma, &mw)) != FORGE_OK) return st;
   fill_tiles(p, N, K, T, kFusedBlockK);
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
@@ -490,9 +500,9 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
     return cuda_fail(e, "clearing the dX counters");
   // Every pair must be resident at once (dW tiles wait for other pairs' dX
   // tiles): at most the occupancy limit, at most one pair per tile.
-  const int pairs = std::min(std::min(d.num_sms / 2, d.step_pairs[state->s_dtype]), p.num_tiles + p.dx_tiles);
+  const int pairs = std::min(std::min(d.num_sms / 2, d.step_pairs[sdt]), p.num_tiles + p.dx_tiles);
   balance_dx(p, pairs, T, N);
-  if ((e = launch_tc_step(state->s_dtype, ma, mb, mda, mdb, m1, m2, mdx, mw, p, 2 * pairs, s)) !=
+  if ((e = launch_tc_step(sdt, ma, mb, mda, mdb, m1, m2, mdx, mw, p, 2 * pairs, s)) !=
       cudaSuccess)
     return cuda_fail(e, "one-launch step");
   return FORGE_OK;
@@ -532,7 +542,7 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   // weights.
   if (lin->dX != nullptr && lin->T > 0 && state->w_dtype == FORGE_W_BF16_SR && lin->N % 64 == 0 &&
       lin->K % 64 == 0 && (lin->K + kTileN - 1) / kTileN <= kMaxDxBlocks && g_step_fusion.load() &&
-      d.step_pairs[state->s_dtype] > 0)
+      d.step_pairs[kernel_sdt(state, lin->T)] > 0)
     return launch_step(lin, state, opt_kind, sc, step, seed, s, d);
   // 1. dX from the pre-update weights, enqueued first on the same stream.
   if (lin->dX != nullptr && (st = launch_dgrad(lin, state->W, state->w_dtype, s, d)) != FORGE_OK) return st;
@@ -566,9 +576,10 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   CUtensorMap m1 = ma, m2 = ma, mw = ma;
   if (state->w_dtype == FORGE_W_BF16_SR &&
       ((st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK ||
-       (st = weight_map(state, lin->N, lin->K, ma, &mw)) != FORGE_OK))
+       (st = weight_map(state, kernel_sdt(state, lin->T), lin->N, lin->K, ma, &mw)) != FORGE_OK))
     return st;
-  if ((e = launch_tc_fused(state->w_dtype, state->s_dtype, ma, mb, m1, m2, mw, p, grid_for(p, d), s)) !=
+  if ((e = launch_tc_fused(state->w_dtype, kernel_sdt(state, lin->T), ma, mb, m1, m2, mw, p, grid_for(p, d),
+                           s)) !=
       cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
@@ -593,7 +604,7 @@ forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const for
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
   if ((st = check_device(d)) != FORGE_OK) return st;
-  if (d.step_pairs[state->s_dtype] <= 0)
+  if (d.step_pairs[kernel_sdt(state, lin->T)] <= 0)
     return fail(FORGE_ERR_UNSUPPORTED, "the one-launch step cannot be resident on this device");
   return launch_step(lin, state, opt_kind, make_scalars(opt_kind, *hp, step), step, seed,
                      static_cast<cudaStream_t>(stream), d, d.static_scratch);
@@ -653,7 +664,8 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FORGE_OK)
     return st;
   if ((st = state_maps(state, opt_kind, N, K, ma, &m1, &m2)) != FORGE_OK) return st;
-  if ((st = weight_map(state, N, K, ma, &mw)) != FORGE_OK) return st;
+  const int sdt = kernel_sdt(state, T);
+  if ((st = weight_map(state, sdt, N, K, ma, &mw)) != FORGE_OK) return st;
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   fill_tiles(p, N, K, T, kFp8BlockK);
@@ -666,7 +678,7 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
   p.gscale = static_cast<float>(c);
-  if ((e = launch_tc_fp8(state->s_dtype, ma, mb, m1, m2, mw, p, grid_for(p, d), s)) != cudaSuccess)
+  if ((e = launch_tc_fp8(sdt, ma, mb, m1, m2, mw, p, grid_for(p, d), s)) != cudaSuccess)
     return cuda_fail(e, "FP8 step launch");
   return FORGE_OK;
 }

@@ -11,7 +11,15 @@ enum OptKind : int32_t {
   kRMSprop = 4, kAdaGrad = 5, kSGD = 6, kSGDMomentum = 7
 };
 enum WDtype : int32_t { kWFp32 = 0, kWBf16 = 1 };
-enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1, kSBf16 = 2 };
+enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1, kSBf16 = 2,
+                        // INT8 states with the bf16 weights staged through shared
+                        // memory by TMA (kernel-side only; the host picks it for
+                        // short reductions, T <= kStageWeightsMaxT)
+                        kSInt8W = 3 };
+// Longest reduction for which the INT8 epilogue stages the weights: it frees
+// the compute warps from row-strided weight accesses (+40 % at T = 4096) but
+// costs an operand stage, which a long main loop needs (-5 % at T = 16384).
+constexpr int64_t kStageWeightsMaxT = 8192;
 
 // Device-side status codes (values match forge_status_t).
 enum DeviceStatus : uint32_t { kStatusOk = 0, kStatusTimeout = 4 };

@@ -27,7 +27,7 @@ struct ElemParams {
 // s1, s2: tensor maps of the state tiles the bf16-weight epilogue stages
 // through shared memory (unused, any valid map, for fp32 weights or for
 // states the rule does not keep); w: bf16 W in 64-column x 128-row boxes
-// (128-byte swizzle), staged with INT8 states (else any valid map).
+// (128-byte swizzle), staged when sdt is kSInt8W (else any valid map).
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
                             const CUtensorMap& s1, const CUtensorMap& s2, const CUtensorMap& w,
                             const GemmParams& p, int grid, cudaStream_t s);

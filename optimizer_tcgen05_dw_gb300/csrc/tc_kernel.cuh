@@ -77,7 +77,7 @@ constexpr int kEpiBufBytes = 32768;
 // INT8 states stage the bf16 weight chunk too (see StagedGeom): a larger
 // buffer, and one operand stage fewer to make room.
 constexpr int kEpiBufBytesW = 37888;
-__host__ __device__ constexpr bool stages_weights(int sdt) { return sdt == kSInt8; }
+__host__ __device__ constexpr bool stages_weights(int sdt) { return sdt == kSInt8W; }
 constexpr int kEpiBarrier = 1;       // named barrier of the epilogue warps
 constexpr int kEpiInnerBarrier = 2;  // the staged epilogue's compute warps only
 constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
@@ -112,8 +112,8 @@ static_assert(KCfg<kModeWgradStore, kWBf16>::kSmem <= 232448, "dynamic shared me
 static_assert(KCfg<kModeFusedOpt, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeDgrad, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeFusedFp8, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
-static_assert(KCfg<kModeStep, kWBf16, kSInt8>::kSmem <= 232448, "dynamic shared memory limit");
-static_assert(KCfg<kModeFusedFp8, kWBf16, kSInt8>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeStep, kWBf16, kSInt8W>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeFusedFp8, kWBf16, kSInt8W>::kSmem <= 232448, "dynamic shared memory limit");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -879,7 +879,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 template <int KIND, int SDT>
 struct StagedGeom {
   static constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
-  static constexpr bool I8 = (SDT == kSInt8);
+  static constexpr bool I8 = (SDT == kSInt8 || SDT == kSInt8W);
   static constexpr bool BF = (SDT == kSBf16);
   static constexpr int kCC = I8 ? 64 : 32;
   static constexpr int kChunks = kTileN / kCC;
@@ -888,9 +888,9 @@ struct StagedGeom {
   static constexpr uint32_t kStateBytes = (I8 || BF) ? 8192u : 16384u;
   static constexpr uint32_t kTx = (U1 ? kStateBytes : 0u) + (U2 ? kStateBytes : 0u);
   static constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
-  // INT8: the chunk's bf16 weights (128 rows x 128 bytes, 128-byte swizzle)
-  // are staged by TMA as well, and the old scales of the next chunk are
-  // handed from the quarter that loads them to the other three.
+  // kSInt8W: the chunk's bf16 weights (128 rows x 128 bytes, 128-byte
+  // swizzle) are staged by TMA as well, and the old scales of the next chunk
+  // are handed from the quarter that loads them to the other three.
   static constexpr bool WST = stages_weights(SDT);
   static constexpr int kOffAmax = 16384, kOffOld = 20480, kOffW = 21504;
   static constexpr int kBuf = WST ? kEpiBufBytesW : kEpiBufBytes;

@@ -386,3 +386,20 @@ def test_int8_requantisation_ties_and_zero_blocks_bitexact():
     codes = ref["s1"].astype(np.int64)
     assert (codes[0, 1:64] % 2 == 0).all() and np.abs(codes[0, 1:64]).max() > 60  # ties went to even
     assert (ref["s1_scale"][1::3] == 0).all() and (codes[1::3] == 0).all()          # zero blocks
+
+
+@pytest.mark.parametrize("T", [8192, 8208], ids=["staged_weights", "direct_weights"])
+@pytest.mark.parametrize("dx", [False, True], ids=["fused", "one_launch"])
+def test_int8_epilogue_variants_bitexact(T, dx):
+    """INT8 states take one of two epilogues by token count: up to 8192
+    tokens the bf16 weights are staged through shared memory with the codes,
+    beyond it they are read and written by the compute warps directly.  Both
+    sides of the switch match the oracle bit for bit (integer grid), with and
+    without dX in the same launch."""
+    prob = Problem(T=T, N=256, K=320, w_dtype="bf16", s_dtype="int8", opt_name="adamw",
+                   hp=_hp("adamw"), grid=True, steps=2, seed=41)
+    gpu, gdx = prob.run_gpu(fused=True, want_dx=dx)
+    ref, _, _ = prob.run_oracle(want_dx=dx)
+    _compare_exact(prob, gpu, ref)
+    if dx:
+        assert_dx_close(gdx[0], to_bits(prob.dY[0]), ls.weights_for_dx(prob.state0["W"], "bf16"), "dX")
