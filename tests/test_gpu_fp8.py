@@ -224,3 +224,21 @@ def _check_rows(sub, rows, K, kind, hp, g, delta, st):
     fp32 = [{k: (None if f0[k] is None else np.concatenate([o[1][j][k] for o in outs_rows]))
              for k in f0} for j, f0 in enumerate(outs_rows[0][1])]
     assert_in_interval(sub, (outs, fp32), "bf16", "int8", "q_proj fp8 sampled rows")
+
+
+@pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
+def test_fp8_nan_codes_propagate(s_dtype):
+    """E4M3 has no infinity; its NaN codes (0x7F, 0xFF) make the columns they
+    sit in NaN in the gradient, and the updated weights there NaN (0x7FC0),
+    exactly as the oracle's decoding does."""
+    prob = Problem(**GRID, w_dtype="bf16", s_dtype=s_dtype, opt_name="adamw", hp=_hp("adamw"),
+                   steps=1, seed=27)
+    xts, dyts = _grid_inputs(GRID["T"], GRID["N"], GRID["K"], 1, 27)
+    xt = xts[0].clone()
+    xt[10, 3] = 0x7F
+    xt[300, 100] = 0xFF
+    xts = [xt]
+    gpu = _run_fp8(prob, xts, dyts, 2.0 ** -3, 2.0 ** -12)
+    ref = _oracle_fp8(prob, xts, dyts, 2.0 ** -3, 2.0 ** -12)
+    _compare_exact(gpu, ref)
+    assert (ref["W"][:, 10] == 0x7FC0).all() and (ref["W"][:, 300] == 0x7FC0).all()

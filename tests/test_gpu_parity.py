@@ -403,3 +403,27 @@ def test_int8_epilogue_variants_bitexact(T, dx):
     _compare_exact(prob, gpu, ref)
     if dx:
         assert_dx_close(gdx[0], to_bits(prob.dY[0]), ls.weights_for_dx(prob.state0["W"], "bf16"), "dX")
+
+
+@pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
+@pytest.mark.parametrize("opt_name", ["adamw", "sgd_momentum"])
+def test_nonfinite_activations_match_oracle(opt_name, s_dtype):
+    """NaN and +-Inf in X (integer grid elsewhere) reach the gradient through
+    the tensor-core sums (Inf * 0 and Inf - Inf are NaN, in any order), then
+    the rule: weights become NaN (stored as 0x7FC0), fp32 moments NaN or Inf,
+    INT8 blocks take an infinite absmax and zero codes for NaN.  Weights and
+    states match the oracle bit for bit (NaN equal to NaN)."""
+    prob = Problem(T=200, N=320, K=384, w_dtype="bf16", s_dtype=s_dtype, opt_name=opt_name,
+                   hp=_hp(opt_name), grid=True, steps=1, seed=43)
+    x = prob.X[0].float().numpy().copy()
+    x[3, 5] = np.nan
+    x[7, 70] = np.inf
+    x[9, 200] = -np.inf
+    x[11, 200] = np.inf  # +Inf and -Inf in one column: NaN wherever both dY are nonzero
+    prob.X[0] = torch.from_numpy(x).to(torch.bfloat16)
+    gpu, gdx = prob.run_gpu(fused=True, want_dx=True)
+    ref, _, _ = prob.run_oracle(want_dx=False)
+    _compare_exact(prob, gpu, ref)
+    assert (ref["W"][:, 5] == 0x7FC0).all() and (ref["W"][:, 200] == 0x7FC0).any()
+    # dX = dY W does not read X: finite, within the usual dX tolerance
+    assert_dx_close(gdx[0], to_bits(prob.dY[0]), ls.weights_for_dx(prob.state0["W"], "bf16"), "dX")
