@@ -384,6 +384,19 @@ void fill_tiles(GemmParams& p, int64_t M, int64_t Ncols, int64_t red, int bk = k
   p.tiles_m = static_cast<int32_t>((M + 2 * kTileM - 1) / (2 * kTileM));  // 256-row pair tiles
   p.tiles_n = static_cast<int32_t>((Ncols + kTileN - 1) / kTileN);
   p.num_tiles = p.tiles_m * p.tiles_n;
+  p.num_units = p.num_tiles;
+  p.split_from = p.num_tiles;
+}
+
+// A last partial wave of pair tiles (R = num_tiles % pairs of them) runs as
+// 2R column halves when they fit one wave, so that it takes half as long.
+// Only for the staged epilogue without dX tiles.
+void split_tail(GemmParams& p, int pairs) {
+  const int F = p.num_tiles, R = F % pairs;
+  if (F > pairs && R > 0 && 2 * R <= pairs) {
+    p.split_from = F - R;
+    p.num_units = F + R;
+  }
 }
 
 // Clusters of two CTAs, at most one CTA per SM.
@@ -573,13 +586,18 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
-  CUtensorMap m1 = ma, m2 = ma, mw = ma;
-  if (state->w_dtype == FORGE_W_BF16_SR &&
-      ((st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK ||
-       (st = weight_map(state, kernel_sdt(state, lin->T), lin->N, lin->K, ma, &mw)) != FORGE_OK))
-    return st;
-  if ((e = launch_tc_fused(state->w_dtype, kernel_sdt(state, lin->T), ma, mb, m1, m2, mw, p, grid_for(p, d),
-                           s)) !=
+  CUtensorMap m1 = ma, m2 = ma, mw = ma, mbh = mb;
+  if (state->w_dtype == FORGE_W_BF16_SR) {
+    if ((st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK ||
+        (st = weight_map(state, kernel_sdt(state, lin->T), lin->N, lin->K, ma, &mw)) != FORGE_OK)
+      return st;
+    split_tail(p, d.num_sms / 2);
+    if (p.split_from < p.num_tiles && p.op3d &&  // half units load one 64-column block of X
+        (st = mn_major_3d_map(&mbh, lin->X, lin->K, lin->T, bk, 1)) != FORGE_OK)
+      return st;
+  }
+  if ((e = launch_tc_fused(state->w_dtype, kernel_sdt(state, lin->T), ma, mb, mbh, m1, m2, mw, p,
+                           grid_for(p, d), s)) !=
       cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
@@ -669,6 +687,12 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   fill_tiles(p, N, K, T, kFp8BlockK);
+  split_tail(p, d.num_sms / 2);
+  CUtensorMap mbh = mb;
+  if (p.split_from < p.num_tiles &&  // half units load 64 rows of X^T
+      (st = tensor_map(&mbh, lin->Xt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, T, K, kFp8BlockK, kTileN / 4,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FORGE_OK)
+    return st;
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
@@ -678,7 +702,7 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
   p.gscale = static_cast<float>(c);
-  if ((e = launch_tc_fp8(sdt, ma, mb, m1, m2, mw, p, grid_for(p, d), s)) != cudaSuccess)
+  if ((e = launch_tc_fp8(sdt, ma, mb, mbh, m1, m2, mw, p, grid_for(p, d), s)) != cudaSuccess)
     return cuda_fail(e, "FP8 step launch");
   return FORGE_OK;
 }

@@ -99,6 +99,11 @@ struct GemmParams {
   int32_t M, Ncols;
   int32_t num_kb;            // reduction blocks of 64
   int32_t tiles_m, tiles_n, num_tiles;
+  // Work units of the weight tiles: tiles 0 .. split_from-1 whole, then each
+  // remaining tile as two 128-column halves (units split_from ..
+  // num_units-1), so that a last partial wave of pair tiles becomes half as
+  // long.  split_from == num_tiles == num_units when nothing is split.
+  int32_t num_units, split_from;
   void* out;                 // wgrad store: fp32 [M x Ncols]; dgrad: bf16 [M x Ncols]
   void* W;                   // fused: [M x Ncols] fp32 or bf16
   void* s1;

@@ -27,10 +27,12 @@ struct ElemParams {
 // s1, s2: tensor maps of the state tiles the bf16-weight epilogue stages
 // through shared memory (unused, any valid map, for fp32 weights or for
 // states the rule does not keep); w: bf16 W in 64-column x 128-row boxes
-// (128-byte swizzle), staged when sdt is kSInt8W (else any valid map).
+// (128-byte swizzle), staged when sdt is kSInt8W (else any valid map); bh:
+// the B operand in 64-column boxes for half units (GemmParams::split_from;
+// any valid map when nothing is split).
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
-                            const CUtensorMap& s1, const CUtensorMap& s2, const CUtensorMap& w,
-                            const GemmParams& p, int grid, cudaStream_t s);
+                            const CUtensorMap& bh, const CUtensorMap& s1, const CUtensorMap& s2,
+                            const CUtensorMap& w, const GemmParams& p, int grid, cudaStream_t s);
 // tc_step.cu: dX and the FORGE step in one launch (mode kModeStep, bf16
 // weights): a, b the dW operands, da, db the dX operands (dY K-major, W),
 // dx the dX output (bf16, 64-column x 128-row boxes, 128-byte swizzle).
@@ -45,9 +47,9 @@ int step_max_pairs(int sdt);
 // tc_fp8.cu: the FORGE step from E4M3 operands (mode kModeFusedFp8, bf16
 // weights): a = dY^T codes [N x T], b = X^T codes [K x T], 128 x 128-byte
 // boxes with the 128-byte swizzle; p.gscale the product of the scales.
-cudaError_t launch_tc_fp8(int sdt, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& s1,
-                          const CUtensorMap& s2, const CUtensorMap& w, const GemmParams& p, int grid,
-                          cudaStream_t s);
+cudaError_t launch_tc_fp8(int sdt, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& bh,
+                          const CUtensorMap& s1, const CUtensorMap& s2, const CUtensorMap& w,
+                          const GemmParams& p, int grid, cudaStream_t s);
 // tc_plain.cu: unfused pass 1 (kModeWgradStore) or dX (kModeDgrad).
 cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b,
                             const GemmParams& p, int grid, cudaStream_t s);

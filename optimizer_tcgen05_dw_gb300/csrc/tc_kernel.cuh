@@ -151,6 +151,14 @@ __device__ __forceinline__ void tile_coords(int tile, const GemmParams& p, int& 
   tile_coords_of(tile, p.tiles_m, p.tiles_n, tm, tn);
 }
 
+// Unit u of the weight tiles (see GemmParams::split_from): its tile and, for
+// a half unit, which 128-column half (0 or 1); -1 for a whole tile.
+__device__ __forceinline__ void unit_coords(int u, const GemmParams& p, int& tm, int& tn, int& half) {
+  const bool split = u >= p.split_from;
+  half = split ? ((u - p.split_from) & 1) : -1;
+  tile_coords(split ? p.split_from + ((u - p.split_from) >> 1) : u, p, tm, tn);
+}
+
 // ------------------------------------------------------------------ roles
 
 // Tile index of the pair's i-th tile, and the CTA's rank in the pair.
@@ -210,22 +218,26 @@ __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, cons
         }
       }
     }
-    for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs()) {
-      int tm, tn;
-      tile_coords(tile, p, tm, tn);
-      const int m0 = tm * kPairM + static_cast<int>(rank) * kTileM;      // this CTA's A rows
-      const int n0 = tn * kTileN + static_cast<int>(rank) * (kTileN / 2);  // this CTA's B columns
+    for (int u = pair_id(); u < p.num_units; u += num_pairs()) {
+      int tm, tn, half;
+      unit_coords(u, p, tm, tn, half);
+      const int m0 = tm * kPairM + static_cast<int>(rank) * kTileM;  // this CTA's A rows
+      // this CTA's B columns: 128 of a whole tile, 64 of a half unit (whose B
+      // boxes come from the half-width map, passed as mDB)
+      const int n0 = half < 0 ? tn * kTileN + static_cast<int>(rank) * (kTileN / 2)
+                              : tn * kTileN + half * (kTileN / 2) + static_cast<int>(rank) * (kTileN / 4);
+      const uint32_t bytes = half < 0 ? 2u * (kA + kB) : 2u * (kA + kB / 2);
       for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
         const int s = static_cast<int>(it % STG);
         const uint32_t ph = (it / STG) & 1u;
         if (!bounded_wait(&ss->empty[s], ph ^ 1u, p, ss)) goto drain;
         const uint32_t bar = full0 + static_cast<uint32_t>(s) * 8u;
-        if (rank == 0) ptx::mbar_arrive_expect_tx(&ss->full[s], 2u * (kA + kB));
+        if (rank == 0) ptx::mbar_arrive_expect_tx(&ss->full[s], bytes);
         uint8_t* a = smA + s * kA;
         uint8_t* b = smB + s * kB;
         if (MODE == kModeFusedFp8) {  // dY^T and X^T, token-contiguous: one 128 x 128-byte box each
           ptx::tma_load_2d_pair(mA, bar, a, kb * BK, m0);
-          ptx::tma_load_2d_pair(mB, bar, b, kb * BK, n0);
+          ptx::tma_load_2d_pair(half < 0 ? mB : mDB, bar, b, kb * BK, n0);
           issued_mask |= 1u << s;
           last_parity = (last_parity & ~(1u << s)) | (ph << s);
           continue;
@@ -239,10 +251,10 @@ __device__ void producer_role(const CUtensorMap* mA, const CUtensorMap* mB, cons
           ptx::tma_load_2d_pair(mA, bar, a + 64 * BK * 2, m0 + 64, kb * BK);
         }
         if (p.op3d) {
-          ptx::tma_load_3d_pair(mB, bar, b, 0, kb * BK, n0 / 64);
+          ptx::tma_load_3d_pair(half < 0 ? mB : mDB, bar, b, 0, kb * BK, n0 / 64);
         } else {
           ptx::tma_load_2d_pair(mB, bar, b, n0, kb * BK);
-          ptx::tma_load_2d_pair(mB, bar, b + 64 * BK * 2, n0 + 64, kb * BK);
+          if (half < 0) ptx::tma_load_2d_pair(mB, bar, b + 64 * BK * 2, n0 + 64, kb * BK);
         }
         issued_mask |= 1u << s;
         last_parity = (last_parity & ~(1u << s)) | (ph << s);
@@ -268,14 +280,14 @@ __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, Shared
   int local = 0;
   // One tile into accumulator local & 1: num_kb stages; A K-major (dX: dY) or
   // MN-major (dW: dY^T); B MN-major.  False if the CTA is aborting.
-  auto run_tile = [&](int num_kb, bool a_kmajor) -> bool {
+  auto run_tile = [&](int num_kb, bool a_kmajor, int n_cols) -> bool {
     const int acc = local & 1;
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
     if (!bounded_wait(&ss->tmem_empty[acc], aph ^ 1u, p, ss)) return false;
     ptx::tc_fence_after();
-    const uint32_t idesc = kFp8       ? ptx::idesc_e4m3_f32(kPairM, kTileN)
-                           : a_kmajor ? ptx::idesc_bf16_f32(kPairM, kTileN, false, true)
-                                      : ptx::idesc_bf16_f32(kPairM, kTileN, true, true);
+    const uint32_t idesc = kFp8       ? ptx::idesc_e4m3_f32(kPairM, n_cols)
+                           : a_kmajor ? ptx::idesc_bf16_f32(kPairM, n_cols, false, true)
+                                      : ptx::idesc_bf16_f32(kPairM, n_cols, true, true);
     const uint32_t d_tmem = ss->tmem_base + static_cast<uint32_t>(acc * kTileN);
     for (int kb = 0; kb < num_kb; ++kb, ++it) {
       const int s = static_cast<int>(it % STG);
@@ -314,10 +326,10 @@ __device__ void mma_role(const GemmParams& p, uint8_t* smA, uint8_t* smB, Shared
   if (MODE == kModeStep) {
     const int ndx = my_dx_tiles(p);
     for (int i = 0; i < ndx; ++i)
-      if (!run_tile(p.dx_num_kb, true)) goto done;
+      if (!run_tile(p.dx_num_kb, true, kTileN)) goto done;
   }
-  for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs())
-    if (!run_tile(p.num_kb, MODE == kModeDgrad)) goto done;
+  for (int u = pair_id(); u < p.num_units; u += num_pairs())  // a half unit: N = 128
+    if (!run_tile(p.num_kb, MODE == kModeDgrad, u < p.split_from ? kTileN : kTileN / 2)) goto done;
 done:
   // Tensor memory may be released only after every issued MMA has finished.
   ptx::mma_commit_pair_multicast(&ss->mma_done, 0x1);
@@ -903,19 +915,24 @@ struct StagedGeom {
 // row and first column.  The origins of the tile in hand and of the next one
 // are kept, found once per tile (tile_coords divides): chunk j and the chunk
 // j + 1 prefetched ahead of it always lie in one of the two.
+// Units are whole tiles (kChunks chunks) or, for a pair's last unit only,
+// 128-column halves (kChunks / 2 chunks): chunk j belongs to unit j / kChunks,
+// and `total` counts the pair's chunks.
 template <int kChunks>
 struct TileWalk {
   int cur_tile = 0, cur_row0 = 0, cur_col0 = 0, nxt_row0 = 0, nxt_col0 = 0;
-  int my_tiles = 0;
+  int my_tiles = 0, total = 0;
   __device__ __forceinline__ void origin(int i, const GemmParams& p, uint32_t rank, int& row0,
                                          int& col0) const {
-    int tm, tn;
-    tile_coords(pair_id() + i * num_pairs(), p, tm, tn);
+    int tm, tn, half;
+    unit_coords(pair_id() + i * num_pairs(), p, tm, tn, half);
     row0 = tm * kPairM + static_cast<int>(rank) * kTileM;
-    col0 = tn * kTileN;
+    col0 = tn * kTileN + (half > 0 ? kTileN / 2 : 0);
   }
   __device__ __forceinline__ void init(const GemmParams& p, uint32_t rank) {
-    my_tiles = p.num_tiles > pair_id() ? (p.num_tiles - 1 - pair_id()) / num_pairs() + 1 : 0;
+    my_tiles = p.num_units > pair_id() ? (p.num_units - 1 - pair_id()) / num_pairs() + 1 : 0;
+    total = my_tiles * kChunks;
+    if (my_tiles > 0 && pair_id() + (my_tiles - 1) * num_pairs() >= p.split_from) total -= kChunks / 2;
     if (my_tiles > 0) origin(0, p, rank, cur_row0, cur_col0);
     if (my_tiles > 1) origin(1, p, rank, nxt_row0, nxt_col0);
   }
@@ -993,7 +1010,7 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
   constexpr bool STEP = MODE == kModeStep;
   TileWalk<G::kChunks> walk;
   walk.init(p, rank);
-  const int total = walk.my_tiles * G::kChunks;
+  const int total = walk.total;
   const bool io = (lane == 0);
   // Weight/state lines are touched once per step: evict-first in L2, so they
   // do not displace the operand tiles the main loop re-reads from L2.
@@ -1116,7 +1133,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   const int64_t K = p.Ncols;
   TileWalk<kChunks> walk;
   walk.init(p, rank);
-  const int total = walk.my_tiles * kChunks;
+  const int total = walk.total;
   const uint32_t empty0 = ptx::mapa(ptx::smem_addr(&ss->tmem_empty[0]), 0);
 
   // This thread's weights of chunk j (and, for INT8 states, the old absmax of
@@ -1232,15 +1249,16 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
     }
-    if (c == kChunks - 1) ptx::tc_fence_before();
-    ptx::fence_proxy_async_smem();
     const bool more = j + 1 < total;
-    if (more && c != kChunks - 1) {  // end of chunk j = start of chunk j + 1 (same tile)
+    const bool unit_end = !more || c == kChunks - 1;  // the unit's accumulator is read out
+    if (unit_end) ptx::tc_fence_before();
+    ptx::fence_proxy_async_smem();
+    if (!unit_end) {  // end of chunk j = start of chunk j + 1 (same unit)
       begin(j + 1);
       stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);
     } else {
       ptx::bar_sync(kEpiBarrier, G::kNB);
-      if (c == kChunks - 1 && lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
+      if (lane == 0) ptx::mbar_arrive_cluster(empty0 + static_cast<uint32_t>(acc) * 8u);
       if (more) {
         begin(j + 1);
         stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);

@@ -242,3 +242,15 @@ def test_fp8_nan_codes_propagate(s_dtype):
     ref = _oracle_fp8(prob, xts, dyts, 2.0 ** -3, 2.0 ** -12)
     _compare_exact(gpu, ref)
     assert (ref["W"][:, 10] == 0x7FC0).all() and (ref["W"][:, 300] == 0x7FC0).all()
+
+
+@pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
+def test_fp8_split_last_wave_bitexact(s_dtype):
+    """80 pair tiles on 76 pairs: the last partial wave runs as 128-column
+    halves (64-row boxes of X^T); bit-exact against the oracle."""
+    T, N, K = 160, 2560, 2048
+    prob = Problem(T=16, N=N, K=K, w_dtype="bf16", s_dtype=s_dtype, opt_name="adamw", hp=_hp("adamw"),
+                   steps=1, seed=28)
+    xts, dyts = _grid_inputs(T, N, K, 1, 28)
+    gpu = _run_fp8(prob, xts, dyts, 2.0 ** -3, 2.0 ** -12)
+    _compare_exact(gpu, _oracle_fp8(prob, xts, dyts, 2.0 ** -3, 2.0 ** -12))

@@ -427,3 +427,19 @@ def test_nonfinite_activations_match_oracle(opt_name, s_dtype):
     assert (ref["W"][:, 5] == 0x7FC0).all() and (ref["W"][:, 200] == 0x7FC0).any()
     # dX = dY W does not read X: finite, within the usual dX tolerance
     assert_dx_close(gdx[0], to_bits(prob.dY[0]), ls.weights_for_dx(prob.state0["W"], "bf16"), "dX")
+
+
+@pytest.mark.parametrize("shape", [dict(T=208, N=2560, K=2048), dict(T=144, N=2568, K=2048)],
+                         ids=["aligned", "ragged_rows"])
+@pytest.mark.parametrize("opt_name,s_dtype", [("adamw", "fp32"), ("adamw", "int8"), ("lion", "bf16"),
+                                              ("sgd_momentum", "fp32")])
+def test_split_last_wave_bitexact(shape, opt_name, s_dtype):
+    """More pair tiles than CTA pairs with a short last wave (80 or 88 tiles
+    on 76 pairs): the last partial wave runs as 128-column half tiles (N = 128
+    MMAs, half-width operand boxes).  Every element still matches the oracle
+    bit for bit, in the split tiles as elsewhere."""
+    prob = Problem(**shape, w_dtype="bf16", s_dtype=s_dtype, opt_name=opt_name, hp=_hp(opt_name),
+                   grid=True, steps=2, seed=47)
+    gpu, _ = prob.run_gpu(fused=True)
+    ref, _, _ = prob.run_oracle()
+    _compare_exact(prob, gpu, ref)
