@@ -28,8 +28,13 @@
 //               Plain modes and fp32 weights: warps 2..9 (direct stores).
 //               The FORGE step with bf16 weights: warps 2..17 compute, warp
 //               18 stages the optimizer states through shared memory with
-//               TMA (and, in the one-launch step, stores the dX tiles that
+//               TMA (with INT8 states over a short reduction, the weights
+//               too; in the one-launch step it also stores the dX tiles that
 //               run first in the same launch).
+// Work units: whole tiles, except that in the FORGE step without dX a last
+// partial wave (fewer tiles than half the pairs) runs as 128-column halves
+// (N = 128 MMAs, half-width B boxes), each pair taking at most one as its
+// last unit, so that wave takes half as long.
 // Operand layouts (all 128-byte swizzled atoms of 8 rows x 128 bytes):
 //   wgrad  A = dY^T tile [128 n x BK t] per CTA: dY is [T x N] with n
 //          contiguous, so A is MN-major: two 64-wide column atoms BK*128
