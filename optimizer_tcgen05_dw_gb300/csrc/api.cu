@@ -251,6 +251,18 @@ forge_status_t weight_map(const forge_state_t* st, int sdt, int64_t N, int64_t K
   return FORGE_OK;
 }
 
+// Philox4x32-10 round keys of `seed`: the key, bumped by the Weyl constants
+// before each round after the first.
+void philox_round_keys(uint64_t seed, uint32_t* rk) {
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    rk[2 * r] = k0;
+    rk[2 * r + 1] = k1;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+}
+
 // ---------------------------------------------------------------- scalars
 
 // Per-step scalars of each rule, in double from the float hyper-parameters,
@@ -498,6 +510,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
   p.seed = seed;
+  philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
@@ -582,6 +595,7 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
   p.seed = seed;
+  philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
@@ -697,6 +711,7 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
   p.seed = seed;
+  philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();

@@ -113,6 +113,9 @@ struct GemmParams {
   OptScalars sc;
   uint64_t seed;
   uint64_t step;
+  // Philox4x32-10 round keys of `seed` (key words 0 and 1 of rounds 0..9),
+  // formed once on the host for the stochastic rounding of the weights.
+  uint32_t round_keys[20];
   uint64_t wait_limit_ns;
   uint32_t* status;          // device status word (first error wins)
   int32_t op3d;              // MN-major operands described as 3-D maps: one load per stage

@@ -121,6 +121,21 @@ __device__ __forceinline__ uint4 sr_words(uint64_t grp, uint64_t seed, uint64_t 
   return philox4x32_10(ctr, static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
 }
 
+// The same words with the ten rounds' keys formed ahead (round_keys[2r],
+// round_keys[2r + 1] = the key after r bumps), e.g. once per launch.
+__device__ __forceinline__ uint4 sr_words_rk(uint64_t grp, uint64_t step, const uint32_t* round_keys) {
+  constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  uint4 c = make_uint4(static_cast<uint32_t>(grp), static_cast<uint32_t>(grp >> 32),
+                       static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32));
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t hi0 = __umulhi(kM0, c.x), lo0 = kM0 * c.x;
+    const uint32_t hi1 = __umulhi(kM1, c.z), lo1 = kM1 * c.z;
+    c = make_uint4(hi1 ^ c.y ^ round_keys[2 * r], lo1, hi0 ^ c.w ^ round_keys[2 * r + 1], lo0);
+  }
+  return c;
+}
+
 // 16 random bits of element j (0..7) of a group.
 __device__ __forceinline__ uint32_t sr_bits(const uint4& r, int j) {
   const uint32_t w = (j >> 1) == 0 ? r.x : (j >> 1) == 1 ? r.y : (j >> 1) == 2 ? r.z : r.w;
