@@ -906,8 +906,9 @@ struct StagedGeom {
   static constexpr uint32_t kTx = (U1 ? kStateBytes : 0u) + (U2 ? kStateBytes : 0u);
   static constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
   // kSInt8W: the chunk's bf16 weights (128 rows x 128 bytes, 128-byte
-  // swizzle) are staged by TMA as well, and the old scales of the next chunk
-  // are handed from the quarter that loads them to the other three.
+  // swizzle) are staged by TMA as well.  With INT8 states the old scales of
+  // the next chunk are handed from the quarter that loads them to the other
+  // three (kOffOld, inside either buffer size).
   static constexpr bool WST = stages_weights(SDT);
   static constexpr int kOffAmax = 16384, kOffOld = 20480, kOffW = 21504;
   static constexpr int kBuf = WST ? kEpiBufBytesW : kEpiBufBytes;
@@ -1158,7 +1159,9 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
       for (int h = 0; h < kWPerThread / 8; ++h)
         v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
     }
-    if (G::I8) {  // one code block per chunk
+    // one code block per chunk; after the first chunk one quarter loads a
+    // row's old scales and hands them to the other three
+    if (G::I8 && (j == 0 || sub == 0)) {
       const bool okb = row < p.M && col0 < K;
       const int64_t sidx = row * (K / 64) + col0 / 64;
       if (G::U1) o1 = okb ? p.s1_scale[sidx] : 0.f;
@@ -1218,6 +1221,11 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     } else {
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
+      if (G::I8 && j > 0) {  // old scales from the quarter that loaded them
+        const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
+        o1 = old[r];
+        o2 = old[128 + r];
+      }
       if (j + 1 < total) prefetch(j + 1, wnext, o1next, o2next);
     }
     ptx::tc_fence_after();
@@ -1249,10 +1257,17 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
         nold[r] = o1next;
         nold[128 + r] = o2next;
       }
-    } else if (row < p.M && col < K) {
-      uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
+    } else {
+      if (G::I8 && j + 1 < total && sub == 0) {  // the next chunk's old scales, for all quarters
+        float* nold = reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffOld);
+        nold[r] = o1next;
+        nold[128 + r] = o2next;
+      }
+      if (row < p.M && col < K) {
+        uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
 #pragma unroll
-      for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
+        for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
+      }
     }
     const bool more = j + 1 < total;
     const bool unit_end = !more || c == kChunks - 1;  // the unit's accumulator is read out
