@@ -228,7 +228,9 @@ def forge_linear_bwd_step_fp8(Xt, dYt, x_scale: float, dy_scale: float, W, opt: 
     K, T = Xt.shape
     N = W.shape[0]
     for t, name, shape in ((Xt, "Xt", (K, T)), (dYt, "dYt", (N, T))):
-        _need(t, name, t.dtype if t.dtype in (torch.uint8, torch.float8_e4m3fn) else torch.uint8, shape)
+        if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError(f"{name}: expected torch.float8_e4m3fn or uint8 E4M3 codes, got {t.dtype}")
+        _need(t, name, t.dtype, shape)
     st = make_state(W, s1, s2, s1_scale, s2_scale)
     lin = ForgeLinearFp8(T, N, K, _ptr(Xt), _ptr(dYt), float(x_scale), float(dy_scale))
     _check(lib().forge_linear_bwd_step_fp8(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],

@@ -163,3 +163,12 @@ def test_fp8_step_empty_problem_is_a_no_op(L):
     hp = api.hparams()
     assert L.forge_linear_bwd_step_fp8(ctypes.byref(_lin8(N=0)), ctypes.byref(_state()), 0,
                                        ctypes.byref(hp), 1, 0, None) == 0
+
+
+def test_fp8_binding_rejects_wrong_dtypes_before_the_library():
+    import torch
+    Xt = torch.zeros((64, 32), dtype=torch.bfloat16)
+    dYt = torch.zeros((64, 32), dtype=torch.uint8)
+    W = torch.zeros((64, 64), dtype=torch.bfloat16)
+    with pytest.raises(TypeError, match="E4M3"):
+        api.forge_linear_bwd_step_fp8(Xt, dYt, 1.0, 1.0, W, "sgd", {}, 1, 0)
