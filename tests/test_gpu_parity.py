@@ -443,3 +443,42 @@ def test_split_last_wave_bitexact(shape, opt_name, s_dtype):
     gpu, _ = prob.run_gpu(fused=True)
     ref, _, _ = prob.run_oracle()
     _compare_exact(prob, gpu, ref)
+
+
+# (T, N, K) chosen for the dealing regimes of the one-launch step on 76 CTA
+# pairs: F weight tiles and D dX tiles fewer than the pairs, exactly a wave,
+# one over a wave, dX-dominated, weight-dominated, and ragged T.
+DEALING = {
+    "F1_D1": (256, 256, 256),
+    "F76_D19": (256, 1024, 4864),
+    "F152_D38": (512, 2048, 4864),
+    "F77_D44": (1024, 1792, 2816),
+    "F2_D128": (16384, 256, 512),
+    "F224_D16": (1024, 14336, 1024),
+    "ragged_T": (1000, 1024, 2048),
+}
+
+
+@pytest.mark.parametrize("case", list(DEALING))
+def test_one_launch_dealing_regimes_equal_two_launches(case):
+    """The host deals dX tiles over the pairs by a load model (full rounds,
+    then the rest to the pairs with fewer weight tiles); every regime must
+    still cover each dX tile exactly once and write no weight before its
+    column block's dX tiles are done: the one launch gives the same bits as
+    two launches (a large SGD-momentum step makes an early weight write
+    visible in dX of the next step)."""
+    T, N, K = DEALING[case]
+    prob = Problem(T=T, N=N, K=K, w_dtype="bf16", s_dtype="fp32", opt_name="sgd_momentum",
+                   hp={"lr": 0.5, "momentum": 0.9}, seed=73, steps=2, device_inputs=True)
+    outs = []
+    for fused_launch in (True, False):
+        api.forge_set_step_fusion(fused_launch)
+        try:
+            outs.append(prob.run_gpu(fused=True, want_dx=True))
+        finally:
+            api.forge_set_step_fusion(True)
+    (g1, dx1), (g2, dx2) = outs
+    for k in g1:
+        assert torch.equal(g1[k], g2[k]), k
+    for s_ in range(prob.steps):
+        assert torch.equal(dx1[s_], dx2[s_]), f"dX step {s_ + 1}"
