@@ -50,7 +50,10 @@ def _digest(sources) -> str:
             h.update(f.encode() + b"\0" + fh.read())
     with open(os.path.join(INCLUDE, "forge.h"), "rb") as fh:
         h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    # the flags without this checkout's absolute include paths, so that the
+    # same sources hash alike wherever the repository sits
+    flags = [f.replace(CSRC, "<csrc>").replace(INCLUDE, "<include>") for f in NVCC_FLAGS]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 
