@@ -1,0 +1,40 @@
+"""Host-side logic of bench.py that needs no GPU: the clock-sample summary
+that decides whether a timed region is measured again."""
+
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _summary(lines):
+    c = bench.ClockSampler(0)
+    c.lines = lines
+    return c.summary()
+
+
+def test_clock_summary_median_and_reasons():
+    # index, clocks.sm, clocks.max.sm, power.draw, active, hw, hw_thermal, sw_thermal, sw_power_cap
+    lines = ["0, 1800, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "0, 1900, 2070, 950.0, 0x4, Not Active, Not Active, Not Active, Active",
+             "0, 2000, 2070, 980.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    s = _summary(lines)
+    assert s["sm_mhz"] == 1900 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    assert not (bench.THROTTLE_REASONS & set(s["reasons"]))  # power cap alone: no re-measure
+
+
+def test_clock_summary_flags_thermal_slowdown():
+    lines = ["0, 1500, 2070, 1000.0, 0x20, Not Active, Not Active, Active, Not Active",
+             "garbled line", "0, [N/A], 2070, 1.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    s = _summary(lines)
+    assert s["samples"] == 1 and s["reasons"] == ["sw_thermal_slowdown"]
+    assert bench.THROTTLE_REASONS & set(s["reasons"])  # would be measured again
+
+
+def test_clock_summary_without_samples():
+    s = _summary([])
+    assert s["sm_mhz"] is None and s["samples"] == 0 and s["reasons"] == []
