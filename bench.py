@@ -180,6 +180,48 @@ def oracle_sample(layer="k_proj", T=16384, seed=7):
     return dt, 4.0 * N * K * T
 
 
+def oracle_sample_workload(key, seed=7):
+    """The oracle as it stands on a bounded sample of a secondary workload:
+    the whole fp32-master layer (its 3 steps), else one step of one
+    representative linear (the smallest of the set, with that workload's
+    state dtype and rule; the first optimizer of a sweep).  Returns (seconds,
+    flops counted like that workload's GPU line, a description)."""
+    from oracle import linear_step as ls
+    from oracle import optimizers as opt
+    from oracle import quant, rounding
+    w = inputs.WORKLOADS[key]
+    name, N, K = min(w.linears, key=lambda x: x[1] * x[2])
+    T = w.T
+    opt_name = list(inputs.SWEEP_HPARAMS)[0] if key == "sweep_4096" else w.opt
+    hp = inputs.SWEEP_HPARAMS[opt_name] if key == "sweep_4096" else w.hparams
+    kind = opt.NAMES.index(opt_name)
+    want_dx = key != "sweep_4096"
+    steps = w.steps if key == "single_256" else 1
+    W = inputs.normal((N, K), w.w_std, seed + 2, torch.float32).numpy()
+    st = {"w_dtype": w.w_dtype, "s_dtype": w.s_dtype,
+          "W": W if w.w_dtype == "fp32" else rounding.bf16_bits_rne(W)}
+    if w.s_dtype == "int8":
+        st["s1"], st["s1_scale"] = quant.quantize_blocks(
+            inputs.normal((N, K), max(w.m_init_std, 1e-30), seed + 3, torch.float32).numpy(), True)
+        st["s2"], st["s2_scale"] = quant.quantize_blocks(
+            inputs.abs_normal((N, K), max(w.v_init_std, 1e-30), seed + 4).numpy(), False)
+    else:
+        st["s1"] = np.zeros((N, K), np.float32)
+        st["s2"] = np.zeros((N, K), np.float32)
+    dt = 0.0
+    for s in range(steps):
+        X = inputs.bf16_to_bits(inputs.normal((T, K), w.x_std, seed + 10 * s + 5))
+        dY = inputs.bf16_to_bits(inputs.normal((T, N), w.dy_std, seed + 10 * s + 6))
+        t0 = time.perf_counter()
+        out = ls.linear_bwd_step(X, dY, st, kind, opt.Hparams(**hp), s + 1, seed, want_dx=want_dx)
+        dt += time.perf_counter() - t0
+        st.update({k: out[k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale") if k in out})
+    flops = steps * (4.0 if want_dx else 2.0) * N * K * T
+    desc = (f"{steps} step(s) of the {name} ({N}x{K}, T={T}): "
+            f"{'dX + ' if want_dx else ''}dW + {opt_name} with {w.w_dtype} weights, {w.s_dtype} states")
+    return dt, flops, desc
+
+
 def run_reference(args):
     world, rank, _ = _dist()
     if rank != 0:
@@ -726,11 +768,19 @@ def run_workload(args):
         "peak_device_memory_bytes": torch.cuda.max_memory_allocated(dev),
         "per_optimizer": results if sweep else None,
         "clocks": results[opts[-1]]["clocks"],
+        "cpu_baseline": None,
         "gpu_launches": sum(1 if (not want_dx or (w.w_dtype == "bf16" and L.N % 64 == 0 and L.K % 64 == 0))
                             else 2 for _, L in layers) * args.steps * len(opts),
         "note": "inputs are drawn once per linear and reused by every timed step (timing does "
                 "not depend on their values); parity for this configuration is in the tests",
     }
+    if not args.no_cpu_baseline and not out["config"]["partial"]:
+        del layers, X
+        torch.cuda.empty_cache()
+        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        dt, f, desc = oracle_sample_workload(args.workload)
+        out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
+                               "kind": "oracle", "sample": desc}
     print(json.dumps(out), flush=True)
 
 
