@@ -38,3 +38,12 @@ def test_clock_summary_flags_thermal_slowdown():
 def test_clock_summary_without_samples():
     s = _summary([])
     assert s["sm_mhz"] is None and s["samples"] == 0 and s["reasons"] == []
+
+
+def test_oracle_sample_of_the_fp32_master_layer():
+    """The secondary lines' CPU leg: the 256x256 fp32-master configuration is
+    sampled whole (3 steps of dX + dW + AdamW), its flops counted like the GPU
+    line (4NKT per step)."""
+    dt, flops, desc = bench.oracle_sample_workload("single_256")
+    assert dt > 0 and flops == 3 * 4.0 * 256 * 256 * 512
+    assert "3 step(s)" in desc and "fp32 weights" in desc
