@@ -9,10 +9,19 @@ tensors resident in HBM; each activation/gradient tensor is >= 134 MB, larger
 than the 129 MB L2, so no L2 flush is needed between steps.
 
 Printed: one JSON line (rank 0).  ``value`` = (2NKT for dW + 2NKT for dX,
-summed over the layers and ranks) / step time, in TFLOP/s.  ``roofline`` is the
-step kernel's own rate (CUDA events around its launches) against the measured
-dense-bf16 peak.  ``two_launch`` times the same step with dX and the fused
-step as separate launches (and each kernel's rate).  ``e2e`` repeats the step with the
+summed over the layers and ranks) / step time, in TFLOP/s; the timed region of
+``--steps`` steps is repeated back to back until it has run for at least 3 s
+(``timed_region``) and ``ms_per_step`` is the median region, so the clock
+samples cover the number.  ``roofline`` is the step kernel's own rate (CUDA
+events around its launches) against the measured dense-bf16 peak that applies
+to the region's length: the sustained peak for a region of 3 s or more, else
+the burst peak.  ``fused_wgrad_opt`` is the rate of the fused weight-gradient
++ optimizer launches alone (2NKT, dX launched separately and not counted).
+``two_launch`` times the same step with dX and the fused step as separate
+launches (and each kernel's rate).  ``configs`` measures the other
+configurations in the same run (the Llama set with INT8 moments, the
+4096x4096 optimizer sweep, the 40-layer Qwen3-14B sweep at T = 4096, the
+fp32-master 256x256 layer), one key each.  ``e2e`` repeats the step with the
 inputs copied from pinned host memory inside the timed region (on a copy
 stream, overlapping the previous step's compute) and the status word read
 back every step.  ``unfused``
@@ -80,6 +89,44 @@ def _profiled_traffic():
         return float(fields["traffic_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+# A timed region at least this long runs at the clocks a seconds-long GEMM
+# loop settles to under the power cap, the conditions of the sustained peak;
+# a shorter one is compared with the burst peak.
+SUSTAINED_REGION_S = 3.0
+
+
+def applicable_peak(region_s: float, burst: float, sustained: float, src: str):
+    """(peak, description) for a kernel timed over a region of region_s seconds."""
+    if region_s >= SUSTAINED_REGION_S:
+        return sustained, (f"bf16 sustained ({src}): the timed region ran {region_s:.2f} s, "
+                           f">= {SUSTAINED_REGION_S:.0f} s")
+    return burst, (f"bf16 burst ({src}): the timed region ran {region_s:.2f} s, "
+                   f"< {SUSTAINED_REGION_S:.0f} s")
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu model", "hardware")):
+                    return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
 
 def max_over_ranks(x: float, dist=None, device=None) -> float:
@@ -244,8 +291,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": inputs.WORKLOADS[WORKLOAD_KEY].name, "sample": "k_proj per step"},
-        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "cpu_model": cpu_model(),
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -326,24 +373,38 @@ def run_ours(args):
     barrier()
 
     def timed_region():
+        """R back-to-back regions of exactly args.steps steps each, R chosen so
+        that together they run for at least SUSTAINED_REGION_S seconds (the
+        nvidia-smi samples, 200 ms apart, then cover the number they qualify).
+        Returns the per-region step times (ms), the total seconds and the clocks."""
         nonlocal s_no
         for v in ev.values():
             v.clear()
+        region_ms = []
         with ClockSampler(local) as clk:
-            start = torch.cuda.Event(enable_timing=True)
-            end = torch.cuda.Event(enable_timing=True)
             barrier()
-            start.record(stream)
-            for _ in range(args.steps):
-                step(s_no, record=True)
-                s_no += 1
-            end.record(stream)
+            t_start = time.perf_counter()
+            while True:
+                start = torch.cuda.Event(enable_timing=True)
+                end = torch.cuda.Event(enable_timing=True)
+                start.record(stream)
+                for _ in range(args.steps):
+                    step(s_no, record=True)
+                    s_no += 1
+                end.record(stream)
+                end.synchronize()
+                region_ms.append(start.elapsed_time(end) / args.steps)
+                # every rank runs the same number of regions
+                go_on = time.perf_counter() - t_start < args.min_region_s
+                if max_over_ranks(1.0 if go_on else 0.0, dist, dev) == 0.0:
+                    break
             torch.cuda.synchronize()
+            total_s = time.perf_counter() - t_start
         barrier()
         api.forge_get_device_status()
-        return start, end, clk
+        return region_ms, total_s, clk
 
-    start, end, clk = timed_region()
+    region_ms, region_s, clk = timed_region()
     # A region whose clock samples saw a hardware or thermal slowdown on any
     # rank is measured once more (sw_power_cap is normal under load and kept).
     first_reasons = clk.summary()["reasons"]
@@ -351,13 +412,14 @@ def run_ours(args):
     remeasured_after = None
     if throttled > 0:
         remeasured_after = first_reasons
-        start, end, clk = timed_region()
-    ms = start.elapsed_time(end) / args.steps
+        region_ms, region_s, clk = timed_region()
+    ms = statistics.median(region_ms)
     ms = max_over_ranks(ms, dist, dev)
     kern_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev[L.name])
     launches = sum(len(v) for v in ev.values())
-    kern_tflops = flops_step * args.steps / (kern_ms * 1e-3) / 1e12
+    kern_tflops = flops_step * launches / len(layers) / (kern_ms * 1e-3) / 1e12
     hbm_gbs, peak_burst, peak_sust, peak_src = _peaks()
+    peak, peak_kind = applicable_peak(region_s, peak_burst, peak_sust, peak_src)
     value = flops_step * world / (ms * 1e-3) / 1e12
     per_layer = {L.name: round(4.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev[L.name]]) * 1e-3) / 1e12, 1)
                  for L in layers}
@@ -458,6 +520,8 @@ def run_ours(args):
     torch.cuda.synchronize()
     api.forge_get_device_status()
     two_ms = max_over_ranks(t0.elapsed_time(t1) / t_steps, dist, dev)
+    fused_peak, fused_peak_kind = applicable_peak(t0.elapsed_time(t1) * 1e-3, peak_burst, peak_sust,
+                                                  peak_src)
     fused_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev2[L.name])
     fused_tflops = flops_dw * t_steps / (fused_ms * 1e-3) / 1e12
     fused_per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev2[L.name]]) * 1e-3) / 1e12, 1)
@@ -535,6 +599,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     api.forge_get_device_status()
     fp8_ms = max_over_ranks(f0.elapsed_time(f1) / t_steps, dist, dev)
+    fp8_peak, fp8_peak_kind = applicable_peak(f0.elapsed_time(f1) * 1e-3, peak_burst, peak_sust, peak_src)
     fp8_kern_ms = sum(a.elapsed_time(b) for L in layers for (a, b) in ev8[L.name])
     fp8_tflops = flops_dw * t_steps / (fp8_kern_ms * 1e-3) / 1e12
     fp8_per_layer = {L.name: round(2.0 * L.N * L.K * T / (np.mean([a.elapsed_time(b) for a, b in ev8[L.name]]) * 1e-3) / 1e12, 1)
@@ -564,16 +629,30 @@ def run_ours(args):
                      "kernel": "one-launch FORGE step (tc_kernel mode 3: dX tiles, then dW tiles "
                                "with the AdamW epilogue), 4NKT flops per launch",
                      "achieved": round(kern_tflops, 2),
-                     "peak": peak_sust, "unit": "TFLOP/s",
-                     "frac": round(kern_tflops / peak_sust, 4),
-                     "peak_kind": f"bf16 sustained, {peak_src}",
+                     "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(kern_tflops / peak, 4),
+                     "peak_kind": peak_kind,
                      "frac_of_burst_peak": round(kern_tflops / peak_burst, 4),
+                     "frac_of_sustained_peak": round(kern_tflops / peak_sust, 4),
                      "traffic": _profiled_traffic(),
                      "traffic_unit": "DRAM bytes per step launch (mean of the 7 layers, ncu)",
                      "algorithmic_bytes_per_launch": round(bytes_step / len(layers)),
                      "algorithmic_bytes_per_step": bytes_step,
                      "launches_timed": launches,
                      "per_layer_tflops": per_layer},
+        "timed_region": {"regions": len(region_ms), "steps_per_region": args.steps,
+                         "seconds": round(region_s, 3),
+                         "ms_per_step_min": round(min(region_ms), 4),
+                         "ms_per_step_max": round(max(region_ms), 4),
+                         "ms_per_step_x_median_sm_mhz": (None if ck["sm_mhz"] is None
+                                                         else round(ms * ck["sm_mhz"], 1))},
+        "fused_wgrad_opt": {
+            "definition": "2NKT per linear / the fused weight-gradient + optimizer launches' own "
+                          "time, dX launched separately and not counted (the two-launch form)",
+            "tflops": round(fused_tflops, 2), "peak": fused_peak,
+            "frac": round(fused_tflops / fused_peak, 4), "peak_kind": fused_peak_kind,
+            "frac_of_burst_peak": round(fused_tflops / peak_burst, 4),
+            "per_layer_tflops": fused_per_layer},
         "two_launch": {"ms_per_step": round(two_ms, 4),
                        "value": round(flops_step * world / (two_ms * 1e-3) / 1e12, 2),
                        "fused_wgrad_opt_tflops": round(fused_tflops, 2),
@@ -591,21 +670,32 @@ def run_ours(args):
                 "value": round(flops_step * world / (fp8_ms * 1e-3) / 1e12, 2),
                 "operands": "E4M3 X^T and dY^T, one power-of-two scale per tensor; dX from bf16 dY",
                 "fused_wgrad_opt_tflops": round(fp8_tflops, 2),
-                "peak": round(2 * peak_sust, 1),
-                "peak_kind": f"2 x bf16 sustained ({peak_src}; nominal FP8/BF16 ratio)",
-                "frac": round(fp8_tflops / (2 * peak_sust), 4),
+                "peak": round(2 * fp8_peak, 1),
+                "peak_kind": "2 x " + fp8_peak_kind + " (nominal FP8/BF16 tensor-rate ratio)",
+                "frac": round(fp8_tflops / (2 * fp8_peak), 4),
                 "fused_per_layer_tflops": fp8_per_layer},
         "hbm_bytes_per_param_algorithmic": round(bytes_step / params, 3),
         "hbm_bytes_per_param_measured": (None if _profiled_traffic() is None else
                                          round(_profiled_traffic() * len(layers) / params, 3)),
-        "gpu_launches": len(layers) * args.steps,
+        "gpu_launches": launches,
         "clocks": ck,
     }
+    # ---- the other measured configurations, in the same run, one key each
+    # (the headline's tensors are freed first: the Qwen3-14B sweep holds ~99 GB)
+    X.clear()
+    layers.clear()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if not args.no_configs:
+        out["configs"] = {}
+        for key in CONFIG_KEYS:
+            r = measure_workload(api, key, args.steps, args.warmup, local, cpu=not args.no_cpu_baseline)
+            out["configs"][key] = r
+            torch.cuda.empty_cache()
     if not args.no_cpu_baseline:
-        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
         dt, f = oracle_sample()
-        out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-                               "kind": "oracle",
+        out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
+                               "cpu_model": cpu_model(), "kind": "oracle",
                                "sample": "one k_proj linear (1024x4096, T=16384): dX + dW + AdamW "
                                          "with bf16 stochastic rounding, one step"}
     print(json.dumps(out), flush=True)
@@ -649,38 +739,36 @@ class _SLayer:
             (2 * 4 * N * (K // 64) if w.s_dtype == "int8" else 0)
 
 
-def run_workload(args):
-    """One JSON line for a secondary workload: its step timed with CUDA events
-    between synchronisations (W warm-up steps, then K), the step launches' own
-    rate against the sustained bf16 peak, peak device memory and the
-    algorithmic HBM bytes per parameter."""
-    from optimizer_tcgen05_dw_gb300 import api
-    from optimizer_tcgen05_dw_gb300.build import build
+CONFIG_KEYS = ("llama8b_bf16_int8state", "sweep_4096", "qwen14b_int8", "single_256")
 
-    world, rank, local = _dist()
-    if rank != 0:
-        return
-    torch.cuda.set_device(local)
-    build()
-    api.lib()
+
+def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_layers=None,
+                     no_dx=False, cpu=True):
+    """One secondary workload: its step timed with CUDA events between
+    synchronisations (warmup steps, then `steps`), the step launches' own rate
+    against the dense-bf16 peak that applies to the region's length, the
+    slower-roofline fraction, per-linear rates, peak device memory and the
+    algorithmic HBM bytes per parameter; with `cpu`, the oracle timed on a
+    bounded sample of the same configuration.  Returns a dict."""
     dev = torch.device("cuda", local)
-    w = inputs.WORKLOADS[args.workload]
+    w = inputs.WORKLOADS[key]
     T = w.T
     stream = torch.cuda.current_stream()
+    torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats(dev)
     hbm_gbs, peak_burst, peak_sust, peak_src = _peaks()
-    sweep = args.workload == "sweep_4096"
+    sweep = key == "sweep_4096"
     opts = list(inputs.SWEEP_HPARAMS) if sweep else [w.opt]
     # layers: (layer index, name, N, K); activations per layer
-    if args.workload == "qwen14b_int8":
-        n_layers = w.layers if args.num_layers is None else args.num_layers
+    if key == "qwen14b_int8":
+        n_layers = w.layers if num_layers is None else num_layers
         shapes = [(li, n, N, K) for li in range(n_layers) for n, N, K in inputs.QWEN3_14B_LINEARS
-                  if not args.layers or n in args.layers]
+                  if not only_layers or n in only_layers]
         acts = {"x_attn": 5120, "x_o": 5120, "x_mlp": 5120, "x_down": 17408}
         act_of = QWEN_ACT
-    elif args.workload == "llama8b_bf16_int8state":
+    elif key == "llama8b_bf16_int8state":
         shapes = [(0, n, N, K) for n, N, K in sorted(inputs.LLAMA31_8B_LINEARS, key=lambda x: ORDER.index(x[0]))
-                  if not args.layers or n in args.layers]
+                  if not only_layers or n in only_layers]
         acts = {"x_attn": 4096, "x_o": 4096, "x_mlp": 4096, "x_down": 14336}
         act_of = ACT
     else:  # one linear
@@ -688,7 +776,7 @@ def run_workload(args):
         shapes = [(0, n0, N0, K0)]
         acts = {"x": K0}
         act_of = {n0: "x"}
-    want_dx = not sweep and not args.no_dx
+    want_dx = not sweep and not no_dx
     X = {(li, a): inputs.normal((T, k), w.x_std, inputs.layer_seed(7, li, 0, 50 + j), torch.bfloat16, dev)
          for li in sorted({s[0] for s in shapes}) for j, (a, k) in enumerate(acts.items())}
     layers = [(li, _SLayer(api, n, N, K, T, dev, inputs.layer_seed(7, li, 0, 10 * (1 + i)), w, want_dx))
@@ -701,6 +789,7 @@ def run_workload(args):
     bytes_step = sum(2 * (L.T * L.K + L.T * L.N) + (2 * L.T * L.K if want_dx else 0) for _, L in layers) + \
         params * w_bytes + sum(L.state_bytes for _, L in layers)
     results = {}
+    per_linear_ms = {}
     s_no = 1
     for opt_name in opts:
         hp = inputs.SWEEP_HPARAMS[opt_name] if sweep else w.hparams
@@ -719,9 +808,9 @@ def run_workload(args):
                                           L.vs if s2 is not None else None, dX=L.dX)
                 if record:
                     b.record(stream)
-                    ev.append((a, b))
+                    ev.append((L.name, a, b))
 
-        for _ in range(args.warmup):
+        for _ in range(warmup):
             step(s_no)
             s_no += 1
         api.forge_get_device_status()
@@ -730,39 +819,48 @@ def run_workload(args):
             start = torch.cuda.Event(enable_timing=True)
             end = torch.cuda.Event(enable_timing=True)
             start.record(stream)
-            for _ in range(args.steps):
+            for _ in range(steps):
                 step(s_no, record=True)
                 s_no += 1
             end.record(stream)
             torch.cuda.synchronize()
         api.forge_get_device_status()
-        ms = start.elapsed_time(end) / args.steps
-        kern_ms = sum(a.elapsed_time(b) for a, b in ev)
+        ms = start.elapsed_time(end) / steps
+        kern_ms = sum(a.elapsed_time(b) for _, a, b in ev)
+        for name, a, b in ev:
+            per_linear_ms.setdefault(name, []).append(a.elapsed_time(b))
         results[opt_name] = {"ms_per_step": round(ms, 4),
                              "value": round(flops_step / (ms * 1e-3) / 1e12, 2),
-                             "kernel_tflops": round(flops_step * args.steps / (kern_ms * 1e-3) / 1e12, 2),
+                             "kernel_tflops": round(flops_step * steps / (kern_ms * 1e-3) / 1e12, 2),
+                             "region_s": round(start.elapsed_time(end) * 1e-3, 4),
                              "clocks": clk.summary()}
     tot_ms = sum(r["ms_per_step"] for r in results.values())
     value = flops_step * len(opts) / (tot_ms * 1e-3) / 1e12
     kern = statistics.mean(r["kernel_tflops"] for r in results.values())
-    t_flop = flops_step / (peak_sust * 1e12)
+    region_s = max(r["region_s"] for r in results.values())
+    peak, peak_kind = applicable_peak(region_s, peak_burst, peak_sust, peak_src)
+    t_flop = flops_step / (peak * 1e12)
     t_byte = bytes_step / (hbm_gbs * 1e9)
     bound = "tensor" if t_flop >= t_byte else "hbm"
+    # per distinct linear shape: 2NKT (+ 2NKT for dX) over its mean launch time
+    shape_of = {L.name: (L.N, L.K) for _, L in layers}
+    per_linear = {n: round((4.0 if want_dx else 2.0) * shape_of[n][0] * shape_of[n][1] * T /
+                           (statistics.mean(v) * 1e-3) / 1e12, 1) for n, v in per_linear_ms.items()}
     out = {
-        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_ms / len(opts), 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16" if w.w_dtype == "bf16" else "fp32", "data": "synthetic",
-        "secondary": True,
-        "config": {"workload": w.name, "key": args.workload, "T": T, "linears": len(layers),
+        "value": round(value, 2), "unit": "TFLOP/s", "ms_per_step": round(tot_ms / len(opts), 4),
+        "steps": steps, "warmup": warmup,
+        "dtype": "bf16" if w.w_dtype == "bf16" else "fp32",
+        "config": {"workload": w.name, "key": key, "T": T, "linears": len(layers),
                    "flops_counted": "2NKT (dW)" + (" + 2NKT (dX)" if want_dx else "") + " per linear",
                    "w_dtype": w.w_dtype, "s_dtype": w.s_dtype, "optimizers": opts,
-                   "partial": bool(args.layers or args.num_layers is not None or args.no_dx)},
+                   "partial": bool(only_layers or num_layers is not None or no_dx)},
         "roofline": {"bound": bound, "achieved": round(kern, 2), "unit": "TFLOP/s",
-                     "peak": peak_sust, "peak_kind": f"bf16 sustained, {peak_src}",
-                     "frac": round(kern / peak_sust, 4),
+                     "peak": peak, "peak_kind": peak_kind,
+                     "frac": round(kern / peak, 4),
+                     "frac_of_burst_peak": round(kern / peak_burst, 4),
                      "frac_of_slower_roofline": round(max(t_flop, t_byte) * 1e3 / (tot_ms / len(opts)), 4),
                      "algorithmic_bytes_per_step": bytes_step},
+        "per_linear_tflops": per_linear,
         "hbm_bytes_per_param_algorithmic": round(bytes_step / params, 3),
         "params": params,
         "peak_device_memory_bytes": torch.cuda.max_memory_allocated(dev),
@@ -770,17 +868,40 @@ def run_workload(args):
         "clocks": results[opts[-1]]["clocks"],
         "cpu_baseline": None,
         "gpu_launches": sum(1 if (not want_dx or (w.w_dtype == "bf16" and L.N % 64 == 0 and L.K % 64 == 0))
-                            else 2 for _, L in layers) * args.steps * len(opts),
+                            else 2 for _, L in layers) * steps * len(opts),
         "note": "inputs are drawn once per linear and reused by every timed step (timing does "
                 "not depend on their values); parity for this configuration is in the tests",
     }
-    if not args.no_cpu_baseline and not out["config"]["partial"]:
-        del layers, X
-        torch.cuda.empty_cache()
-        cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-        dt, f, desc = oracle_sample_workload(args.workload)
-        out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
-                               "kind": "oracle", "sample": desc}
+    del layers, X
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    if cpu and not out["config"]["partial"]:
+        dt, f, desc = oracle_sample_workload(key)
+        out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
+                               "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
+    return out
+
+
+def run_workload(args):
+    """One JSON line for a secondary workload (marked "secondary")."""
+    from optimizer_tcgen05_dw_gb300 import api
+    from optimizer_tcgen05_dw_gb300.build import build
+
+    world, rank, local = _dist()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local)
+    build()
+    api.lib()
+    r = measure_workload(api, args.workload, args.steps, args.warmup, local, args.layers,
+                         args.num_layers, args.no_dx, cpu=not args.no_cpu_baseline)
+    out = {"metric": METRIC, "value": r.pop("value"), "unit": r.pop("unit"), "n_gpus": 1,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": r.pop("ms_per_step"),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+           "dtype": r.pop("dtype"), "data": "synthetic", "secondary": True}
+    r.pop("steps")
+    r.pop("warmup")
+    out.update(r)
     print(json.dumps(out), flush=True)
 
 
@@ -791,6 +912,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--min-region-s", type=float, default=None,
+                    help="repeat the timed region of --steps steps until this many seconds have "
+                         "run (the value is the median region); 0 = one region; default "
+                         f"{SUSTAINED_REGION_S:.0f}, or 0 with --no-extras")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other measured configurations in the headline line")
     ap.add_argument("--layers", nargs="*", default=None, choices=ORDER,
                     help="restrict to some linears (profiling); the bench line uses all seven")
     ap.add_argument("--no-extras", action="store_true",
@@ -803,6 +930,8 @@ def main():
                     help="a secondary measured configuration instead of the headline one "
                          "(its own JSON line, marked \"secondary\")")
     args = ap.parse_args()
+    if args.min_region_s is None:
+        args.min_region_s = 0.0 if args.no_extras else SUSTAINED_REGION_S
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.impl == "reference":

@@ -1,6 +1,6 @@
 """Shared test utilities: input construction, oracle/GPU adapters, tolerance checks.
 
-Tolerances (DESIGN.md §5):
+Tolerances:
 * exact FP32 inputs (integer-grid data, oracle-supplied gradients): bit-exact;
 * realistic data, one step from a common state: an *interval oracle*.  The GPU
   sums the T token products on the tensor cores in FP32 (T/16 accumulator

@@ -47,3 +47,18 @@ def test_oracle_sample_of_the_fp32_master_layer():
     dt, flops, desc = bench.oracle_sample_workload("single_256")
     assert dt > 0 and flops == 3 * 4.0 * 256 * 256 * 512
     assert "3 step(s)" in desc and "fp32 weights" in desc
+
+
+def test_peak_follows_the_timed_region_length():
+    """A region shorter than the sustained threshold is compared with the burst
+    peak, a longer one with the sustained peak, and the line says which."""
+    p, kind = bench.applicable_peak(0.17, 1931.0, 1747.4, "measured")
+    assert p == 1931.0 and kind.startswith("bf16 burst")
+    p, kind = bench.applicable_peak(bench.SUSTAINED_REGION_S, 1931.0, 1747.4, "measured")
+    assert p == 1747.4 and kind.startswith("bf16 sustained")
+
+
+def test_cpu_model_is_a_nonempty_string():
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m
+    assert bench.host_cores() >= 1
