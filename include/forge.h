@@ -130,7 +130,15 @@ typedef struct forge_hparams {
  * after every dX tile of its 256-column block has finished reading W); the
  * launch uses a library-owned counter array in device memory (cleared on
  * `stream` first), so two such calls must not run concurrently on one device
- * (order them on one stream, or call forge_set_step_fusion(0)).  Otherwise
+ * (order them on one stream, or call forge_set_step_fusion(0)).  The one
+ * launch sizes its grid so that all of its CTA pairs fit on the device at
+ * once, and a weight tile waits (bounded) for dX tiles that other pairs run:
+ * a kernel on another stream that holds SMs for longer than the wait limit
+ * (forge_set_wait_limit_ns, 2 s by default) can keep pairs from starting, and
+ * the call then ends in FORGE_ERR_TIMEOUT with W and the states partly
+ * updated.  Callers that overlap long-lived kernels (e.g. a persistent
+ * communication kernel) with this step should call forge_set_step_fusion(0),
+ * whose two launches wait on nothing.  Otherwise
  * dX is a separate launch enqueued first on `stream`.  Both forms compute the
  * same bits.  step is 1-based (bias corrections).  Nothing is allocated; no
  * gradient tensor is written.  Returns FORGE_OK once the launches are
@@ -150,8 +158,9 @@ FORGE_API forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const 
  *     are cleared (set to zero) on `stream` before its launch.
  *   - Requests the one launch applies to (bf16 weights, dX requested, T > 0,
  *     N and K multiples of 64) with K > 262144 return FORGE_ERR_UNSUPPORTED
- *     before any CUDA call.  Other requests need no scratch and run exactly
- *     as forge_linear_bwd_step's two-launch form.
+ *     before any CUDA call.  Other requests, and those whose one launch
+ *     cannot be resident on the device, need no scratch and run exactly as
+ *     forge_linear_bwd_step's two-launch form.
  *   - Races: every call on a device uses the same array.  Two calls whose
  *     launches overlap in time (different streams, no ordering between them)
  *     corrupt each other's counters; order them on one stream or with events.

@@ -43,8 +43,20 @@ def lib_path(name: str = "libforge.so") -> str:
     return os.path.join(BUILD, name)
 
 
+def _nvcc_version() -> str:
+    """The toolkit's release line (e.g. "Cuda compilation tools, release 13.0,
+    V13.0.88"), part of the digest so a build by another toolkit never matches."""
+    try:
+        out = subprocess.run([nvcc(), "--version"], capture_output=True, text=True, timeout=60).stdout
+    except (OSError, RuntimeError, subprocess.SubprocessError):
+        return "unknown"
+    lines = [ln.strip() for ln in out.splitlines() if "release" in ln]
+    return lines[0] if lines else "unknown"
+
+
 def _digest(sources) -> str:
     h = hashlib.sha256()
+    h.update(_nvcc_version().encode() + b"\0")
     for f in sorted(set(sources) | set(HEADERS)):
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())

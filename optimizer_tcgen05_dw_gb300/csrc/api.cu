@@ -636,8 +636,8 @@ forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const for
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
   if ((st = check_device(d)) != FORGE_OK) return st;
-  if (d.step_pairs[kernel_sdt(state, lin->T)] <= 0)
-    return fail(FORGE_ERR_UNSUPPORTED, "the one-launch step cannot be resident on this device");
+  if (d.step_pairs[kernel_sdt(state, lin->T)] <= 0)  // the one launch cannot be resident: no scratch
+    return forge_linear_bwd_step(lin, state, opt_kind, hp, step, seed, stream);  // two launches
   return launch_step(lin, state, opt_kind, make_scalars(opt_kind, *hp, step), step, seed,
                      static_cast<cudaStream_t>(stream), d, d.static_scratch);
 }

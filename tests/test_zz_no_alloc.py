@@ -29,6 +29,45 @@ def test_oversize_request_rejected_before_any_cuda_call():
     assert b"static scratch" in L.forge_last_error_message()
 
 
+def _static_call(K, s_dtype=None, N=128):
+    """forge_linear_bwd_step_static with never-dereferenced fake pointers."""
+    L = api.lib()
+    fake = 1 << 20
+    lin = api.ForgeLinear(64, N, K, fake, fake, fake)
+    sd = api.STATE_FP32 if s_dtype is None else s_dtype
+    st = api.ForgeState(fake, api.W_BF16_SR, sd, fake, fake, fake, fake)
+    hp = api.hparams(lr=1e-3)
+    r = L.forge_linear_bwd_step_static(ctypes.byref(lin), ctypes.byref(st), api.OPT_KINDS["adamw"],
+                                       ctypes.byref(hp), 1, 0, None)
+    return r, L.forge_last_error_message()
+
+
+def test_size_limit_edge_one_block_over_is_rejected():
+    build()
+    # K = 262144 + 64: 1025 column blocks of 256, one more than the scratch holds
+    r, msg = _static_call(262144 + 64)
+    assert r == 2 and b"static scratch" in msg, (r, msg)
+
+
+def test_requests_outside_the_one_launch_reach_the_two_launch_checks():
+    build()
+    # K above the limit but not a multiple of 64: no one launch, so no scratch;
+    # with INT8 states the two-launch path's own check (K % 64) refuses it on
+    # the host, not the scratch limit
+    r, msg = _static_call(270336 + 8, api.STATE_INT8_B64)
+    assert r == 1 and b"K % 64" in msg, (r, msg)
+    assert b"static scratch" not in msg
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers on a GPU host")
+def test_size_limit_edge_largest_accepted_passes_the_host_check():
+    build()
+    # K = 262144: exactly 1024 blocks, accepted by the size check; on a host
+    # without a GPU the call then fails at its first CUDA call instead
+    r, msg = _static_call(262144)
+    assert r == 3 and b"static scratch" not in msg, (r, msg)
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("s_dtype", ["fp32", "int8"])
 def test_static_scratch_step_equals_regular_step(cuda_device, s_dtype):
