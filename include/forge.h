@@ -147,6 +147,32 @@ FORGE_API forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const 
                                      int32_t opt_kind, const forge_hparams_t* hp,
                                      int64_t step, uint64_t seed, void* stream);
 
+/* forge_linear_bwd_step on one row shard of a larger weight matrix: the
+ * column-parallel (output-feature) split of tensor parallelism, under which
+ * the pages' Technical Summary §2 "Distributed Training Compatibility" says
+ * the fused step stays exact, because a shard's weight gradient
+ * dW_r = dY_r^T X is complete on its own device at backward time (dY_r, the
+ * shard's columns of dY, is what that device produced in the forward pass;
+ * X is replicated).
+ *   - lin->N is the shard's row count; W, s1, s2 and the scales hold only the
+ *     shard's rows [row_offset, row_offset + N) of a matrix with K columns;
+ *     lin->dY is the shard's [T x N] columns of the upstream gradient.
+ *   - Every element is stepped exactly as forge_linear_bwd_step steps the same
+ *     element of the whole matrix: stochastic rounding draws the bits of
+ *     index (row_offset + n) * K + k, so the shards of a split matrix,
+ *     stepped one by one with the same seed, reproduce the unsplit step's
+ *     weights and states bit for bit.
+ *   - dX (if requested) is this shard's PARTIAL input gradient dY_r W_r
+ *     (pre-update W_r, bf16); the layer's dX is the sum of the shards'
+ *     partials, which the caller forms (an all-reduce across the devices).
+ *   - row_offset >= 0, else FORGE_ERR_INVALID_ARG; row_offset + N must fit in
+ *     31 bits.  Everything else as forge_linear_bwd_step (same one-launch and
+ *     two-launch forms, same concurrency rule). */
+FORGE_API forge_status_t forge_linear_bwd_step_shard(const forge_linear_t* lin,
+                                                     const forge_state_t* state, int32_t opt_kind,
+                                                     const forge_hparams_t* hp, int64_t step,
+                                                     uint64_t seed, int64_t row_offset, void* stream);
+
 /* forge_linear_bwd_step computing the same bits, with the one-launch form's
  * scratch in a fixed, static device array of this library instead of the
  * array that forge_linear_bwd_step uses: the dX-completion counters of the

@@ -69,6 +69,9 @@ _SIGNATURES = {
     "forge_linear_bwd_step_static": (c_int32, [ctypes.POINTER(ForgeLinear), ctypes.POINTER(ForgeState),
                                                c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
                                                c_void_p]),
+    "forge_linear_bwd_step_shard": (c_int32, [ctypes.POINTER(ForgeLinear), ctypes.POINTER(ForgeState),
+                                              c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
+                                              c_int64, c_void_p]),
     "forge_linear_bwd_step_fp8": (c_int32, [ctypes.POINTER(ForgeLinearFp8), ctypes.POINTER(ForgeState),
                                             c_int32, ctypes.POINTER(ForgeHparams), c_int64, c_uint64,
                                             c_void_p]),
@@ -200,6 +203,27 @@ def forge_linear_bwd_step(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1
     _check(lib().forge_linear_bwd_step(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
                                        ctypes.byref(hparams(**hp)), int(step),
                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
+
+
+def forge_linear_bwd_step_shard(X, dY, W, opt: str, hp: dict, step: int, seed: int, row_offset: int,
+                                s1=None, s2=None, s1_scale=None, s2_scale=None, dX=None, stream=None):
+    """The FORGE step on rows [row_offset, row_offset + N) of a larger weight
+    matrix (a column-parallel shard): dY holds the shard's N columns of the
+    upstream gradient, W and the states the shard's rows; stochastic rounding
+    uses the elements' indices in the whole matrix.  dX, if given, receives the
+    shard's partial input gradient (the layer's dX is the sum over shards)."""
+    T, K = X.shape
+    N = W.shape[0]
+    _need(X, "X", torch.bfloat16, (T, K))
+    _need(dY, "dY", torch.bfloat16, (T, N))
+    if dX is not None:
+        _need(dX, "dX", torch.bfloat16, (T, K))
+    st = make_state(W, s1, s2, s1_scale, s2_scale)
+    lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), _ptr(dX))
+    _check(lib().forge_linear_bwd_step_shard(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
+                                             ctypes.byref(hparams(**hp)), int(step),
+                                             int(seed) & 0xFFFFFFFFFFFFFFFF, int(row_offset),
+                                             _stream(stream)))
 
 
 def forge_linear_bwd_step_static(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1=None,

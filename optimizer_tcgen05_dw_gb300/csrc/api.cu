@@ -491,8 +491,8 @@ void balance_dx(GemmParams& p, int pairs, int64_t T, int64_t N) {
 // multiples of 64; T > 0): dX tiles over (T, K) reducing over N, then dW
 // tiles over (N, K) reducing over T.
 forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state, int32_t opt_kind,
-                           const OptScalars& sc, int64_t step, uint64_t seed, cudaStream_t s,
-                           const DeviceInfo& d, uint32_t* counters = nullptr) {
+                           const OptScalars& sc, int64_t step, uint64_t seed, uint64_t sr_base,
+                           cudaStream_t s, const DeviceInfo& d, uint32_t* counters = nullptr) {
   const int64_t T = lin->T, N = lin->N, K = lin->K;
   forge_status_t st;
   CUtensorMap ma, mb, mda, mdb, m1, m2, mdx, mw;
@@ -512,6 +512,7 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   p.seed = seed;
   philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
+  p.sr_base = sr_base;
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
@@ -540,17 +541,12 @@ forge_status_t check_device(const DeviceInfo& d) {
   return FORGE_OK;
 }
 
-}  // namespace
-}  // namespace forge
-
-using namespace forge;
-
-extern "C" {
-
-forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_state_t* state,
-                                     int32_t opt_kind, const forge_hparams_t* hp, int64_t step,
-                                     uint64_t seed, void* stream) {
-  g_msg[0] = '\0';
+// forge_linear_bwd_step on rows [row_offset, row_offset + N) of a matrix with
+// K columns: the stochastic-rounding counter takes the element's index in the
+// whole matrix, (row_offset + n) * K + k.
+forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, int32_t opt_kind,
+                        const forge_hparams_t* hp, int64_t step, uint64_t seed, int64_t row_offset,
+                        void* stream) {
   forge_status_t st;
   if ((st = check_linear(lin, true)) != FORGE_OK) return st;
   if ((st = check_hp(opt_kind, hp, step)) != FORGE_OK) return st;
@@ -563,13 +559,14 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   if ((st = check_device(d)) != FORGE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const OptScalars sc = make_scalars(opt_kind, *hp, step);
+  const uint64_t sr_base = static_cast<uint64_t>(row_offset) * static_cast<uint64_t>(lin->K) / 8u;
   // One launch for dX and the FORGE step (bf16 weights, 64-aligned N and K):
   // the dX tiles first, each dW tile's update after the dX tiles that read its
   // weights.
   if (lin->dX != nullptr && lin->T > 0 && state->w_dtype == FORGE_W_BF16_SR && lin->N % 64 == 0 &&
       lin->K % 64 == 0 && (lin->K + kTileN - 1) / kTileN <= kMaxDxBlocks && g_step_fusion.load() &&
       d.step_pairs[kernel_sdt(state, lin->T)] > 0)
-    return launch_step(lin, state, opt_kind, sc, step, seed, s, d);
+    return launch_step(lin, state, opt_kind, sc, step, seed, sr_base, s, d);
   // 1. dX from the pre-update weights, enqueued first on the same stream.
   if (lin->dX != nullptr && (st = launch_dgrad(lin, state->W, state->w_dtype, s, d)) != FORGE_OK) return st;
   cudaError_t e;
@@ -580,6 +577,7 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
     ep.W = state->W; ep.s1 = state->s1; ep.s2 = state->s2;
     ep.s1_scale = state->s1_scale; ep.s2_scale = state->s2_scale;
     ep.N = lin->N; ep.K = lin->K; ep.sc = sc; ep.seed = seed; ep.step = static_cast<uint64_t>(step);
+    ep.sr_base = sr_base;
     if ((e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "optimizer launch (T = 0)");
     return FORGE_OK;
@@ -597,6 +595,7 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
   p.seed = seed;
   philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
+  p.sr_base = sr_base;
   p.status = d.status;
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
@@ -615,6 +614,30 @@ forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_stat
       cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
+}
+
+}  // namespace
+}  // namespace forge
+
+using namespace forge;
+
+extern "C" {
+
+forge_status_t forge_linear_bwd_step(const forge_linear_t* lin, const forge_state_t* state,
+                                     int32_t opt_kind, const forge_hparams_t* hp, int64_t step,
+                                     uint64_t seed, void* stream) {
+  g_msg[0] = '\0';
+  return bwd_step(lin, state, opt_kind, hp, step, seed, 0, stream);
+}
+
+forge_status_t forge_linear_bwd_step_shard(const forge_linear_t* lin, const forge_state_t* state,
+                                           int32_t opt_kind, const forge_hparams_t* hp, int64_t step,
+                                           uint64_t seed, int64_t row_offset, void* stream) {
+  g_msg[0] = '\0';
+  if (row_offset < 0) return fail(FORGE_ERR_INVALID_ARG, "row_offset must be >= 0 (got %lld)", (long long)row_offset);
+  if (lin != nullptr && row_offset > (int64_t{1} << 31) - 1 - lin->N)
+    return fail(FORGE_ERR_UNSUPPORTED, "row_offset + N must fit in 31 bits");
+  return bwd_step(lin, state, opt_kind, hp, step, seed, row_offset, stream);
 }
 
 forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const forge_state_t* state,
@@ -638,7 +661,7 @@ forge_status_t forge_linear_bwd_step_static(const forge_linear_t* lin, const for
   if ((st = check_device(d)) != FORGE_OK) return st;
   if (d.step_pairs[kernel_sdt(state, lin->T)] <= 0)  // the one launch cannot be resident: no scratch
     return forge_linear_bwd_step(lin, state, opt_kind, hp, step, seed, stream);  // two launches
-  return launch_step(lin, state, opt_kind, make_scalars(opt_kind, *hp, step), step, seed,
+  return launch_step(lin, state, opt_kind, make_scalars(opt_kind, *hp, step), step, seed, 0,
                      static_cast<cudaStream_t>(stream), d, d.static_scratch);
 }
 

@@ -113,6 +113,10 @@ struct GemmParams {
   OptScalars sc;
   uint64_t seed;
   uint64_t step;
+  // Added to each 8-element group's index (element index / 8) in the
+  // stochastic-rounding counter: row_offset * K / 8 for a row shard of a
+  // larger matrix, so a shard draws the bits of its rows in the whole matrix.
+  uint64_t sr_base;
   // Philox4x32-10 round keys of `seed` (key words 0 and 1 of rounds 0..9),
   // formed once on the host for the stochastic rounding of the weights.
   uint32_t round_keys[20];

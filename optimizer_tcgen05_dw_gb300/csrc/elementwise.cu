@@ -113,7 +113,7 @@ __device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemPa
 #pragma unroll
     for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
     if (WDT == kWBf16) {
-      const uint4 r = dev::sr_words(static_cast<uint64_t>(e0) >> 3, p.seed, p.step);
+      const uint4 r = dev::sr_words((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.seed, p.step);
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)

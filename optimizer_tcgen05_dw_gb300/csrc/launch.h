@@ -20,6 +20,7 @@ struct ElemParams {
   int64_t N, K;      // rows, columns
   OptScalars sc;
   uint64_t seed, step;
+  uint64_t sr_base;  // added to each 8-element group's index in the rounding counter
   int32_t is_signed; // quantise / dequantise
 };
 

@@ -404,7 +404,7 @@ __device__ __forceinline__ void group8_fp32state(const float* g, int64_t e0, con
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
   if (WDT == kWBf16) {
-    const uint4 r = dev::sr_words_rk(static_cast<uint64_t>(e0) >> 3, p.step, p.round_keys);
+    const uint4 r = dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys);
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -555,7 +555,7 @@ __device__ __forceinline__ void epi_fused_int8_block(uint32_t tblock, int64_t ro
           o2[jj >> 2] |= (static_cast<uint32_t>(dev::quant<false>(s2, n2)) & 0xFFu) << (8 * (jj & 3));
       }
       if (WDT == kWBf16) {
-        const uint4 r = dev::sr_words_rk(static_cast<uint64_t>(e0) >> 3, p.step, p.round_keys);
+        const uint4 r = dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys);
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -754,7 +754,7 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
   if (SCALE) scale_grad(g, p);
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
-  wv = pack_sr_bf16x8(w, dev::sr_words_rk(static_cast<uint64_t>(e0) >> 3, p.step, p.round_keys));
+  wv = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys));
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     if (uses_s1(KIND))
@@ -791,7 +791,7 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
-  wv = pack_sr_bf16x8(w, dev::sr_words_rk(static_cast<uint64_t>(e0) >> 3, p.step, p.round_keys));
+  wv = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys));
   uint32_t o1[4], o2[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -843,7 +843,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
       if (uses_s1(KIND)) n1 = fmaxf(n1, fabsf(m[j]));  // = absmax_acc: n1 is never NaN
       if (uses_s2(KIND)) n2 = fmaxf(n2, fabsf(v[j]));
     }
-    wv[h] = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + h, p.step, p.round_keys));
+    wv[h] = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base + h, p.step, p.round_keys));
   }
   float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][quarter][row]
   amax[(0 * 4 + sub) * 128 + r] = n1;
