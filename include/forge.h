@@ -76,16 +76,23 @@ typedef enum forge_opt_kind {
 typedef enum forge_wdtype { FORGE_W_FP32 = 0, FORGE_W_BF16_SR = 1 } forge_wdtype_t;
 
 /* State storage (§2 "Precision and Fidelity", last bullet): FP32, or INT8
- * codes in blocks of 64 contiguous elements of a row with one FP32 absmax per
- * block.  s1 (may be negative) is int8 with codes -127..127 and value
+ * codes in blocks of B contiguous elements of a row with one FP32 absmax per
+ * block -- B = 64 is the pages' block size; 32, 128 and 256, the other widths
+ * that stay inside one 256-column tile pair, exist to measure the pages'
+ * block-size claim (64 against the 2048 of standard 8-bit optimizers).  s1
+ * (may be negative) is int8 with codes -127..127 and value
  * code * (absmax/127); s2 (never negative) is uint8 with codes 0..255 and value
- * code * (absmax/255).  Scale arrays are [N x K/64] FP32. */
+ * code * (absmax/255).  Scale arrays are [N x K/B] FP32; K % 64 == 0 and
+ * K % B == 0.  With fp32 weights the fused step (T > 0) takes B = 64 only. */
 typedef enum forge_sdtype {
   FORGE_STATE_FP32 = 0,      /* float32 moments                                           */
   FORGE_STATE_INT8_B64 = 1,  /* int8 / uint8 codes, float32 absmax per 64 row elements     */
-  FORGE_STATE_BF16 = 2       /* bf16 moments, rounded to nearest even after the FP32 rule; */
+  FORGE_STATE_BF16 = 2,      /* bf16 moments, rounded to nearest even after the FP32 rule; */
                              /* with fp32 weights only the optimizer-only entry points and */
                              /* T = 0 accept them (the fused kernels stage bf16 weights)    */
+  FORGE_STATE_INT8_B32 = 3,  /* as INT8_B64 with one absmax per 32 row elements            */
+  FORGE_STATE_INT8_B128 = 4, /* ... per 128 row elements                                    */
+  FORGE_STATE_INT8_B256 = 5  /* ... per 256 row elements                                    */
 } forge_sdtype_t;
 
 /* The activations of one linear layer. */
@@ -103,8 +110,8 @@ typedef struct forge_state {
   int32_t s_dtype;     /* forge_sdtype_t                                        */
   void* s1;            /* [N x K] fp32 or int8, or NULL if the rule keeps none  */
   void* s2;            /* [N x K] fp32 or uint8, or NULL if the rule keeps none */
-  float* s1_scale;     /* [N x K/64] fp32 absmax, INT8 only (else NULL)         */
-  float* s2_scale;     /* [N x K/64] fp32 absmax, INT8 only (else NULL)         */
+  float* s1_scale;     /* [N x K/B] fp32 absmax, INT8 only (else NULL)          */
+  float* s2_scale;     /* [N x K/B] fp32 absmax, INT8 only (else NULL)          */
 } forge_state_t;
 
 /* Hyper-parameters; fields a rule does not use are ignored.
@@ -220,7 +227,7 @@ typedef struct forge_linear_fp8 {
  * formed in double and rounded once to float, and the rule `opt_kind` is
  * applied exactly as in forge_linear_bwd_step.  BF16 weights (stochastic
  * rounding) only: FP32 weights return FORGE_ERR_UNSUPPORTED.  States: FP32,
- * INT8 blocks of 64 or BF16.  No dX is computed: call forge_linear_dgrad
+ * INT8 blocks (any width) or BF16.  No dX is computed: call forge_linear_dgrad
  * first on the same stream (it reads the weights before this call updates
  * them).  T == 0 applies the rule to a zero gradient.  Requirements as in
  * the shared conventions plus T % 16 == 0 and finite scales; NaN codes
@@ -259,6 +266,16 @@ FORGE_API forge_status_t forge_quantize_state(const float* x, void* codes, float
 FORGE_API forge_status_t forge_dequantize_state(const void* codes, const float* absmax, float* x,
                                       int64_t rows, int64_t cols, int32_t is_signed,
                                       void* stream);
+/* The same two helpers for blocks of `block` (32, 64, 128 or 256) row
+ * elements: absmax is [rows x cols/block]; cols % 64 == 0 and
+ * cols % block == 0, else FORGE_ERR_INVALID_ARG. */
+FORGE_API forge_status_t forge_quantize_state_block(const float* x, void* codes, float* absmax,
+                                                    int64_t rows, int64_t cols, int32_t is_signed,
+                                                    int32_t block, void* stream);
+FORGE_API forge_status_t forge_dequantize_state_block(const void* codes, const float* absmax,
+                                                      float* x, int64_t rows, int64_t cols,
+                                                      int32_t is_signed, int32_t block,
+                                                      void* stream);
 
 /* Synchronises `stream`, then returns and clears the current device's status
  * word: FORGE_OK, FORGE_ERR_TIMEOUT (a bounded wait expired in a kernel) or

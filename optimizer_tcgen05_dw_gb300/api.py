@@ -22,6 +22,9 @@ OPT_KINDS = {"adamw": 0, "nadam": 1, "radam": 2, "lion": 3, "rmsprop": 4, "adagr
              "sgd": 6, "sgd_momentum": 7}
 W_FP32, W_BF16_SR = 0, 1
 STATE_FP32, STATE_INT8_B64, STATE_BF16 = 0, 1, 2
+STATE_INT8_B32, STATE_INT8_B128, STATE_INT8_B256 = 3, 4, 5
+INT8_STATE_OF_BLOCK = {32: STATE_INT8_B32, 64: STATE_INT8_B64, 128: STATE_INT8_B128,
+                       256: STATE_INT8_B256}
 USES_S1 = {"adamw", "nadam", "radam", "lion", "sgd_momentum"}
 USES_S2 = {"adamw", "nadam", "radam", "rmsprop", "adagrad"}
 
@@ -84,6 +87,10 @@ _SIGNATURES = {
                                        c_void_p]),
     "forge_dequantize_state": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32,
                                          c_void_p]),
+    "forge_quantize_state_block": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32,
+                                             c_int32, c_void_p]),
+    "forge_dequantize_state_block": (c_int32, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int32,
+                                               c_int32, c_void_p]),
     "forge_get_device_status": (c_int32, [c_void_p]),
     "forge_set_wait_limit_ns": (c_int32, [c_uint64]),
     "forge_debug_skip_loads": (c_int32, [c_int32]),
@@ -173,19 +180,26 @@ def make_state(W, s1=None, s2=None, s1_scale=None, s2_scale=None) -> ForgeState:
             if t is not None:
                 _need(t, nm, torch.bfloat16, (N, K))
         return ForgeState(_ptr(W), wdt, STATE_BF16, _ptr(s1), _ptr(s2), None, None)
+    sdt = STATE_FP32
     if int8:
+        # the block width follows from the scale arrays: [N, K / block]
+        sc = s1_scale if s1_scale is not None else s2_scale
+        if sc is None or sc.dim() != 2 or sc.shape[1] == 0 or K % sc.shape[1] != 0 \
+                or K // sc.shape[1] not in INT8_STATE_OF_BLOCK:
+            raise ValueError("INT8 states need [N, K / B] float32 scales with B in 32, 64, 128, 256")
+        block = K // sc.shape[1]
+        sdt = INT8_STATE_OF_BLOCK[block]
         if s1 is not None:
             _need(s1, "s1", torch.int8, (N, K))
-            _need(s1_scale, "s1_scale", torch.float32, (N, K // 64))
+            _need(s1_scale, "s1_scale", torch.float32, (N, K // block))
         if s2 is not None:
             _need(s2, "s2", torch.uint8, (N, K))
-            _need(s2_scale, "s2_scale", torch.float32, (N, K // 64))
+            _need(s2_scale, "s2_scale", torch.float32, (N, K // block))
     else:
         for t, nm in ((s1, "s1"), (s2, "s2")):
             if t is not None:
                 _need(t, nm, torch.float32, (N, K))
-    return ForgeState(_ptr(W), wdt, STATE_INT8_B64 if int8 else STATE_FP32, _ptr(s1), _ptr(s2),
-                      _ptr(s1_scale), _ptr(s2_scale))
+    return ForgeState(_ptr(W), wdt, sdt, _ptr(s1), _ptr(s2), _ptr(s1_scale), _ptr(s2_scale))
 
 
 def forge_linear_bwd_step(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1=None, s2=None,
@@ -294,22 +308,23 @@ def forge_unfused_opt_step(dW, W, opt: str, hp: dict, step: int, seed: int, s1=N
                                         int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
-def forge_quantize_state(x, codes, absmax, is_signed: bool, stream=None):
+def forge_quantize_state(x, codes, absmax, is_signed: bool, stream=None, block: int = 64):
+    """x fp32 [rows, cols] -> INT8 codes and absmax [rows, cols / block]."""
     rows, cols = x.shape
     _need(x, "x", torch.float32, (rows, cols))
     _need(codes, "codes", torch.int8 if is_signed else torch.uint8, (rows, cols))
-    _need(absmax, "absmax", torch.float32, (rows, cols // 64))
-    _check(lib().forge_quantize_state(_ptr(x), _ptr(codes), _ptr(absmax), rows, cols,
-                                      1 if is_signed else 0, _stream(stream)))
+    _need(absmax, "absmax", torch.float32, (rows, cols // block))
+    _check(lib().forge_quantize_state_block(_ptr(x), _ptr(codes), _ptr(absmax), rows, cols,
+                                            1 if is_signed else 0, int(block), _stream(stream)))
 
 
-def forge_dequantize_state(codes, absmax, x, is_signed: bool, stream=None):
+def forge_dequantize_state(codes, absmax, x, is_signed: bool, stream=None, block: int = 64):
     rows, cols = x.shape
     _need(x, "x", torch.float32, (rows, cols))
     _need(codes, "codes", torch.int8 if is_signed else torch.uint8, (rows, cols))
-    _need(absmax, "absmax", torch.float32, (rows, cols // 64))
-    _check(lib().forge_dequantize_state(_ptr(codes), _ptr(absmax), _ptr(x), rows, cols,
-                                        1 if is_signed else 0, _stream(stream)))
+    _need(absmax, "absmax", torch.float32, (rows, cols // block))
+    _check(lib().forge_dequantize_state_block(_ptr(codes), _ptr(absmax), _ptr(x), rows, cols,
+                                              1 if is_signed else 0, int(block), _stream(stream)))
 
 
 def forge_get_device_status(stream=None):

@@ -68,7 +68,7 @@ struct DeviceInfo {
   uint32_t* status = nullptr;
   uint32_t* dx_done = nullptr;
   uint32_t* static_scratch = nullptr;  // g_static_scratch on this device
-  int step_pairs[4] = {0, 0, 0, 0};  // resident one-launch-step pairs, by kernel state dtype
+  int step_pairs[kNumKernelSdt] = {};  // resident one-launch-step pairs, by kernel state dtype
   int cc_major = 0, cc_minor = 0;
 };
 
@@ -103,6 +103,8 @@ forge_status_t device_info(DeviceInfo* out) {
       d.step_pairs[kSInt8] = step_max_pairs(kSInt8);
       d.step_pairs[kSBf16] = step_max_pairs(kSBf16);
       d.step_pairs[kSInt8W] = step_max_pairs(kSInt8W);
+      d.step_pairs[kSInt8X] = step_max_pairs(kSInt8X);
+      d.step_pairs[kSInt8WX] = step_max_pairs(kSInt8WX);
     }
     g_dev[dev] = d;
     g_dev_ready[dev] = true;
@@ -206,6 +208,21 @@ forge_status_t wgrad_maps(const forge_linear_t* lin, int bk, CUtensorMap* ma, CU
   return bf16_map(mb, lin->X, lin->K, lin->T, 64, bk);
 }
 
+// INT8 states: the absmax block width of a state dtype (0 if not INT8).
+int qblock_of(int32_t s_dtype) {
+  switch (s_dtype) {
+    case FORGE_STATE_INT8_B32: return 32;
+    case FORGE_STATE_INT8_B64: return 64;
+    case FORGE_STATE_INT8_B128: return 128;
+    case FORGE_STATE_INT8_B256: return 256;
+    default: return 0;
+  }
+}
+
+// The kernels' state dtype (every INT8 block width is kSInt8; the block width
+// travels in the parameters).
+int base_sdt(int32_t s_dtype) { return qblock_of(s_dtype) != 0 ? kSInt8 : s_dtype; }
+
 // Maps of the state tiles the bf16-weight epilogue stages through shared
 // memory: fp32 states in 32-column boxes (128-byte rows, 128-byte swizzle),
 // INT8 codes in 64-column boxes and bf16 states in 32-column boxes (64-byte
@@ -214,7 +231,7 @@ forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t 
                           const CUtensorMap& other, CUtensorMap* m1, CUtensorMap* m2) {
   *m1 = other;
   *m2 = other;
-  const bool int8 = st->s_dtype == FORGE_STATE_INT8_B64;
+  const bool int8 = qblock_of(st->s_dtype) != 0;
   const void* bufs[2] = {st->s1, st->s2};
   const bool used[2] = {uses_s1(kind), uses_s2(kind)};
   CUtensorMap* maps[2] = {m1, m2};
@@ -235,11 +252,24 @@ forge_status_t state_maps(const forge_state_t* st, int kind, int64_t N, int64_t 
 
 // The state dtype the tensor-core kernel is instantiated for: INT8 states
 // over a short reduction (T <= kStageWeightsMaxT) with bf16 weights take the
-// epilogue that stages the weights too.
+// epilogue that stages the weights too; INT8 blocks other than 64 the
+// variants that read the block width from the parameters.
 int kernel_sdt(const forge_state_t* st, int64_t T) {
-  if (st->s_dtype == FORGE_STATE_INT8_B64 && st->w_dtype == FORGE_W_BF16_SR && T <= kStageWeightsMaxT)
-    return kSInt8W;
-  return st->s_dtype;
+  const int qb = qblock_of(st->s_dtype);
+  if (qb != 0 && st->w_dtype == FORGE_W_BF16_SR) {
+    const bool staged = T <= kStageWeightsMaxT;
+    if (qb == 64) return staged ? kSInt8W : kSInt8;
+    return staged ? kSInt8WX : kSInt8X;
+  }
+  return base_sdt(st->s_dtype);
+}
+
+// log2 of an INT8 block width (0 when not INT8).
+int qshift_of(int32_t s_dtype) {
+  const int qb = qblock_of(s_dtype);
+  int sh = 0;
+  while (qb > 0 && (1 << sh) < qb) ++sh;
+  return sh;
 }
 
 // The bf16 weights in 64-column x 128-row boxes (128-byte swizzle), for the
@@ -247,7 +277,7 @@ int kernel_sdt(const forge_state_t* st, int64_t T) {
 forge_status_t weight_map(const forge_state_t* st, int sdt, int64_t N, int64_t K, const CUtensorMap& other,
                           CUtensorMap* mw) {
   *mw = other;
-  if (sdt == kSInt8W) return bf16_map(mw, st->W, K, N, 64, kTileM);
+  if (sdt == kSInt8W || sdt == kSInt8WX) return bf16_map(mw, st->W, K, N, 64, kTileM);
   return FORGE_OK;
 }
 
@@ -342,13 +372,17 @@ forge_status_t check_state(const forge_state_t* st, int kind, int64_t N, int64_t
   if (st == nullptr) return fail(FORGE_ERR_INVALID_ARG, "state is NULL");
   if (st->w_dtype != FORGE_W_FP32 && st->w_dtype != FORGE_W_BF16_SR)
     return fail(FORGE_ERR_INVALID_ARG, "w_dtype %d", st->w_dtype);
-  if (st->s_dtype != FORGE_STATE_FP32 && st->s_dtype != FORGE_STATE_INT8_B64 &&
-      st->s_dtype != FORGE_STATE_BF16)
+  if (st->s_dtype != FORGE_STATE_FP32 && st->s_dtype != FORGE_STATE_BF16 && qblock_of(st->s_dtype) == 0)
     return fail(FORGE_ERR_INVALID_ARG, "s_dtype %d", st->s_dtype);
   if (N * K > 0 && (st->W == nullptr || !aligned16(st->W)))
     return fail(FORGE_ERR_INVALID_ARG, "W must be a non-NULL 16-byte aligned device pointer");
-  const bool int8 = st->s_dtype == FORGE_STATE_INT8_B64;
-  if (int8 && K % 64 != 0) return fail(FORGE_ERR_INVALID_ARG, "INT8 states need K %% 64 == 0 (K=%lld)", (long long)K);
+  const int qb = qblock_of(st->s_dtype);
+  const bool int8 = qb != 0;
+  if (int8 && K % qb != 0)
+    return fail(FORGE_ERR_INVALID_ARG, "INT8 states in blocks of %d need K %% %d == 0 (K=%lld)", qb, qb,
+                (long long)K);
+  if (int8 && K % 64 != 0)
+    return fail(FORGE_ERR_INVALID_ARG, "INT8 states need K %% 64 == 0 (K=%lld)", (long long)K);
   if (N * K == 0) return FORGE_OK;
   if (uses_s1(kind)) {
     if (st->s1 == nullptr || !aligned16(st->s1))
@@ -509,6 +543,8 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
+  p.qblock = qblock_of(state->s_dtype);
+  p.qshift = qshift_of(state->s_dtype);
   p.seed = seed;
   philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
@@ -554,6 +590,9 @@ forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, i
   if (lin->N == 0 || lin->K == 0) return FORGE_OK;
   if (state->s_dtype == FORGE_STATE_BF16 && state->w_dtype == FORGE_W_FP32 && lin->T > 0)
     return fail(FORGE_ERR_UNSUPPORTED, "bf16 moments need bf16 weights in the fused step");
+  if (state->w_dtype == FORGE_W_FP32 && lin->T > 0 && qblock_of(state->s_dtype) != 0 &&
+      qblock_of(state->s_dtype) != 64)
+    return fail(FORGE_ERR_UNSUPPORTED, "INT8 blocks other than 64 need bf16 weights in the fused step");
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
   if ((st = check_device(d)) != FORGE_OK) return st;
@@ -578,7 +617,8 @@ forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, i
     ep.s1_scale = state->s1_scale; ep.s2_scale = state->s2_scale;
     ep.N = lin->N; ep.K = lin->K; ep.sc = sc; ep.seed = seed; ep.step = static_cast<uint64_t>(step);
     ep.sr_base = sr_base;
-    if ((e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, s)) != cudaSuccess)
+    ep.qblock = qblock_of(state->s_dtype);
+    if ((e = launch_opt_step(state->w_dtype, base_sdt(state->s_dtype), ep, d.num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "optimizer launch (T = 0)");
     return FORGE_OK;
   }
@@ -592,6 +632,8 @@ forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, i
   p.W = state->W; p.s1 = state->s1; p.s2 = state->s2;
   p.s1_scale = state->s1_scale; p.s2_scale = state->s2_scale;
   p.sc = sc;
+  p.qblock = qblock_of(state->s_dtype);
+  p.qshift = qshift_of(state->s_dtype);
   p.seed = seed;
   philox_round_keys(seed, p.round_keys);
   p.step = static_cast<uint64_t>(step);
@@ -604,7 +646,7 @@ forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, i
     if ((st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK ||
         (st = weight_map(state, kernel_sdt(state, lin->T), lin->N, lin->K, ma, &mw)) != FORGE_OK)
       return st;
-    split_tail(p, d.num_sms / 2);
+    if (p.qblock != 256) split_tail(p, d.num_sms / 2);  // a 256-column block spans both halves
     if (p.split_from < p.num_tiles && p.op3d &&  // half units load one 64-column block of X
         (st = mn_major_3d_map(&mbh, lin->X, lin->K, lin->T, bk, 1)) != FORGE_OK)
       return st;
@@ -705,7 +747,8 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
     ep.W = state->W; ep.s1 = state->s1; ep.s2 = state->s2;
     ep.s1_scale = state->s1_scale; ep.s2_scale = state->s2_scale;
     ep.N = N; ep.K = K; ep.sc = sc; ep.seed = seed; ep.step = static_cast<uint64_t>(step);
-    if ((e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, s)) != cudaSuccess)
+    ep.qblock = qblock_of(state->s_dtype);
+    if ((e = launch_opt_step(state->w_dtype, base_sdt(state->s_dtype), ep, d.num_sms, s)) != cudaSuccess)
       return cuda_fail(e, "optimizer launch (T = 0)");
     return FORGE_OK;
   }
@@ -724,7 +767,9 @@ forge_status_t forge_linear_bwd_step_fp8(const forge_linear_fp8_t* lin, const fo
   GemmParams p;
   std::memset(&p, 0, sizeof(p));
   fill_tiles(p, N, K, T, kFp8BlockK);
-  split_tail(p, d.num_sms / 2);
+  p.qblock = qblock_of(state->s_dtype);
+  p.qshift = qshift_of(state->s_dtype);
+  if (p.qblock != 256) split_tail(p, d.num_sms / 2);  // a 256-column block spans both halves
   CUtensorMap mbh = mb;
   if (p.split_from < p.num_tiles &&  // half units load 64 rows of X^T
       (st = tensor_map(&mbh, lin->Xt, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, T, K, kFp8BlockK, kTileN / 4,
@@ -812,41 +857,46 @@ forge_status_t forge_unfused_opt_step(const float* dW, const forge_state_t* stat
   ep.sc = make_scalars(opt_kind, *hp, step);
   ep.seed = seed;
   ep.step = static_cast<uint64_t>(step);
-  cudaError_t e = launch_opt_step(state->w_dtype, state->s_dtype, ep, d.num_sms, static_cast<cudaStream_t>(stream));
+  ep.qblock = qblock_of(state->s_dtype);
+  cudaError_t e = launch_opt_step(state->w_dtype, base_sdt(state->s_dtype), ep, d.num_sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "optimizer launch");
   return FORGE_OK;
 }
 
 static forge_status_t quant_common(const void* a, const void* b, const float* absmax, int64_t rows,
-                                   int64_t cols) {
-  if (rows < 0 || cols < 0 || cols % 64 != 0) return fail(FORGE_ERR_INVALID_ARG, "need cols %% 64 == 0");
+                                   int64_t cols, int32_t block = 64) {
+  if (block != 32 && block != 64 && block != 128 && block != 256)
+    return fail(FORGE_ERR_INVALID_ARG, "block must be 32, 64, 128 or 256 (got %d)", block);
+  if (rows < 0 || cols < 0 || cols % 64 != 0 || cols % block != 0)
+    return fail(FORGE_ERR_INVALID_ARG, "need cols %% 64 == 0 and cols %% block == 0");
   if (rows * cols == 0) return FORGE_OK;
   if (a == nullptr || b == nullptr || absmax == nullptr || !aligned16(a) || !aligned16(b))
     return fail(FORGE_ERR_INVALID_ARG, "NULL or misaligned pointer");
   return FORGE_OK;
 }
 
-forge_status_t forge_quantize_state(const float* x, void* codes, float* absmax, int64_t rows, int64_t cols,
-                                    int32_t is_signed, void* stream) {
+forge_status_t forge_quantize_state_block(const float* x, void* codes, float* absmax, int64_t rows,
+                                          int64_t cols, int32_t is_signed, int32_t block, void* stream) {
   g_msg[0] = '\0';
   forge_status_t st;
-  if ((st = quant_common(x, codes, absmax, rows, cols)) != FORGE_OK) return st;
+  if ((st = quant_common(x, codes, absmax, rows, cols, block)) != FORGE_OK) return st;
   if (rows * cols == 0) return FORGE_OK;
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
   ElemParams ep;
   std::memset(&ep, 0, sizeof(ep));
   ep.dW = x; ep.s1 = codes; ep.s1_scale = absmax; ep.N = rows; ep.K = cols; ep.is_signed = is_signed ? 1 : 0;
+  ep.qblock = block;
   cudaError_t e = launch_quantize(ep, d.num_sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return FORGE_OK;
 }
 
-forge_status_t forge_dequantize_state(const void* codes, const float* absmax, float* x, int64_t rows,
-                                      int64_t cols, int32_t is_signed, void* stream) {
+forge_status_t forge_dequantize_state_block(const void* codes, const float* absmax, float* x, int64_t rows,
+                                            int64_t cols, int32_t is_signed, int32_t block, void* stream) {
   g_msg[0] = '\0';
   forge_status_t st;
-  if ((st = quant_common(x, codes, absmax, rows, cols)) != FORGE_OK) return st;
+  if ((st = quant_common(x, codes, absmax, rows, cols, block)) != FORGE_OK) return st;
   if (rows * cols == 0) return FORGE_OK;
   DeviceInfo d;
   if ((st = device_info(&d)) != FORGE_OK) return st;
@@ -854,9 +904,20 @@ forge_status_t forge_dequantize_state(const void* codes, const float* absmax, fl
   std::memset(&ep, 0, sizeof(ep));
   ep.W = x; ep.s1 = const_cast<void*>(codes); ep.s1_scale = const_cast<float*>(absmax);
   ep.N = rows; ep.K = cols; ep.is_signed = is_signed ? 1 : 0;
+  ep.qblock = block;
   cudaError_t e = launch_dequantize(ep, d.num_sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "dequantize launch");
   return FORGE_OK;
+}
+
+forge_status_t forge_quantize_state(const float* x, void* codes, float* absmax, int64_t rows, int64_t cols,
+                                    int32_t is_signed, void* stream) {
+  return forge_quantize_state_block(x, codes, absmax, rows, cols, is_signed, 64, stream);
+}
+
+forge_status_t forge_dequantize_state(const void* codes, const float* absmax, float* x, int64_t rows,
+                                      int64_t cols, int32_t is_signed, void* stream) {
+  return forge_dequantize_state_block(codes, absmax, x, rows, cols, is_signed, 64, stream);
 }
 
 forge_status_t forge_get_device_status(void* stream) {

@@ -15,7 +15,12 @@ enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1, kSBf16 = 2,
                         // INT8 states with the bf16 weights staged through shared
                         // memory by TMA (kernel-side only; the host picks it for
                         // short reductions, T <= kStageWeightsMaxT)
-                        kSInt8W = 3 };
+                        kSInt8W = 3,
+                        // kSInt8 / kSInt8W with the absmax block width read from
+                        // the parameters (32, 128 or 256 columns); the two above
+                        // are compiled for the method's block of 64
+                        kSInt8X = 4, kSInt8WX = 5 };
+constexpr int kNumKernelSdt = 6;
 // Longest reduction for which the INT8 epilogue stages the weights: it frees
 // the compute warps from row-strided weight accesses (+40 % at T = 4096) but
 // costs an operand stage, which a long main loop needs (-5 % at T = 16384).
@@ -143,6 +148,9 @@ struct GemmParams {
   // kModeFusedFp8: the accumulated sum of code products times gscale
   // (= x_scale * dy_scale) is the gradient.
   float gscale;
+  // INT8 states: elements per absmax block along a row (32, 64, 128 or 256;
+  // the scale arrays are [M x Ncols / qblock]) and its base-2 logarithm.
+  int32_t qblock, qshift;
 };
 
 }  // namespace forge

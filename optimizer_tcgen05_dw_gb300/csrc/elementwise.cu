@@ -9,8 +9,8 @@
 // Layout of work: each thread owns 8 consecutive elements of a row (one
 // Philox call, 16/32-byte vector accesses; consecutive threads own
 // consecutive groups, so a warp touches 256 contiguous elements).  For INT8
-// states the 8 threads of a block of 64 share the block's absmax through
-// warp shuffles.
+// states the qblock/8 threads of a block (4, 8, 16 or 32 lanes for blocks of
+// 32, 64, 128 or 256) share the block's absmax through warp shuffles.
 #include <cuda_bf16.h>
 
 #include "launch.h"
@@ -33,11 +33,10 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-// Max over the 8 lanes of an aligned lane group (all 32 lanes call it).
-__device__ __forceinline__ float group8_max(float a) {
-  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
-  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
-  a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 4));
+// Max over the `lanes` lanes (a power of two up to 32) of an aligned lane
+// group; all 32 lanes call it.
+__device__ __forceinline__ float group_max(float a, int lanes) {
+  for (int o = 1; o < lanes; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
   return a;
 }
 
@@ -86,7 +85,8 @@ __device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemPa
   float g[8], w[8], s1[8], s2[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) { g[j] = 0.f; w[j] = 0.f; s1[j] = 0.f; s2[j] = 0.f; }
-  const int64_t sidx = e0 / 64;  // block index (rows hold K/64 whole blocks)
+  // block index (rows hold K/qblock whole blocks)
+  const int64_t sidx = SDT == kSInt8 ? e0 / p.qblock : 0;
   if (active) {
     if (p.dW != nullptr) load8(p.dW + e0, g);
     if (WDT == kWBf16) {
@@ -140,10 +140,10 @@ __device__ __forceinline__ void opt_group(int64_t gid, bool active, const ElemPa
       n1 = dev::absmax_acc(n1, s1[j]);
       n2 = dev::absmax_acc(n2, s2[j]);
     }
-    if (uses_s1(KIND)) n1 = group8_max(n1);
-    if (uses_s2(KIND)) n2 = group8_max(n2);
+    if (uses_s1(KIND)) n1 = group_max(n1, p.qblock / 8);
+    if (uses_s2(KIND)) n2 = group_max(n2, p.qblock / 8);
     if (active) {
-      const bool leader = (gid & 7) == 0;
+      const bool leader = (gid & (p.qblock / 8 - 1)) == 0;
       if (uses_s1(KIND)) {
         store_codes8<true>(p.s1, e0, n1, s1);
         if (leader) p.s1_scale[sidx] = n1;
@@ -194,10 +194,10 @@ __global__ void __launch_bounds__(kElemThreads) quantize_kernel(const ElemParams
     float a = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) a = dev::absmax_acc(a, v[j]);
-    a = group8_max(a);
+    a = group_max(a, p.qblock / 8);
     if (active) {
       store_codes8<SIGNED>(p.s1, gid * 8, a, v);
-      if ((gid & 7) == 0) p.s1_scale[gid / 8] = a;
+      if ((gid & (p.qblock / 8 - 1)) == 0) p.s1_scale[gid * 8 / p.qblock] = a;
     }
   }
 }
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kElemThreads) dequantize_kernel(const ElemPara
   for (int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; gid < groups;
        gid += stride) {
     float v[8];
-    load_codes8<SIGNED>(p.s1, gid * 8, p.s1_scale[gid / 8], v);
+    load_codes8<SIGNED>(p.s1, gid * 8, p.s1_scale[gid * 8 / p.qblock], v);
     store8(static_cast<float*>(p.W) + gid * 8, v);
   }
 }

@@ -22,6 +22,7 @@ struct ElemParams {
   uint64_t seed, step;
   uint64_t sr_base;  // added to each 8-element group's index in the rounding counter
   int32_t is_signed; // quantise / dequantise
+  int32_t qblock;    // INT8 states: elements per absmax block (32, 64, 128 or 256)
 };
 
 // tc_fused.cu: the FORGE step (mode kModeFusedOpt) for one (W dtype, state dtype).

@@ -19,10 +19,12 @@ cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtens
                             const CUtensorMap& bh, const CUtensorMap& s1, const CUtensorMap& s2,
                             const CUtensorMap& w, const GemmParams& p, int grid, cudaStream_t s) {
   if (wdt == kWBf16) {
-    return sdt == kSInt8    ? run_fused<kWBf16, kSInt8>(a, b, bh, s1, s2, w, p, grid, s)
-           : sdt == kSInt8W ? run_fused<kWBf16, kSInt8W>(a, b, bh, s1, s2, w, p, grid, s)
-           : sdt == kSBf16  ? run_fused<kWBf16, kSBf16>(a, b, bh, s1, s2, w, p, grid, s)
-                           : run_fused<kWBf16, kSFp32>(a, b, bh, s1, s2, w, p, grid, s);
+    return sdt == kSInt8     ? run_fused<kWBf16, kSInt8>(a, b, bh, s1, s2, w, p, grid, s)
+           : sdt == kSInt8W  ? run_fused<kWBf16, kSInt8W>(a, b, bh, s1, s2, w, p, grid, s)
+           : sdt == kSInt8X  ? run_fused<kWBf16, kSInt8X>(a, b, bh, s1, s2, w, p, grid, s)
+           : sdt == kSInt8WX ? run_fused<kWBf16, kSInt8WX>(a, b, bh, s1, s2, w, p, grid, s)
+           : sdt == kSBf16   ? run_fused<kWBf16, kSBf16>(a, b, bh, s1, s2, w, p, grid, s)
+                             : run_fused<kWBf16, kSFp32>(a, b, bh, s1, s2, w, p, grid, s);
   }
   return sdt == kSInt8 ? run_fused<kWFp32, kSInt8>(a, b, bh, s1, s2, w, p, grid, s)
                        : run_fused<kWFp32, kSFp32>(a, b, bh, s1, s2, w, p, grid, s);

@@ -82,7 +82,7 @@ constexpr int kEpiBufBytes = 32768;
 // INT8 states stage the bf16 weight chunk too (see StagedGeom): a larger
 // buffer, and one operand stage fewer to make room.
 constexpr int kEpiBufBytesW = 37888;
-__host__ __device__ constexpr bool stages_weights(int sdt) { return sdt == kSInt8W; }
+__host__ __device__ constexpr bool stages_weights(int sdt) { return sdt == kSInt8W || sdt == kSInt8WX; }
 constexpr int kEpiBarrier = 1;       // named barrier of the epilogue warps
 constexpr int kEpiInnerBarrier = 2;  // the staged epilogue's compute warps only
 constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
@@ -119,6 +119,8 @@ static_assert(KCfg<kModeDgrad, kWBf16>::kSmem <= 232448, "dynamic shared memory 
 static_assert(KCfg<kModeFusedFp8, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeStep, kWBf16, kSInt8W>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeFusedFp8, kWBf16, kSInt8W>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeStep, kWBf16, kSInt8WX>::kSmem == KCfg<kModeStep, kWBf16, kSInt8W>::kSmem,
+              "block-width variants share the layout");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -804,16 +806,18 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
     *reinterpret_cast<uint4*>(buf + kOffS2 + sw64(r, sub)) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
 }
 
-// INT8 states: a chunk is 128 rows x 64 columns (one code block per row;
-// codes 8 KiB per state in shared memory); this thread owns 16 columns (a
-// quarter block) of row r, its 16 bf16 weights in registers (`wv`).  The new
-// block absmax combines the four quarters through shared memory; the weights
-// use the new float32 moments, then the moments are quantised with the new
-// absmax.
+// INT8 states: a chunk is 128 rows x 64 columns (codes 8 KiB per state in
+// shared memory); this thread owns 16 columns (a quarter) of row r, its 16
+// bf16 weights in registers (`wv`).  The new block absmax of a 64-column block
+// combines the four quarters through shared memory, of a 32-column block the
+// two quarters it spans; blocks of 128 or 256 columns span several chunks and
+// arrive found already (wide1, wide2: int8_wide_absmax).  The weights use the
+// new float32 moments, then the moments are quantised with the new absmax.
 template <int KIND, bool SCALE>
 __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int r, int sub,
                                                int64_t e0, uint4 (&wv)[2], float a1, float a2,
                                                float* n1_out, float* n2_out, int nthreads,
+                                               int qb, float wide1, float wide2,
                                                const GemmParams& p) {
   constexpr int kOffS1 = 0, kOffS2 = 8192, kOffAmax = 16384;
   float m[16], v[16];  // the new moments stay live until the block absmax is known
@@ -845,14 +849,20 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
     }
     wv[h] = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base + h, p.step, p.round_keys));
   }
-  float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][quarter][row]
-  amax[(0 * 4 + sub) * 128 + r] = n1;
-  amax[(1 * 4 + sub) * 128 + r] = n2;
-  ptx::bar_sync(kEpiInnerBarrier, nthreads);
-#pragma unroll
-  for (int o = 0; o < 4; ++o) {
-    n1 = fmaxf(n1, amax[(0 * 4 + o) * 128 + r]);
-    n2 = fmaxf(n2, amax[(1 * 4 + o) * 128 + r]);
+  if (qb > 64) {  // the block spans chunks: its absmax was found ahead
+    n1 = wide1;
+    n2 = wide2;
+  } else {
+    float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][quarter][row]
+    amax[(0 * 4 + sub) * 128 + r] = n1;
+    amax[(1 * 4 + sub) * 128 + r] = n2;
+    ptx::bar_sync(kEpiInnerBarrier, nthreads);
+    const int o0 = qb == 32 ? (sub & 2) : 0, on = qb == 32 ? 2 : 4;  // quarters of the block
+#pragma unroll 1
+    for (int o = o0; o < o0 + on; ++o) {
+      n1 = fmaxf(n1, amax[(0 * 4 + o) * 128 + r]);
+      n2 = fmaxf(n2, amax[(1 * 4 + o) * 128 + r]);
+    }
   }
   // New codes (dev::quant_recip's rule): round x * (1/s) with the shifter;
   // the few near a half-integer, and every code of a block whose reciprocal
@@ -888,6 +898,111 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   *n2_out = n2;
 }
 
+// INT8 states with blocks wider than a chunk (qb = 128 or 256 columns): the
+// new absmax of each block of this thread's row in the unit (a pair tile's
+// 256 columns, or a 128-column half), found before its chunks are quantised.
+// The thread forms the new moments of its 16 columns of each of the unit's
+// `nch` chunks with the arithmetic of epi_chunk_int8, reading the old codes,
+// scales and (for rules whose moments depend on the weights) weights straight
+// from global memory, all still unchanged; the four column quarters of a row
+// then combine their maxima in shared memory (`amax`, 1024 floats of the
+// chunk's buffer).  The results go to the first 512 floats of both buffers'
+// regions (`amax` and `amax_other`), [state][block b of the unit][row]: two
+// blocks of 128 in a whole unit, else one.
+template <int KIND, bool SCALE>
+__device__ __forceinline__ void int8_wide_absmax(uint32_t tunit, int64_t row, int col0, int nch, int r,
+                                                 int sub, int qs, float* amax, float* amax_other,
+                                                 int nthreads, const GemmParams& p) {
+  const int64_t K = p.Ncols;
+  const bool need_w = (KIND != kAdamW && KIND != kLion) && p.sc.l2 != 0.f;
+  float l1a = 0.f, l1b = 0.f, l2a = 0.f, l2b = 0.f;  // blocks 0 and 1 of the unit
+#pragma unroll 1
+  for (int c = 0; c < nch; ++c) {
+    const int col = col0 + c * 64 + sub * 16;
+    uint32_t gr[16];
+    ptx::tmem_ld_issue(tunit + static_cast<uint32_t>(c * 64 + sub * 16), gr);
+    uint4 q1 = make_uint4(0, 0, 0, 0), q2 = make_uint4(0, 0, 0, 0), w0 = q1, w1 = q1;
+    float a1 = 0.f, a2 = 0.f;
+    if (row < p.M && col < K) {
+      const int64_t e0 = row * K + col, sidx = row * (K >> qs) + (col >> qs);
+      if (uses_s1(KIND)) {
+        q1 = *reinterpret_cast<const uint4*>(static_cast<const int8_t*>(p.s1) + e0);
+        a1 = p.s1_scale[sidx];
+      }
+      if (uses_s2(KIND)) {
+        q2 = *reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.s2) + e0);
+        a2 = p.s2_scale[sidx];
+      }
+      if (need_w) {
+        w0 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0);
+        w1 = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.W) + e0 + 8);
+      }
+    }
+    ptx::tmem_wait_ld(gr);
+    const uint32_t c1[4] = {q1.x, q1.y, q1.z, q1.w}, c2[4] = {q2.x, q2.y, q2.z, q2.w};
+    const float sd1 = dev::dvd(a1, 127.f), sd2 = dev::dvd(a2, 255.f);
+    float n1 = 0.f, n2 = 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float g[8], w[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = __uint_as_float(gr[8 * h + i]);
+      if (SCALE) scale_grad(g, p);
+      unpack_bf16x8(h == 0 ? w0 : w1, w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = 8 * h + i;
+        float m = uses_s1(KIND) ? dev::mul(dev::code_f32<true>(c1[j >> 2], j & 3), sd1) : 0.f;
+        float v = uses_s2(KIND) ? dev::mul(dev::code_f32<false>(c2[j >> 2], j & 3), sd2) : 0.f;
+        dev::rule<KIND>(w[i], g[i], m, v, p.sc);
+        if (uses_s1(KIND)) n1 = fmaxf(n1, fabsf(m));
+        if (uses_s2(KIND)) n2 = fmaxf(n2, fabsf(v));
+      }
+    }
+    const bool second = ((c * 64) >> qs) != 0;  // the unit's block this chunk lies in: 0 or 1
+    if (second) {
+      l1b = fmaxf(l1b, n1);
+      l2b = fmaxf(l2b, n2);
+    } else {
+      l1a = fmaxf(l1a, n1);
+      l2a = fmaxf(l2a, n2);
+    }
+  }
+  const int nblk = ((nch * 64) >> qs) > 1 ? 2 : 1;
+  float f1a = 0.f, f1b = 0.f, f2a = 0.f, f2b = 0.f;
+#pragma unroll 1
+  for (int b = 0; b < nblk; ++b) {
+    amax[(0 * 4 + sub) * 128 + r] = b == 0 ? l1a : l1b;
+    amax[(1 * 4 + sub) * 128 + r] = b == 0 ? l2a : l2b;
+    ptx::bar_sync(kEpiInnerBarrier, nthreads);
+    float m1 = 0.f, m2 = 0.f;
+#pragma unroll
+    for (int o = 0; o < 4; ++o) {
+      m1 = fmaxf(m1, amax[(0 * 4 + o) * 128 + r]);
+      m2 = fmaxf(m2, amax[(1 * 4 + o) * 128 + r]);
+    }
+    ptx::bar_sync(kEpiInnerBarrier, nthreads);  // read by all before the region is written again
+    if (b == 0) {
+      f1a = m1;
+      f2a = m2;
+    } else {
+      f1b = m1;
+      f2b = m2;
+    }
+  }
+  if (sub == 0) {  // one quarter publishes its row's results in both buffers
+    float* dst[2] = {amax, amax_other};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      dst[i][(0 * 2 + 0) * 128 + r] = f1a;
+      dst[i][(0 * 2 + 1) * 128 + r] = f1b;
+      dst[i][(1 * 2 + 0) * 128 + r] = f2a;
+      dst[i][(1 * 2 + 1) * 128 + r] = f2b;
+    }
+  }
+  ptx::bar_sync(kEpiInnerBarrier, nthreads);  // published before any quarter reads them
+}
+
 // Chunk geometry of the staged FORGE epilogue for one state dtype.  A chunk
 // is 128 rows x kCC columns of the CTA's 128 x 256 half of a pair tile:
 // fp32 states 32 columns (m and v 16 KiB each in shared memory), bf16 states
@@ -896,7 +1011,10 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 template <int KIND, int SDT>
 struct StagedGeom {
   static constexpr bool U1 = uses_s1(KIND), U2 = uses_s2(KIND);
-  static constexpr bool I8 = (SDT == kSInt8 || SDT == kSInt8W);
+  static constexpr bool I8 = (SDT == kSInt8 || SDT == kSInt8W || SDT == kSInt8X || SDT == kSInt8WX);
+  // INT8 block width: the method's 64, compiled in, or (0) read from the
+  // parameters (32, 128 or 256)
+  static constexpr int QB = (SDT == kSInt8 || SDT == kSInt8W) ? 64 : 0;
   static constexpr bool BF = (SDT == kSBf16);
   static constexpr int kCC = I8 ? 64 : 32;
   static constexpr int kChunks = kTileN / kCC;
@@ -1141,6 +1259,9 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   walk.init(p, rank);
   const int total = walk.total;
   const uint32_t empty0 = ptx::mapa(ptx::smem_addr(&ss->tmem_empty[0]), 0);
+  // INT8 block width (columns) and its base-2 logarithm
+  const int qb = G::QB ? G::QB : p.qblock;
+  const int qs = G::QB ? 6 : p.qshift;
 
   // This thread's weights of chunk j (and, for INT8 states, the old absmax of
   // its code block): loaded one chunk ahead.  They are 2 of the 10 or 4.25
@@ -1159,11 +1280,13 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
       for (int h = 0; h < kWPerThread / 8; ++h)
         v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
     }
-    // one code block per chunk; after the first chunk one quarter loads a
-    // row's old scales and hands them to the other three
-    if (G::I8 && (j == 0 || sub == 0)) {
-      const bool okb = row < p.M && col0 < K;
-      const int64_t sidx = row * (K / 64) + col0 / 64;
+    // the old scale of this thread's code block; blocks of 64 or more
+    // columns are whole in a quarter's row of the chunk, so after the first
+    // chunk one quarter loads a row's old scales and hands them to the other
+    // three; with 32-column blocks every thread loads its own
+    if (G::I8 && (j == 0 || sub == 0 || qb == 32)) {
+      const bool okb = row < p.M && col < K;
+      const int64_t sidx = row * (K >> qs) + (col >> qs);
       if (G::U1) o1 = okb ? p.s1_scale[sidx] : 0.f;
       if (G::U2) o2 = okb ? p.s2_scale[sidx] : 0.f;
     }
@@ -1212,16 +1335,16 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h)
         wcur[h] = *reinterpret_cast<const uint4*>(buf + G::kOffW + sw128(r, 2 * sub + h));
-      if (j > 0) {
+      if (j > 0 && qb != 32) {
         const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
         o1 = old[r];
         o2 = old[128 + r];
       }
-      if (j + 1 < total && sub == 0) prefetch(j + 1, wnext, o1next, o2next);
+      if (j + 1 < total && (sub == 0 || qb == 32)) prefetch(j + 1, wnext, o1next, o2next);
     } else {
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
-      if (G::I8 && j > 0) {  // old scales from the quarter that loaded them
+      if (G::I8 && j > 0 && qb != 32) {  // old scales from the quarter that loaded them
         const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
         o1 = old[r];
         o2 = old[128 + r];
@@ -1235,11 +1358,29 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
                            static_cast<uint32_t>(acc * kTileN + c * kCC + sub * kWPerThread);
     const int64_t e0 = row * K + col;
     if (G::I8) {
+      float wd1 = 0.f, wd2 = 0.f;  // blocks of 128 or 256 columns: their absmax, found ahead
+      if (!G::QB && qb > 64) {
+        if (c == 0) {  // a new unit
+          const uint32_t tunit = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                 static_cast<uint32_t>(acc * kTileN);
+          int8_wide_absmax<KIND, SCALE>(tunit, row, col0, min(kChunks, total - j), r, sub, qs,
+                                        reinterpret_cast<float*>(buf + G::kOffAmax),
+                                        reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffAmax),
+                                        G::kNC, p);
+        }
+        const float* fin = reinterpret_cast<const float*>(buf + G::kOffAmax);
+        const int wb = (c * kCC) >> qs;
+        wd1 = fin[(0 * 2 + wb) * 128 + r];
+        wd2 = fin[(1 * 2 + wb) * 128 + r];
+      }
       float n1, n2;
       epi_chunk_int8<KIND, SCALE>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
-                           &n1, &n2, G::kNC, p);
-      if (sub == 0 && row < p.M && col0 < K) {
-        const int64_t sidx = row * (K / 64) + col0 / 64;
+                                  &n1, &n2, G::kNC, qb, wd1, wd2, p);
+      // the thread with the block's last 16 columns stores its new absmax: a
+      // block wider than a chunk keeps its old one until its last chunk has
+      // read it (the next chunks' old scales are loaded a chunk ahead)
+      if ((col & (qb - 1)) == qb - 16 && row < p.M && col < K) {
+        const int64_t sidx = row * (K >> qs) + (col >> qs);
         if (G::U1) p.s1_scale[sidx] = n1;
         if (G::U2) p.s2_scale[sidx] = n2;
       }
@@ -1252,13 +1393,13 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h)
         *reinterpret_cast<uint4*>(buf + G::kOffW + sw128(r, 2 * sub + h)) = wcur[h];
-      if (j + 1 < total && sub == 0) {
+      if (G::I8 && j + 1 < total && sub == 0 && qb != 32) {
         float* nold = reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffOld);
         nold[r] = o1next;
         nold[128 + r] = o2next;
       }
     } else {
-      if (G::I8 && j + 1 < total && sub == 0) {  // the next chunk's old scales, for all quarters
+      if (G::I8 && j + 1 < total && sub == 0 && qb != 32) {  // the next chunk's old scales, for all quarters
         float* nold = reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffOld);
         nold[r] = o1next;
         nold[128 + r] = o2next;

@@ -40,20 +40,24 @@ static int step_pairs() {
 }
 
 int step_max_pairs(int sdt) {
-  return sdt == kSInt8    ? step_pairs<kSInt8>()
-         : sdt == kSInt8W ? step_pairs<kSInt8W>()
-         : sdt == kSBf16  ? step_pairs<kSBf16>()
-                          : step_pairs<kSFp32>();
+  return sdt == kSInt8     ? step_pairs<kSInt8>()
+         : sdt == kSInt8W  ? step_pairs<kSInt8W>()
+         : sdt == kSInt8X  ? step_pairs<kSInt8X>()
+         : sdt == kSInt8WX ? step_pairs<kSInt8WX>()
+         : sdt == kSBf16   ? step_pairs<kSBf16>()
+                           : step_pairs<kSFp32>();
 }
 
 cudaError_t launch_tc_step(int sdt, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& da, const CUtensorMap& db, const CUtensorMap& s1,
                            const CUtensorMap& s2, const CUtensorMap& dx, const CUtensorMap& w,
                            const GemmParams& p, int grid, cudaStream_t s) {
-  return sdt == kSInt8    ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, w, p, grid, s)
-         : sdt == kSInt8W ? run_step<kSInt8W>(a, b, da, db, s1, s2, dx, w, p, grid, s)
-         : sdt == kSBf16  ? run_step<kSBf16>(a, b, da, db, s1, s2, dx, w, p, grid, s)
-                         : run_step<kSFp32>(a, b, da, db, s1, s2, dx, w, p, grid, s);
+  return sdt == kSInt8     ? run_step<kSInt8>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+         : sdt == kSInt8W  ? run_step<kSInt8W>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+         : sdt == kSInt8X  ? run_step<kSInt8X>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+         : sdt == kSInt8WX ? run_step<kSInt8WX>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+         : sdt == kSBf16   ? run_step<kSBf16>(a, b, da, db, s1, s2, dx, w, p, grid, s)
+                           : run_step<kSFp32>(a, b, da, db, s1, s2, dx, w, p, grid, s);
 }
 
 }  // namespace forge

@@ -43,8 +43,9 @@ class Problem:
 
     def __init__(self, T, N, K, w_dtype, s_dtype, opt_name, hp, seed=1, grid=False,
                  x_std=1.0, dy_std=1e-3, w_std=0.02, m_std=1e-4, v_std=1e-6, steps=2,
-                 device_inputs=False):
+                 device_inputs=False, qblock=64):
         self.T, self.N, self.K = T, N, K
+        self.qblock = qblock  # INT8 states: elements per absmax block
         self.w_dtype, self.s_dtype, self.opt, self.hp = w_dtype, s_dtype, opt_name, hp
         self.kind = NAME_TO_KIND[opt_name]
         self.seed = seed
@@ -67,14 +68,14 @@ class Problem:
               "W": W.numpy() if w_dtype == "fp32" else rounding.bf16_bits_rne(W.numpy())}
         if opt.USES_S1[self.kind]:
             if s_dtype == "int8":
-                st["s1"], st["s1_scale"] = quant.quantize_blocks(m.numpy(), signed=True)
+                st["s1"], st["s1_scale"] = quant.quantize_blocks(m.numpy(), signed=True, block=qblock)
             elif s_dtype == "bf16":
                 st["s1"] = rounding.bf16_bits_rne(m.numpy())
             else:
                 st["s1"] = m.numpy()
         if opt.USES_S2[self.kind]:
             if s_dtype == "int8":
-                st["s2"], st["s2_scale"] = quant.quantize_blocks(v.numpy(), signed=False)
+                st["s2"], st["s2_scale"] = quant.quantize_blocks(v.numpy(), signed=False, block=qblock)
             elif s_dtype == "bf16":
                 st["s2"] = rounding.bf16_bits_rne(v.numpy())
             else:
@@ -137,8 +138,8 @@ class Problem:
             api.forge_get_device_status()
             g = ls.weight_gradient(Xb, dYb)
             iv = oracle_interval(self.kind, hp, s + 1, self.seed, g, st, self.w_dtype,
-                                 self.s_dtype, 0, 0, self.K, grad_error_bound(Xb, dYb))
-            assert_in_interval(g_dev, iv, self.w_dtype, self.s_dtype, f"step {s + 1}")
+                                 self.s_dtype, 0, 0, self.K, grad_error_bound(Xb, dYb), self.qblock)
+            assert_in_interval(g_dev, iv, self.w_dtype, self.s_dtype, f"step {s + 1}", self.qblock)
             st = dict(st)
             st.update({k: iv[0][0][k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale")})
         return st
@@ -152,7 +153,16 @@ class Problem:
         for s in range(self.steps):
             Xb, dYb = to_bits(self.X[s]), to_bits(self.dY[s])
             sens |= self.sensitive(Xb, dYb, st)
-            out = ls.linear_bwd_step(Xb, dYb, st, self.kind, hp, s + 1, self.seed, want_dx=want_dx)
+            if self.qblock == 64:
+                out = ls.linear_bwd_step(Xb, dYb, st, self.kind, hp, s + 1, self.seed, want_dx=want_dx)
+            else:  # the same step with another INT8 block width
+                out = {}
+                if want_dx:
+                    out["dX"] = ls.input_gradient(dYb, ls.weights_for_dx(st["W"], self.w_dtype))
+                out.update(ls.update_block(self.kind, hp, s + 1, self.seed, ls.weight_gradient(Xb, dYb),
+                                           st["W"], self.w_dtype, st.get("s1"), st.get("s2"),
+                                           st.get("s1_scale"), st.get("s2_scale"), self.s_dtype,
+                                           0, 0, self.K, block=self.qblock))
             dxs.append(out.get("dX"))
             st.update({k: out[k] for k in ("W", "s1", "s2", "s1_scale", "s2_scale")})
         return st, dxs, sens
@@ -170,7 +180,7 @@ class Problem:
             elif self.s_dtype == "bf16":
                 m = rounding.bf16_bits_to_f32(st["s1"])
             else:
-                m = quant.dequantize_blocks(st["s1"], st["s1_scale"], True)
+                m = quant.dequantize_blocks(st["s1"], st["s1_scale"], True, block=self.qblock)
             b1 = np.float32(self.hp.get("beta1", 0.9))
             c = b1 * m.astype(np.float64) + (1 - b1) * g
             mask |= np.abs(c) <= bound
@@ -237,17 +247,17 @@ def assert_bf16_close(gpu, ref_bits, what, exclude=None, free_running=False):
         f"({d[tuple(bad[0])]} ULP)"
 
 
-def block_mask(mask):
-    """Element mask -> the same mask widened to whole 64-element blocks."""
+def block_mask(mask, block=64):
+    """Element mask -> the same mask widened to whole blocks of `block` elements."""
     N, K = mask.shape
-    b = mask.reshape(N, K // 64, 64).any(axis=2)
-    return np.repeat(b, 64, axis=1), b
+    b = mask.reshape(N, K // block, block).any(axis=2)
+    return np.repeat(b, block, axis=1), b
 
 
-def assert_int8_close(gpu_codes, gpu_scale, ref_codes, ref_scale, what, exclude=None):
+def assert_int8_close(gpu_codes, gpu_scale, ref_codes, ref_scale, what, exclude=None, block=64):
     a = gpu_np(gpu_codes).astype(np.int64)
     b = np.asarray(ref_codes).astype(np.int64)
-    ex_el, ex_blk = (None, None) if exclude is None else block_mask(exclude)
+    ex_el, ex_blk = (None, None) if exclude is None else block_mask(exclude, block)
     diff = np.abs(a - b) > 1
     if ex_el is not None:
         diff &= ~ex_el
@@ -287,7 +297,7 @@ def grad_error_bound(Xb, dYb):
     return 2.0 ** -24 * (np.ceil(T / 16.0) * 3.0 * rw + 4.0 * np.abs(g)) + 1e-30
 
 
-def oracle_interval(kind, hp, step, seed, g, st_block, w_dtype, s_dtype, n0, k0, K, delta):
+def oracle_interval(kind, hp, step, seed, g, st_block, w_dtype, s_dtype, n0, k0, K, delta, block=64):
     """Oracle results for one block of W at four gradients: g, g - delta,
     g + delta, and the point of [g - delta, g + delta] nearest zero (where a
     squared gradient is smallest).  Returns (outs, fp32_states): outs[i] is
@@ -301,8 +311,8 @@ def oracle_interval(kind, hp, step, seed, g, st_block, w_dtype, s_dtype, n0, k0,
           else np.asarray(st_block["W"], dtype=np.float32))
     uses1, uses2 = opt.USES_S1[kind], opt.USES_S2[kind]
     if s_dtype == "int8":
-        m0 = quant.dequantize_blocks(st_block["s1"], st_block["s1_scale"], True) if uses1 else None
-        v0 = quant.dequantize_blocks(st_block["s2"], st_block["s2_scale"], False) if uses2 else None
+        m0 = quant.dequantize_blocks(st_block["s1"], st_block["s1_scale"], True, block) if uses1 else None
+        v0 = quant.dequantize_blocks(st_block["s2"], st_block["s2_scale"], False, block) if uses2 else None
     elif s_dtype == "bf16":
         m0 = rounding.bf16_bits_to_f32(st_block["s1"]) if uses1 else None
         v0 = rounding.bf16_bits_to_f32(st_block["s2"]) if uses2 else None
@@ -314,7 +324,7 @@ def oracle_interval(kind, hp, step, seed, g, st_block, w_dtype, s_dtype, n0, k0,
         outs.append(ls.update_block(kind, hp, step, seed, gg, st_block["W"], w_dtype,
                                     st_block.get("s1"), st_block.get("s2"),
                                     st_block.get("s1_scale"), st_block.get("s2_scale"),
-                                    s_dtype, n0, k0, K))
+                                    s_dtype, n0, k0, K, block=block))
         _, m1, v1 = opt.apply_rule(kind, sc, wf, gg, m0, v0)
         fp32.append({"s1": m1, "s2": v1})
     return outs, fp32
@@ -329,7 +339,7 @@ def _fp32_in(g, lo, hi):
     return (g >= lo - (1e-7 + 1e-5 * np.abs(lo))) & (g <= hi + (1e-7 + 1e-5 * np.abs(hi)))
 
 
-def assert_in_interval(gpu_state, interval, w_dtype, s_dtype, what):
+def assert_in_interval(gpu_state, interval, w_dtype, s_dtype, what, block=64):
     """GPU outputs inside the hull of the oracle's interval results, widened
     by the base tolerance (see module docstring)."""
     outs, fp32 = interval
@@ -372,7 +382,7 @@ def assert_in_interval(gpu_state, interval, w_dtype, s_dtype, what):
         # magnitude and the largest upper magnitude; each dequantised code lies
         # within half a quantisation step of its element's interval.
         R, C = lo.shape
-        lo_b, hi_b = lo.reshape(R, C // 64, 64), hi.reshape(R, C // 64, 64)
+        lo_b, hi_b = lo.reshape(R, C // block, block), hi.reshape(R, C // block, block)
         min_mag = np.where((lo_b > 0) | (hi_b < 0), np.minimum(np.abs(lo_b), np.abs(hi_b)), 0.0)
         max_mag = np.maximum(np.abs(lo_b), np.abs(hi_b))
         a_lo, a_hi = min_mag.max(axis=2), max_mag.max(axis=2)
@@ -382,7 +392,7 @@ def assert_in_interval(gpu_state, interval, w_dtype, s_dtype, what):
         assert bad.size == 0, f"{what} {key} scale: {len(bad)} outside the interval; first " \
             f"{bad[:3].tolist()}: gpu={gs[tuple(bad[0])]} [{a_lo[tuple(bad[0])]}, {a_hi[tuple(bad[0])]}]"
         step = gs / (127.0 if signed else 255.0)
-        deq = g.astype(np.float64).reshape(R, C // 64, 64) * step[..., None]
+        deq = g.astype(np.float64).reshape(R, C // block, block) * step[..., None]
         half = 0.5 * step[..., None] * (1 + 1e-5) + 1e-30
         ok = (deq >= lo_b - half - 1e-5 * np.abs(lo_b)) & (deq <= hi_b + half + 1e-5 * np.abs(hi_b))
         bad = np.argwhere(~ok)

@@ -98,6 +98,33 @@ def test_bf16_moments_with_fp32_weights_unsupported_in_the_fused_step(L):
     assert b"bf16 moments" in L.forge_last_error_message()
 
 
+@pytest.mark.parametrize("sdt,K,rc", [(api.STATE_INT8_B256, 320, 1), (api.STATE_INT8_B128, 320, 1),
+                                      (api.STATE_INT8_B32, 200, 1), (9, 256, 1)],
+                         ids=["b256_k320", "b128_k320", "b32_k200", "unknown_sdtype"])
+def test_int8_block_width_checked_on_host(L, sdt, K, rc):
+    """K must be a multiple of the INT8 block width (and of 64); unknown state
+    dtypes are refused."""
+    hp = api.hparams()
+    st = _state(sdt=sdt, sc1=80, sc2=96)
+    got = L.forge_linear_bwd_step(ctypes.byref(_lin(K=K)), ctypes.byref(st), 0, ctypes.byref(hp), 1, 0, None)
+    assert got == rc, (got, L.forge_last_error_message())
+
+
+@pytest.mark.parametrize("sdt", [api.STATE_INT8_B32, api.STATE_INT8_B128, api.STATE_INT8_B256])
+def test_int8_block_widths_other_than_64_need_bf16_weights_in_the_fused_step(L, sdt):
+    hp = api.hparams()
+    st = _state(wdt=api.W_FP32, sdt=sdt, sc1=80, sc2=96)
+    rc = L.forge_linear_bwd_step(ctypes.byref(_lin(K=512)), ctypes.byref(st), 0, ctypes.byref(hp), 1, 0, None)
+    assert rc == 2 and b"bf16 weights" in L.forge_last_error_message()
+
+
+def test_quantiser_block_width_checked_on_host(L):
+    assert L.forge_quantize_state_block(None, None, None, 4, 256, 1, 48, None) == 1   # width 48
+    assert L.forge_quantize_state_block(None, None, None, 4, 320, 1, 256, None) == 1  # cols % 256
+    assert L.forge_dequantize_state_block(None, None, None, 4, 192, 0, 128, None) == 1  # cols % 128
+    assert b"cols" in L.forge_last_error_message()
+
+
 def test_other_entry_points_validate(L):
     assert L.forge_unfused_opt_step(None, None, 8, 8, 0, None, 1, 0, None) == 1
     assert L.forge_quantize_state(None, None, None, 4, 100, 1, None) == 1  # cols % 64
