@@ -692,6 +692,9 @@ def run_ours(args):
             r = measure_workload(api, key, args.steps, args.warmup, local, cpu=not args.no_cpu_baseline)
             out["configs"][key] = r
             torch.cuda.empty_cache()
+    if not args.no_configs:
+        out["int8_block_sizes"] = measure_int8_blocks(api, args.steps, args.warmup, local)
+        torch.cuda.empty_cache()
     if not args.no_cpu_baseline:
         dt, f = oracle_sample()
         out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
@@ -880,6 +883,102 @@ def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_lay
         out["cpu_baseline"] = {"value": round(f / dt / 1e12, 6), "unit": "TFLOP/s", "cores": host_cores(),
                                "cpu_model": cpu_model(), "kind": "oracle", "sample": desc}
     return out
+
+
+INT8_BLOCKS = (32, 64, 128, 256)
+
+
+def measure_int8_blocks(api, steps, warmup, local=0, moment_steps=10):
+    """The INT8-moment Llama step (dX + FORGE step, T = 16384, AdamW) with each
+    absmax block width the kernels support, and the quantisation error each
+    width leaves in the moments: one q_proj (4096 x 4096) stepped
+    `moment_steps` times with INT8 moments and, from the same dequantised
+    start and the same inputs, with fp32 moments (the moments of AdamW do not
+    depend on the weights, so the fp32 run is the INT8 run's exact reference);
+    reported as ||dequant(m_B) - m|| / ||m||, and likewise for v."""
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    w = inputs.WORKLOADS["llama8b_bf16_int8state"]
+    T, hp = w.T, w.hparams
+    _, peak_burst, _, _ = _peaks()
+    acts = {"x_attn": 4096, "x_o": 4096, "x_mlp": 4096, "x_down": 14336}
+    X = {a: inputs.normal((T, k), 1.0, 200 + i, torch.bfloat16, dev) for i, (a, k) in enumerate(acts.items())}
+    shapes = {n: (N, K) for n, N, K in inputs.LLAMA31_8B_LINEARS}
+    res = {}
+    for qb in INT8_BLOCKS:
+        layers = []
+        for i, n in enumerate(ORDER):
+            N, K = shapes[n]
+            L = {"name": n, "N": N, "K": K, "seed": 3000 + 17 * i,
+                 "W": inputs.normal((N, K), 0.02, 3000 + 17 * i, torch.bfloat16, dev),
+                 "dY": inputs.normal((T, N), 1e-3, 3001 + 17 * i, torch.bfloat16, dev),
+                 "dX": torch.empty((T, K), dtype=torch.bfloat16, device=dev),
+                 "m": torch.empty((N, K), dtype=torch.int8, device=dev),
+                 "v": torch.empty((N, K), dtype=torch.uint8, device=dev),
+                 "ms": torch.empty((N, K // qb), dtype=torch.float32, device=dev),
+                 "vs": torch.empty((N, K // qb), dtype=torch.float32, device=dev)}
+            api.forge_quantize_state(inputs.normal((N, K), w.m_init_std, 3002 + 17 * i, torch.float32, dev),
+                                     L["m"], L["ms"], True, block=qb)
+            api.forge_quantize_state(inputs.abs_normal((N, K), w.v_init_std, 3003 + 17 * i, torch.float32, dev),
+                                     L["v"], L["vs"], False, block=qb)
+            layers.append(L)
+
+        def step(s):
+            for L in layers:
+                api.forge_linear_bwd_step(X[ACT[L["name"]]], L["dY"], L["W"], "adamw", hp, s, L["seed"],
+                                          L["m"], L["v"], L["ms"], L["vs"], dX=L["dX"])
+
+        for s in range(warmup):
+            step(s + 1)
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for s in range(steps):
+            step(warmup + s + 1)
+        b.record(stream)
+        torch.cuda.synchronize()
+        api.forge_get_device_status()
+        step_ms = a.elapsed_time(b) / steps
+        flops = sum(4.0 * L["N"] * L["K"] * T for L in layers)
+        del layers
+        torch.cuda.empty_cache()
+        # moment error after moment_steps steps of one q_proj
+        N = K = 4096
+        W8 = inputs.normal((N, K), 0.02, 4000, torch.bfloat16, dev)
+        W32 = W8.clone()
+        m8 = torch.empty((N, K), dtype=torch.int8, device=dev)
+        v8 = torch.empty((N, K), dtype=torch.uint8, device=dev)
+        sm8 = torch.empty((N, K // qb), dtype=torch.float32, device=dev)
+        sv8 = torch.empty((N, K // qb), dtype=torch.float32, device=dev)
+        api.forge_quantize_state(inputs.normal((N, K), w.m_init_std, 4001, torch.float32, dev), m8, sm8, True, block=qb)
+        api.forge_quantize_state(inputs.abs_normal((N, K), w.v_init_std, 4002, torch.float32, dev), v8, sv8, False,
+                                 block=qb)
+        m32 = torch.empty((N, K), dtype=torch.float32, device=dev)
+        v32 = torch.empty((N, K), dtype=torch.float32, device=dev)
+        api.forge_dequantize_state(m8, sm8, m32, True, block=qb)
+        api.forge_dequantize_state(v8, sv8, v32, False, block=qb)
+        for s in range(moment_steps):
+            Xs = inputs.normal((T, K), 1.0, 4100 + s, torch.bfloat16, dev)
+            dYs = inputs.normal((T, N), 1e-3, 4200 + s, torch.bfloat16, dev)
+            api.forge_linear_bwd_step(Xs, dYs, W8, "adamw", hp, s + 1, 4003, m8, v8, sm8, sv8)
+            api.forge_linear_bwd_step(Xs, dYs, W32, "adamw", hp, s + 1, 4003, m32, v32)
+        mq = torch.empty_like(m32)
+        vq = torch.empty_like(v32)
+        api.forge_dequantize_state(m8, sm8, mq, True, block=qb)
+        api.forge_dequantize_state(v8, sv8, vq, False, block=qb)
+        api.forge_get_device_status()
+        rel = lambda a, r: float((a.double() - r.double()).norm() / r.double().norm())  # noqa: E731
+        res[str(qb)] = {"ms_per_step": round(step_ms, 4), "tflops": round(flops / (step_ms * 1e-3) / 1e12, 1),
+                        "frac_of_burst_peak": round(flops / (step_ms * 1e-3) / 1e12 / peak_burst, 4),
+                        "m_rel_error": rel(mq, m32), "v_rel_error": rel(vq, v32),
+                        "scale_bytes_per_param": 2 * 4.0 / qb}
+        del W8, W32, m8, v8, sm8, sv8, m32, v32, mq, vq
+        torch.cuda.empty_cache()
+    return {"workload": "Llama-3.1-8B layer linears, T=16384, dX + FORGE step, bf16 W (SR), INT8 AdamW "
+                        "moments with one fp32 absmax per block of B row elements",
+            "moment_error": f"q_proj 4096x4096 after 10 steps against fp32 moments from the same start",
+            "per_block": res}
 
 
 def run_workload(args):

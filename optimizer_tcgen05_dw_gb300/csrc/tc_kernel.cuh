@@ -1357,6 +1357,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     const uint32_t taddr = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(acc * kTileN + c * kCC + sub * kWPerThread);
     const int64_t e0 = row * K + col;
+    float n1 = 0.f, n2 = 0.f;  // INT8: the new absmax of this thread's block
     if (G::I8) {
       float wd1 = 0.f, wd2 = 0.f;  // blocks of 128 or 256 columns: their absmax, found ahead
       if (!G::QB && qb > 64) {
@@ -1373,17 +1374,8 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
         wd1 = fin[(0 * 2 + wb) * 128 + r];
         wd2 = fin[(1 * 2 + wb) * 128 + r];
       }
-      float n1, n2;
       epi_chunk_int8<KIND, SCALE>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
                                   &n1, &n2, G::kNC, qb, wd1, wd2, p);
-      // the thread with the block's last 16 columns stores its new absmax: a
-      // block wider than a chunk keeps its old one until its last chunk has
-      // read it (the next chunks' old scales are loaded a chunk ahead)
-      if ((col & (qb - 1)) == qb - 16 && row < p.M && col < K) {
-        const int64_t sidx = row * (K >> qs) + (col >> qs);
-        if (G::U1) p.s1_scale[sidx] = n1;
-        if (G::U2) p.s2_scale[sidx] = n2;
-      }
     } else if (G::BF) {
       epi_chunk_bf16s<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     } else {
@@ -1404,16 +1396,27 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
         nold[r] = o1next;
         nold[128 + r] = o2next;
       }
-      if (row < p.M && col < K) {
-        uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
-#pragma unroll
-        for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
-      }
     }
     const bool more = j + 1 < total;
     const bool unit_end = !more || c == kChunks - 1;  // the unit's accumulator is read out
     if (unit_end) ptx::tc_fence_before();
+    // The staged states, visible to the TMA stores.  The global stores below
+    // come after this fence, so that it has no global write in flight to
+    // wait for: they are ordered by nothing in this CTA.
     ptx::fence_proxy_async_smem();
+    if (!G::WST && row < p.M && col < K) {
+      uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
+#pragma unroll
+      for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
+    }
+    // INT8: the thread with the block's last 16 columns stores the block's
+    // new absmax; a block wider than a chunk keeps its old one until its last
+    // chunk has read it (the next chunks' old scales are loaded a chunk ahead)
+    if (G::I8 && (col & (qb - 1)) == qb - 16 && row < p.M && col < K) {
+      const int64_t sidx = row * (K >> qs) + (col >> qs);
+      if (G::U1) p.s1_scale[sidx] = n1;
+      if (G::U2) p.s2_scale[sidx] = n2;
+    }
     if (!unit_end) {  // end of chunk j = start of chunk j + 1 (same unit)
       begin(j + 1);
       stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);
