@@ -750,13 +750,16 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
       s2[4 * i] = s2[4 * i + 1] = s2[4 * i + 2] = s2[4 * i + 3] = 0.f;
     }
   }
+  // the rounding bits depend on the element index only: their ten dependent
+  // rounds overlap the wait for the gradient
+  const uint4 rnd = dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys);
   ptx::tmem_wait_ld(gr);
 #pragma unroll
   for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
   if (SCALE) scale_grad(g, p);
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
-  wv = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys));
+  wv = pack_sr_bf16x8(w, rnd);
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     if (uses_s1(KIND))
@@ -782,6 +785,7 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
   unpack_bf16x8(wv, w);
   if (uses_s1(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS1 + sw64(r, sub)), s1);
   if (uses_s2(KIND)) unpack_bf16x8(*reinterpret_cast<const uint4*>(buf + kOffS2 + sw64(r, sub)), s2);
+  const uint4 rnd = dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys);
   ptx::tmem_wait_ld(gr);
 #pragma unroll
   for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
@@ -793,7 +797,7 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
-  wv = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base, p.step, p.round_keys));
+  wv = pack_sr_bf16x8(w, rnd);
   uint32_t o1[4], o2[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -830,6 +834,10 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   const uint32_t q1[4] = {c1.x, c1.y, c1.z, c1.w}, q2[4] = {c2.x, c2.y, c2.z, c2.w};
   const float sd1 = dev::dvd(a1, 127.f), sd2 = dev::dvd(a2, 255.f);  // old code steps
   float n1 = 0.f, n2 = 0.f;
+  // the rounding bits of the 16 weights, ahead of the gradient wait
+  const uint64_t grp = (static_cast<uint64_t>(e0) >> 3) + p.sr_base;
+  const uint4 rnd0 = dev::sr_words_rk(grp, p.step, p.round_keys);
+  const uint4 rnd1 = dev::sr_words_rk(grp + 1, p.step, p.round_keys);
   ptx::tmem_wait_ld(gr);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {  // two halves of 8 columns: gradient and weights
@@ -847,7 +855,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
       if (uses_s1(KIND)) n1 = fmaxf(n1, fabsf(m[j]));  // = absmax_acc: n1 is never NaN
       if (uses_s2(KIND)) n2 = fmaxf(n2, fabsf(v[j]));
     }
-    wv[h] = pack_sr_bf16x8(w, dev::sr_words_rk((static_cast<uint64_t>(e0) >> 3) + p.sr_base + h, p.step, p.round_keys));
+    wv[h] = pack_sr_bf16x8(w, h == 0 ? rnd0 : rnd1);
   }
   if (qb > 64) {  // the block spans chunks: its absmax was found ahead
     n1 = wide1;
@@ -872,19 +880,30 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   const float st1 = dev::dvd(n1, 127.f), st2 = dev::dvd(n2, 255.f);  // code steps
   const float iv1 = dev::dvd(1.f, st1), iv2 = dev::dvd(1.f, st2);
   const bool bad1 = !(fabsf(iv1) <= 3.0e38f), bad2 = !(fabsf(iv2) <= 3.0e38f);
+  // The sixteen codes are formed branch-free; if any lies near a rounding
+  // boundary (rare) all sixteen are formed again from the exact quotient,
+  // which gives the others' codes unchanged.
   auto codes = [&](const float (&x)[16], float st, float inv, bool bad, uint32_t (&o)[4], auto sgn) {
     constexpr bool S = decltype(sgn)::value;
+    int k[16];
+    bool any = bad;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {  // four codes per word, byte i = code 4q + i
-      int k[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        bool nr;
-        k[i] = dev::code_round<S, false>(dev::mul(x[4 * q + i], inv), nr);
-        if (nr || bad) k[i] = dev::code_round<S>(dev::dvd(x[4 * q + i], st), nr);
-      }
-      o[q] = __byte_perm(__byte_perm(k[0], k[1], 0x0040u), __byte_perm(k[2], k[3], 0x0040u), 0x5410u);
+    for (int i = 0; i < 16; ++i) {
+      bool nr;
+      k[i] = dev::code_round<S, false>(dev::mul(x[i], inv), nr);
+      any |= nr;
     }
+    if (any) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        bool nr;
+        k[i] = dev::code_round<S>(dev::dvd(x[i], st), nr);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)  // four codes per word, byte i = code 4q + i
+      o[q] = __byte_perm(__byte_perm(k[4 * q], k[4 * q + 1], 0x0040u),
+                         __byte_perm(k[4 * q + 2], k[4 * q + 3], 0x0040u), 0x5410u);
   };
   if (uses_s1(KIND)) codes(m, st1, iv1, bad1, o1, std::true_type{});
   if (uses_s2(KIND)) codes(v, st2, iv2, bad2, o2, std::false_type{});
