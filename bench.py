@@ -546,17 +546,30 @@ def run_ours(args):
         unfused_step(s_no)
         s_no += 1
     barrier()
-    u0 = torch.cuda.Event(enable_timing=True)
-    u1 = torch.cuda.Event(enable_timing=True)
+    # The two schedules alternate in short regions of u_steps steps (three of
+    # each, the fastest kept), so that both see the same clocks: the headline
+    # region above runs for seconds under the power cap, these do not.
     u_steps = max(3, args.steps // 4)
-    u0.record(stream)
-    for _ in range(u_steps):
-        unfused_step(s_no)
-        s_no += 1
-    u1.record(stream)
-    torch.cuda.synchronize()
+
+    def short_region(fn):
+        nonlocal s_no
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(u_steps):
+            fn(s_no)
+            s_no += 1
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / u_steps
+
+    unf_runs, fused_runs = [], []
+    for _ in range(3):
+        fused_runs.append(short_region(step))
+        unf_runs.append(short_region(unfused_step))
     api.forge_get_device_status()
-    unf_ms = max_over_ranks(u0.elapsed_time(u1) / u_steps, dist, dev)
+    unf_ms = max_over_ranks(min(unf_runs), dist, dev)
+    fused_short_ms = max_over_ranks(min(fused_runs), dist, dev)
     del dW
     torch.cuda.synchronize()
 
@@ -662,7 +675,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": 4, "ms_per_step": round(e2e_ms, 4)},
         "unfused": {"ms_per_step": round(unf_ms, 4),
                     "value": round(flops_step * world / (unf_ms * 1e-3) / 1e12, 2),
-                    "speedup_fused_vs_unfused": round(unf_ms / ms, 3),
+                    "fused_ms_per_step_same_regions": round(fused_short_ms, 4),
+                    "speedup_fused_vs_unfused": round(unf_ms / fused_short_ms, 3),
+                    "regions": f"3 x {u_steps} steps of each schedule, alternating; fastest of each",
                     "dW_pool_bytes": params * 4,
                     "peak_alloc_bytes_fused": base_alloc,
                     "peak_alloc_bytes_unfused": unf_peak},
