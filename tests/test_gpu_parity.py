@@ -455,6 +455,7 @@ DEALING = {
     "F77_D44": (1024, 1792, 2816),
     "F2_D128": (16384, 256, 512),
     "F224_D16": (1024, 14336, 1024),
+    "F160_D32": (512, 2560, 4096),
     "ragged_T": (1000, 1024, 2048),
 }
 
