@@ -761,7 +761,7 @@ CONFIG_KEYS = ("llama8b_bf16_int8state", "sweep_4096", "qwen14b_int8", "single_2
 
 
 def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_layers=None,
-                     no_dx=False, cpu=True):
+                     no_dx=False, cpu=True, tokens=None, optimizers=None):
     """One secondary workload: its step timed with CUDA events between
     synchronisations (warmup steps, then `steps`), the step launches' own rate
     against the dense-bf16 peak that applies to the region's length, the
@@ -770,13 +770,15 @@ def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_lay
     bounded sample of the same configuration.  Returns a dict."""
     dev = torch.device("cuda", local)
     w = inputs.WORKLOADS[key]
-    T = w.T
+    T = w.T if tokens is None else tokens
     stream = torch.cuda.current_stream()
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats(dev)
     hbm_gbs, peak_burst, peak_sust, peak_src = _peaks()
     sweep = key == "sweep_4096"
     opts = list(inputs.SWEEP_HPARAMS) if sweep else [w.opt]
+    if sweep and optimizers:
+        opts = [o for o in opts if o in optimizers]
     # layers: (layer index, name, N, K); activations per layer
     if key == "qwen14b_int8":
         n_layers = w.layers if num_layers is None else num_layers
@@ -871,7 +873,8 @@ def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_lay
         "config": {"workload": w.name, "key": key, "T": T, "linears": len(layers),
                    "flops_counted": "2NKT (dW)" + (" + 2NKT (dX)" if want_dx else "") + " per linear",
                    "w_dtype": w.w_dtype, "s_dtype": w.s_dtype, "optimizers": opts,
-                   "partial": bool(only_layers or num_layers is not None or no_dx)},
+                   "partial": bool(only_layers or num_layers is not None or no_dx or tokens is not None
+                                   or (sweep and optimizers))},
         "roofline": {"bound": bound, "achieved": round(kern, 2), "unit": "TFLOP/s",
                      "peak": peak, "peak_kind": peak_kind,
                      "frac": round(kern / peak, 4),
@@ -1008,7 +1011,8 @@ def run_workload(args):
     build()
     api.lib()
     r = measure_workload(api, args.workload, args.steps, args.warmup, local, args.layers,
-                         args.num_layers, args.no_dx, cpu=not args.no_cpu_baseline)
+                         args.num_layers, args.no_dx, cpu=not args.no_cpu_baseline,
+                         tokens=args.tokens, optimizers=args.optimizers)
     out = {"metric": METRIC, "value": r.pop("value"), "unit": r.pop("unit"), "n_gpus": 1,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r.pop("ms_per_step"),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -1038,6 +1042,10 @@ def main():
                     help="time the step only (profiling runs): no e2e, unfused or CPU legs")
     ap.add_argument("--num-layers", type=int, default=None,
                     help="with --workload qwen14b_int8: decoder layers to sweep (profiling; default 40)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --workload: another token count T (profiling; the line is marked partial)")
+    ap.add_argument("--optimizers", nargs="*", default=None, choices=list(inputs.SWEEP_HPARAMS),
+                    help="with --workload sweep_4096: only these rules (profiling)")
     ap.add_argument("--no-dx", action="store_true",
                     help="with --workload: the weight step alone, without dX (profiling)")
     ap.add_argument("--workload", default=WORKLOAD_KEY, choices=(WORKLOAD_KEY,) + SECONDARY,
