@@ -214,39 +214,80 @@ __global__ void __launch_bounds__(kElemThreads) dequantize_kernel(const ElemPara
   }
 }
 
+// 16-byte asynchronous copy global -> shared (cp.async, L1 bypassed); with
+// `valid` false the destination is zero-filled and nothing is read.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // dX[t, k] = sum_n dY[t, n] * bf16(W[n, k]) with fp32 accumulation; a 64 x 64
-// output tile per block, 4 x 4 per thread, 32-deep shared-memory slices.
+// output tile per block, 4 x 4 per thread, the reduction in slices of 32 n:
+// a 3-deep ring of slices in shared memory filled with asynchronous copies,
+// so two slices are in flight while the block multiplies the third.  Each
+// output sums its products in ascending n (one fused multiply-add each).
+constexpr int kDgStages = 3;
 __global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* __restrict__ dY,
                                                           const float* __restrict__ W,
                                                           __nv_bfloat16* __restrict__ dX,
                                                           int64_t T, int64_t N, int64_t K) {
-  __shared__ float sA[32][64 + 1];  // [n][t]
-  __shared__ float sB[32][64 + 1];  // [n][k]
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  __shared__ __align__(16) uint16_t sA[kDgStages][64][40];  // [stage][t][n]: dY bits, 80-byte rows
+  __shared__ __align__(16) float sB[kDgStages][32][64];     // [stage][n][k]: W
+  const int tid = static_cast<int>(threadIdx.x);
+  const int tx = tid & 15, ty = tid >> 4;
   const int64_t t0 = static_cast<int64_t>(blockIdx.y) * 64, k0 = static_cast<int64_t>(blockIdx.x) * 64;
-  float acc[4][4] = {};
-  for (int64_t n0 = 0; n0 < N; n0 += 32) {
-    for (int i = threadIdx.x; i < 32 * 64; i += 256) {
-      const int nn = i & 31, tt = i >> 5;
-      const int64_t t = t0 + tt, n = n0 + nn;
-      sA[nn][tt] = (t < T && n < N) ? __bfloat162float(dY[t * N + n]) : 0.f;
-      const int kk = i & 63, nr = i >> 6;
-      const int64_t k = k0 + kk, n2 = n0 + nr;
-      sB[nr][kk] = (k < K && n2 < N) ? __bfloat162float(__float2bfloat16_rn(W[n2 * K + k])) : 0.f;
+  const int64_t slices = (N + 31) / 32;
+  // slice `sl` into stage `st`: dY rows of 32 n (four 16-byte pieces each),
+  // W rows of 64 k (sixteen pieces each); N and K are multiples of 8, so a
+  // piece is wholly inside or wholly outside the matrix
+  auto load = [&](int64_t sl, int st) {
+    if (sl < slices) {
+      const int64_t n0 = sl * 32;
+      {
+        const int row = tid >> 2, ch = tid & 3;
+        const int64_t t = t0 + row, n = n0 + ch * 8;
+        const bool ok = t < T && n < N;
+        cp_async16(&sA[st][row][ch * 8], ok ? static_cast<const void*>(dY + t * N + n) : dY, ok);
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = tid + u * 256, nr = c >> 4, kc = c & 15;
+        const int64_t n = n0 + nr, k = k0 + kc * 4;
+        const bool ok = n < N && k < K;
+        cp_async16(&sB[st][nr][kc * 4], ok ? static_cast<const void*>(W + n * K + k) : W, ok);
+      }
     }
-    __syncthreads();
+    cp_async_commit();  // an empty group past the last slice keeps the counting uniform
+  };
+  float acc[4][4] = {};
+#pragma unroll
+  for (int st = 0; st < kDgStages - 1; ++st) load(st, st);
+  for (int64_t sl = 0; sl < slices; ++sl) {
+    cp_async_wait<kDgStages - 2>();  // slice sl has landed (this thread's pieces)
+    __syncthreads();                 // ... everyone's; and slice sl - 1 is no longer read
+    load(sl + kDgStages - 1, static_cast<int>((sl + kDgStages - 1) % kDgStages));
+    const int st = static_cast<int>(sl % kDgStages);
 #pragma unroll 4
     for (int nn = 0; nn < 32; ++nn) {
-      float a[4], b[4];
+      float a[4], w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) { a[i] = sA[nn][ty * 4 + i]; b[i] = sB[nn][tx * 4 + i]; }
+      for (int i = 0; i < 4; ++i) a[i] = __uint_as_float(static_cast<uint32_t>(sA[st][ty * 4 + i][nn]) << 16);
+      const float4 wv = *reinterpret_cast<const float4*>(&sB[st][nn][tx * 4]);
+      w[0] = __bfloat162float(__float2bfloat16_rn(wv.x));
+      w[1] = __bfloat162float(__float2bfloat16_rn(wv.y));
+      w[2] = __bfloat162float(__float2bfloat16_rn(wv.z));
+      w[3] = __bfloat162float(__float2bfloat16_rn(wv.w));
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
+        for (int j = 0; j < 4; ++j) acc[i][j] = __fmaf_rn(a[i], w[j], acc[i][j]);
     }
-    __syncthreads();
   }
+  cp_async_wait<0>();
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int64_t t = t0 + ty * 4 + i;

@@ -650,6 +650,24 @@ __device__ __forceinline__ void epi_store(uint32_t tbase, int64_t row, int colba
   }
 }
 
+// L2 prefetch of the (up to) 128 columns from `col0` of row `row` of W and of
+// the states the rule reads: one request per 128-byte line, no registers held.
+__device__ __forceinline__ void prefetch_l2(const void* base, int64_t byte0, int64_t bytes) {
+  const char* b = static_cast<const char*>(base) + byte0;
+  for (int64_t o = 0; o < bytes; o += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(b + o));
+}
+template <int WDT, int SDT>
+__device__ __forceinline__ void prefetch_row_l2(int64_t row, int col0, const GemmParams& p) {
+  const int64_t K = p.Ncols;
+  const int64_t n = min(static_cast<int64_t>(128), K - col0);
+  const int64_t e0 = row * K + col0;
+  prefetch_l2(p.W, e0 * (WDT == kWBf16 ? 2 : 4), n * (WDT == kWBf16 ? 2 : 4));
+  const int esz = SDT == kSInt8 ? 1 : (SDT == kSBf16 ? 2 : 4);
+  const bool u1 = uses_s1(p.sc.kind), u2 = uses_s2(p.sc.kind);
+  if (u1) prefetch_l2(p.s1, e0 * esz, n * esz);
+  if (u2) prefetch_l2(p.s2, e0 * esz, n * esz);
+}
+
 template <int MODE, int WDT, int SDT>
 __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, int lane,
                               uint32_t rank) {
@@ -661,6 +679,14 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
   for (int tile = pair_id(); tile < p.num_tiles; tile += num_pairs(), ++local) {
     const int acc = local & 1;
     const uint32_t aph = (static_cast<uint32_t>(local) >> 1) & 1u;
+    int tm, tn;
+    tile_coords(tile, p, tm, tn);
+    const int64_t row = static_cast<int64_t>(tm) * kPairM + rank * kTileM + r;
+    const int colbase = tn * kTileN + half * 128;
+    const bool row_ok = row < p.M;
+    // While the tile's main loop runs, pull this thread's weights and states
+    // into L2, so the epilogue's loads (one round trip per 8 elements) hit.
+    if (MODE == kModeFusedOpt && row_ok && colbase < p.Ncols) prefetch_row_l2<WDT, SDT>(row, colbase, p);
     // One thread waits; the others block on the named barrier, which also
     // hands every warp the same verdict, so warps stay converged for the
     // .sync.aligned tensor-memory loads that follow.
@@ -668,11 +694,6 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
     if (warp == 2 && lane == 0) ok = bounded_wait(&ss->tmem_full[acc], aph, p, ss);
     if (ptx::bar_red_or(kEpiBarrier, 32 * kNumEpiWarps, !ok)) break;
     ptx::tc_fence_after();
-    int tm, tn;
-    tile_coords(tile, p, tm, tn);
-    const int64_t row = static_cast<int64_t>(tm) * kPairM + rank * kTileM + r;
-    const int colbase = tn * kTileN + half * 128;
-    const bool row_ok = row < p.M;
     const uint32_t tbase = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(acc * kTileN + half * 128);
     if (MODE == kModeFusedOpt)
@@ -1529,6 +1550,9 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
     ptx::tmem_alloc_pair(&ss->tmem_base, kTmemCols);
     ptx::tmem_relinquish_pair();
   }
+  // Each warp reconverges before the CTA barrier (lanes of warps 0 and 1 took
+  // different paths above), so the barrier counts every thread.
+  __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
@@ -1545,6 +1569,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
 
+  __syncwarp();  // the producer's and MMA thread's lanes rejoin their warps first
   ptx::tc_fence_before();
   __syncthreads();
   ptx::cluster_sync();  // the peer's shared and tensor memory stay valid until the pair is done
