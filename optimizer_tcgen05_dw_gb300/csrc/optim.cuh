@@ -234,6 +234,18 @@ __device__ __forceinline__ int code_round(float y, bool& near) {
   return (y == y) ? k : 0;
 }
 
+// code_round<SIGNED, false> without its NaN test, for a caller that forms all
+// codes of a group again from the exact quotient (code_round) whenever one
+// reports `redo`: the comparison is written so that a NaN y (and an infinite
+// one) reports it, and every other y gets the same code as code_round<SIGNED,
+// false>.
+template <bool SIGNED>
+__device__ __forceinline__ int code_round_fast(float y, bool& redo) {
+  const float t = __fadd_rn(y, kShifter);
+  redo = !(fabsf(__fsub_rn(y, __fsub_rn(t, kShifter))) < 0.49997f);
+  return static_cast<int>(__float_as_uint(t) - 0x4B400000u);
+}
+
 // Running absmax that never takes a NaN (NaN > a is false).
 __device__ __forceinline__ float absmax_acc(float a, float x) {
   const float ax = fabsf(x);

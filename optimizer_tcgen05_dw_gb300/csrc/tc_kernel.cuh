@@ -894,9 +894,9 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
     }
   }
   // New codes (dev::quant_recip's rule): round x * (1/s) with the shifter;
-  // the few near a half-integer, and every code of a block whose reciprocal
-  // is not finite, are redone from the exact quotient x / s (a branch that is
-  // rarely taken).
+  // the few near a half-integer or not finite, and every code of a block
+  // whose reciprocal is not finite, are redone from the exact quotient x / s
+  // (a branch that is rarely taken).
   uint32_t o1[4] = {0u, 0u, 0u, 0u}, o2[4] = {0u, 0u, 0u, 0u};
   const float st1 = dev::dvd(n1, 127.f), st2 = dev::dvd(n2, 255.f);  // code steps
   const float iv1 = dev::dvd(1.f, st1), iv2 = dev::dvd(1.f, st2);
@@ -911,7 +911,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       bool nr;
-      k[i] = dev::code_round<S, false>(dev::mul(x[i], inv), nr);
+      k[i] = dev::code_round_fast<S>(dev::mul(x[i], inv), nr);
       any |= nr;
     }
     if (any) {
