@@ -237,13 +237,14 @@ __device__ __forceinline__ int code_round(float y, bool& near) {
 // code_round<SIGNED, false> without its NaN test, for a caller that forms all
 // codes of a group again from the exact quotient (code_round) whenever one
 // reports `redo`: the comparison is written so that a NaN y (and an infinite
-// one) reports it, and every other y gets the same code as code_round<SIGNED,
-// false>.
+// one) reports it.  Returns the bit pattern of y + 1.5 * 2^23, whose low byte
+// is the code (two's complement for a negative one) that code_round<SIGNED,
+// false> gives for every other y: 1.5 * 2^23 has a zero low byte.
 template <bool SIGNED>
-__device__ __forceinline__ int code_round_fast(float y, bool& redo) {
+__device__ __forceinline__ uint32_t code_round_fast(float y, bool& redo) {
   const float t = __fadd_rn(y, kShifter);
   redo = !(fabsf(__fsub_rn(y, __fsub_rn(t, kShifter))) < 0.49997f);
-  return static_cast<int>(__float_as_uint(t) - 0x4B400000u);
+  return __float_as_uint(t);
 }
 
 // Running absmax that never takes a NaN (NaN > a is false).

@@ -728,12 +728,27 @@ __device__ __forceinline__ void unpack_bf16x8(uint4 v, float* w) {
   }
 }
 
+// Eight weights to bf16 by stochastic rounding (dev::bf16_sr), packed in
+// pairs.  When all eight are finite (w * 0 is then 0; an infinite or NaN w
+// makes the sum NaN), each is its bit pattern plus its 16 random bits, upper
+// half kept: the two halves of a word come from one byte permutation.
 __device__ __forceinline__ uint4 pack_sr_bf16x8(const float* w, uint4 rnd) {
-  uint32_t o[4];
+  float probe = 0.f;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(rnd, 2 * j)) |
-           (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(rnd, 2 * j + 1)) << 16);
+  for (int j = 0; j < 8; ++j) probe = __fmaf_rn(w[j], 0.f, probe);
+  const uint32_t rw[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+  uint32_t o[4];
+  if (probe == probe) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = __byte_perm(__float_as_uint(w[2 * j]) + (rw[j] & 0xFFFFu),
+                         __float_as_uint(w[2 * j + 1]) + (rw[j] >> 16), 0x7632u);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = dev::bf16_sr(w[2 * j], dev::sr_bits(rnd, 2 * j)) |
+             (dev::bf16_sr(w[2 * j + 1], dev::sr_bits(rnd, 2 * j + 1)) << 16);
+  }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -906,7 +921,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
   // which gives the others' codes unchanged.
   auto codes = [&](const float (&x)[16], float st, float inv, bool bad, uint32_t (&o)[4], auto sgn) {
     constexpr bool S = decltype(sgn)::value;
-    int k[16];
+    uint32_t k[16];  // the low byte of each is the code
     bool any = bad;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -918,7 +933,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         bool nr;
-        k[i] = dev::code_round<S>(dev::dvd(x[i], st), nr);
+        k[i] = static_cast<uint32_t>(dev::code_round<S>(dev::dvd(x[i], st), nr));
       }
     }
 #pragma unroll
