@@ -79,10 +79,14 @@ struct SharedState {
 // deeper ring.  A stage holds 128 rows of A and 128 columns of B (half of the
 // pair's 256): 32 KiB at 64 tokens.
 constexpr int kEpiBufBytes = 32768;
-// INT8 states stage the bf16 weight chunk too (see StagedGeom): a larger
-// buffer, and one operand stage fewer to make room.
+// INT8 states stage the bf16 weight chunk too (see StagedGeom).  With the
+// method's block of 64 the buffer holds codes and weights only (32 KiB: the
+// block absmax is exchanged inside the weight region, each thread loads its
+// own old scale), so the ring keeps all five stages; the other block widths
+// need two more small regions (a larger buffer) and give up one stage.
 constexpr int kEpiBufBytesW = 37888;
 __host__ __device__ constexpr bool stages_weights(int sdt) { return sdt == kSInt8W || sdt == kSInt8WX; }
+__host__ __device__ constexpr bool compact_int8(int sdt) { return sdt == kSInt8W; }
 constexpr int kEpiBarrier = 1;       // named barrier of the epilogue warps
 constexpr int kEpiInnerBarrier = 2;  // the staged epilogue's compute warps only
 constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
@@ -97,12 +101,12 @@ struct KCfg {
       kFp8 ? kFp8BlockK
            : (kTmaEpi ? kFusedBlockK : (MODE == kModeWgradStore ? kWgradBlockK : kBlockK));  // tokens per stage
   static constexpr int kStg =
-      kTmaEpi ? (kStageW ? kFusedStages - 1 : kFusedStages)
+      kTmaEpi ? (kStageW && !compact_int8(SDT) ? kFusedStages - 1 : kFusedStages)
               : (MODE == kModeWgradStore ? kWgradStages : kStages);
   static constexpr int kEsz = kFp8 ? 1 : 2;           // operand element bytes
   static constexpr int kA = kTileM * kBK * kEsz;       // bytes of A per stage (this CTA's 128 rows)
   static constexpr int kB = (kTileN / 2) * kBK * kEsz; // bytes of B per stage (this CTA's 128 columns)
-  static constexpr int kEpiBuf = kStageW ? kEpiBufBytesW : kEpiBufBytes;
+  static constexpr int kEpiBuf = kStageW && !compact_int8(SDT) ? kEpiBufBytesW : kEpiBufBytes;
   static constexpr int kEpiBytes = kTmaEpi ? 2 * kEpiBuf : 0;
   static constexpr int kSmem = kStg * (kA + kB) + kEpiBytes + 512 + 1024;
   // TMA warp, MMA warp, epilogue warps (four per 32-lane quarter of TMEM in the
@@ -119,8 +123,8 @@ static_assert(KCfg<kModeDgrad, kWBf16>::kSmem <= 232448, "dynamic shared memory 
 static_assert(KCfg<kModeFusedFp8, kWBf16>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeStep, kWBf16, kSInt8W>::kSmem <= 232448, "dynamic shared memory limit");
 static_assert(KCfg<kModeFusedFp8, kWBf16, kSInt8W>::kSmem <= 232448, "dynamic shared memory limit");
-static_assert(KCfg<kModeStep, kWBf16, kSInt8WX>::kSmem == KCfg<kModeStep, kWBf16, kSInt8W>::kSmem,
-              "block-width variants share the layout");
+static_assert(KCfg<kModeStep, kWBf16, kSInt8WX>::kSmem <= 232448, "dynamic shared memory limit");
+static_assert(KCfg<kModeFusedFp8, kWBf16, kSInt8WX>::kSmem <= 232448, "dynamic shared memory limit");
 
 // Bounded wait on an mbarrier phase.  Returns false if the CTA is aborting
 // or the wait expired (the first expiry records the timeout).
@@ -853,7 +857,11 @@ __device__ __forceinline__ void epi_chunk_bf16s(uint32_t taddr, uint8_t* buf, in
 // two quarters it spans; blocks of 128 or 256 columns span several chunks and
 // arrive found already (wide1, wide2: int8_wide_absmax).  The weights use the
 // new float32 moments, then the moments are quantised with the new absmax.
-template <int KIND, bool SCALE>
+// CMP (compact layout): the exchange region is the start of the weight region,
+// free only once every compute thread has taken its weights into registers
+// (a barrier before the exchange) and until the first weights are written
+// back (a barrier after it).
+template <int KIND, bool SCALE, bool CMP = false>
 __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int r, int sub,
                                                int64_t e0, uint4 (&wv)[2], float a1, float a2,
                                                float* n1_out, float* n2_out, int nthreads,
@@ -898,6 +906,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
     n2 = wide2;
   } else {
     float* amax = reinterpret_cast<float*>(buf + kOffAmax);  // [state][quarter][row]
+    if (CMP) ptx::bar_sync(kEpiInnerBarrier, nthreads);  // every thread's weights are read
     amax[(0 * 4 + sub) * 128 + r] = n1;
     amax[(1 * 4 + sub) * 128 + r] = n2;
     ptx::bar_sync(kEpiInnerBarrier, nthreads);
@@ -907,6 +916,7 @@ __device__ __forceinline__ void epi_chunk_int8(uint32_t taddr, uint8_t* buf, int
       n1 = fmaxf(n1, amax[(0 * 4 + o) * 128 + r]);
       n2 = fmaxf(n2, amax[(1 * 4 + o) * 128 + r]);
     }
+    if (CMP) ptx::bar_sync(kEpiInnerBarrier, nthreads);  // read by all before weights return
   }
   // New codes (dev::quant_recip's rule): round x * (1/s) with the shifter;
   // the few near a half-integer or not finite, and every code of a block
@@ -1078,13 +1088,18 @@ struct StagedGeom {
   static constexpr uint32_t kStateBytes = (I8 || BF) ? 8192u : 16384u;
   static constexpr uint32_t kTx = (U1 ? kStateBytes : 0u) + (U2 ? kStateBytes : 0u);
   static constexpr int kWPerThread = kCC / 4;  // bf16 weights per thread and chunk (8 or 16)
-  // kSInt8W: the chunk's bf16 weights (128 rows x 128 bytes, 128-byte
-  // swizzle) are staged by TMA as well.  With INT8 states the old scales of
-  // the next chunk are handed from the quarter that loads them to the other
-  // three (kOffOld, inside either buffer size).
+  // kSInt8W, kSInt8WX: the chunk's bf16 weights (128 rows x 128 bytes,
+  // 128-byte swizzle) are staged by TMA as well.  With INT8 states the old
+  // scales of the next chunk are handed from the quarter that loads them to
+  // the other three (kOffOld), and the block absmax is exchanged at kOffAmax;
+  // except in the compact layout (kSInt8W: CMP), where the weights follow the
+  // codes at 16384, the absmax exchange uses the weight region once every
+  // compute thread holds its weights in registers, and each thread loads its
+  // own old scale.
   static constexpr bool WST = stages_weights(SDT);
-  static constexpr int kOffAmax = 16384, kOffOld = 20480, kOffW = 21504;
-  static constexpr int kBuf = WST ? kEpiBufBytesW : kEpiBufBytes;
+  static constexpr bool CMP = compact_int8(SDT);
+  static constexpr int kOffAmax = 16384, kOffOld = 20480, kOffW = CMP ? 16384 : 21504;
+  static constexpr int kBuf = WST && !CMP ? kEpiBufBytesW : kEpiBufBytes;
   static constexpr uint32_t kTxAll = kTx + (WST ? 16384u : 0u);
   static constexpr int kNC = 32 * kNumEpiWarpsStaged;  // compute threads
   static constexpr int kNB = kNC + 32;                 // compute threads + the I/O warp
@@ -1317,6 +1332,9 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   // INT8 block width (columns) and its base-2 logarithm
   const int qb = G::QB ? G::QB : p.qblock;
   const int qs = G::QB ? 6 : p.qshift;
+  // every thread loads its own old scale (32-column blocks, compact layout),
+  // or one quarter of a row loads them and hands them to the other three
+  const bool own = G::CMP || qb == 32;
 
   // This thread's weights of chunk j (and, for INT8 states, the old absmax of
   // its code block): loaded one chunk ahead.  They are 2 of the 10 or 4.25
@@ -1338,8 +1356,8 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     // the old scale of this thread's code block; blocks of 64 or more
     // columns are whole in a quarter's row of the chunk, so after the first
     // chunk one quarter loads a row's old scales and hands them to the other
-    // three; with 32-column blocks every thread loads its own
-    if (G::I8 && (j == 0 || sub == 0 || qb == 32)) {
+    // three, unless every thread loads its own (`own`)
+    if (G::I8 && (j == 0 || sub == 0 || own)) {
       const bool okb = row < p.M && col < K;
       const int64_t sidx = row * (K >> qs) + (col >> qs);
       if (G::U1) o1 = okb ? p.s1_scale[sidx] : 0.f;
@@ -1390,16 +1408,16 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h)
         wcur[h] = *reinterpret_cast<const uint4*>(buf + G::kOffW + sw128(r, 2 * sub + h));
-      if (j > 0 && qb != 32) {
+      if (j > 0 && !own) {
         const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
         o1 = old[r];
         o2 = old[128 + r];
       }
-      if (j + 1 < total && (sub == 0 || qb == 32)) prefetch(j + 1, wnext, o1next, o2next);
+      if (j + 1 < total && (sub == 0 || own)) prefetch(j + 1, wnext, o1next, o2next);
     } else {
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
-      if (G::I8 && j > 0 && qb != 32) {  // old scales from the quarter that loaded them
+      if (G::I8 && j > 0 && !own) {  // old scales from the quarter that loaded them
         const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
         o1 = old[r];
         o2 = old[128 + r];
@@ -1429,8 +1447,8 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
         wd1 = fin[(0 * 2 + wb) * 128 + r];
         wd2 = fin[(1 * 2 + wb) * 128 + r];
       }
-      epi_chunk_int8<KIND, SCALE>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1, o2,
-                                  &n1, &n2, G::kNC, qb, wd1, wd2, p);
+      epi_chunk_int8<KIND, SCALE, G::CMP>(taddr, buf, r, sub, e0, *reinterpret_cast<uint4(*)[2]>(wcur), o1,
+                                          o2, &n1, &n2, G::kNC, qb, wd1, wd2, p);
     } else if (G::BF) {
       epi_chunk_bf16s<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     } else {
@@ -1440,13 +1458,13 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
 #pragma unroll
       for (int h = 0; h < kWPerThread / 8; ++h)
         *reinterpret_cast<uint4*>(buf + G::kOffW + sw128(r, 2 * sub + h)) = wcur[h];
-      if (G::I8 && j + 1 < total && sub == 0 && qb != 32) {
+      if (G::I8 && j + 1 < total && sub == 0 && !own) {
         float* nold = reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffOld);
         nold[r] = o1next;
         nold[128 + r] = o2next;
       }
     } else {
-      if (G::I8 && j + 1 < total && sub == 0 && qb != 32) {  // the next chunk's old scales, for all quarters
+      if (G::I8 && j + 1 < total && sub == 0 && !own) {  // the next chunk's old scales, for all quarters
         float* nold = reinterpret_cast<float*>(epi + ((j + 1) & 1) * G::kBuf + G::kOffOld);
         nold[r] = o1next;
         nold[128 + r] = o2next;
