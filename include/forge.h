@@ -139,13 +139,16 @@ typedef struct forge_hparams {
  * `stream` first), so two such calls must not run concurrently on one device
  * (order them on one stream, or call forge_set_step_fusion(0)).  The one
  * launch sizes its grid so that all of its CTA pairs fit on the device at
- * once, and a weight tile waits (bounded) for dX tiles that other pairs run:
- * a kernel on another stream that holds SMs for longer than the wait limit
- * (forge_set_wait_limit_ns, 2 s by default) can keep pairs from starting, and
- * the call then ends in FORGE_ERR_TIMEOUT with W and the states partly
- * updated.  Callers that overlap long-lived kernels (e.g. a persistent
- * communication kernel) with this step should call forge_set_step_fusion(0),
- * whose two launches wait on nothing.  Otherwise
+ * once, and a weight tile waits (bounded) for dX tiles that other pairs run,
+ * so it needs all its pairs running together: before any pair writes a
+ * weight, the launch checks that every one of its CTAs has started.  If a
+ * kernel on another stream holds SMs for longer than the wait limit
+ * (forge_set_wait_limit_ns, 2 s by default), the launch stops there: the call
+ * reports FORGE_ERR_TIMEOUT (forge_get_device_status) with W, the states and
+ * the scales unchanged (dX may be written) and can be repeated, for example
+ * after forge_set_step_fusion(0), whose two launches wait on nothing.
+ * Callers that overlap long-lived kernels (e.g. a persistent communication
+ * kernel) with this step should use that form.  Otherwise
  * dX is a separate launch enqueued first on `stream`.  Both forms compute the
  * same bits.  step is 1-based (bias corrections).  Nothing is allocated; no
  * gradient tensor is written.  Returns FORGE_OK once the launches are

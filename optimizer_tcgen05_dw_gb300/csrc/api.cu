@@ -29,15 +29,15 @@ __device__ uint32_t g_device_status;
 // launched concurrently on different streams of one device would share
 // them, so the one-launch path is taken only while the caller keeps its
 // steps on one device ordered (forge.h, forge_set_step_fusion).
-__device__ uint32_t g_dx_done[kMaxDxBlocks];
+__device__ uint32_t g_dx_done[kMaxDxBlocks + 2];  // + the residency gate's two words
 
 // Scratch of forge_linear_bwd_step_static alone: that entry point's own
 // dX-completion counters for the one-launch step, one word per 256-column
-// block of W (1024 words: K up to 262144).  Static device memory, so the
-// entry point never allocates; cleared on the caller's stream before each
-// launch that uses it.
+// block of W (1024 words: K up to 262144), and the residency gate's two words.
+// Static device memory, so the entry point never allocates; cleared on the
+// caller's stream before each launch that uses it.
 constexpr int kStaticScratchWords = 1024;
-static __device__ __align__(256) uint32_t g_static_scratch[kStaticScratchWords];
+static __device__ __align__(256) uint32_t g_static_scratch[kStaticScratchWords + 2];
 
 namespace {
 
@@ -559,7 +559,8 @@ forge_status_t launch_step(const forge_linear_t* lin, const forge_state_t* state
   p.dx_done = counters != nullptr ? counters : d.dx_done;
   p.dx_target = static_cast<uint32_t>(2 * p.dx_tiles_m);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(p.dx_done, 0, static_cast<size_t>(p.tiles_n) * sizeof(uint32_t), s)) != cudaSuccess)
+  // the per-column-block counters and the residency gate's two words
+  if ((e = cudaMemsetAsync(p.dx_done, 0, static_cast<size_t>(p.tiles_n + 2) * sizeof(uint32_t), s)) != cudaSuccess)
     return cuda_fail(e, "clearing the dX counters");
   // Every pair must be resident at once (dW tiles wait for other pairs' dX
   // tiles): at most the occupancy limit, at most one pair per tile.

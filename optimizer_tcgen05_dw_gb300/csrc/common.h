@@ -138,7 +138,7 @@ struct GemmParams {
   int32_t dx_tiles_m;        // 256-row pair tiles over T
   int32_t dx_tiles;          // dx_tiles_m * tiles_n
   int32_t dx_num_kb;         // reduction blocks of 64 over M
-  uint32_t* dx_done;         // [tiles_n], zero at launch
+  uint32_t* dx_done;         // [tiles_n + 2], zero at launch (+ the residency gate's words)
   uint32_t dx_target;        // 2 * dx_tiles_m
   // How the dX tiles are dealt (balancing the pairs' total work): every pair
   // takes one per round for dx_rounds rounds; the rest go round-robin to the

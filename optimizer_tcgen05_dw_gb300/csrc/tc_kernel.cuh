@@ -1162,6 +1162,40 @@ __device__ __forceinline__ bool bounded_wait_count(const uint32_t* cnt, uint32_t
   }
 }
 
+// The one-launch step's residency gate, passed by each CTA's I/O thread before
+// its first weight tile: no weight or state of the launch is written unless
+// every CTA of the launch is running (a dW tile waits for dX tiles of other
+// pairs, which a pair that never started would never finish).  Each CTA adds
+// one to `started` (dx_done[tiles_n]) when it starts; the first thread to see
+// all of them there writes the decision "go" (1) to dx_done[tiles_n + 1], the
+// first whose wait expires writes "stop" (2); one compare-and-swap settles it,
+// so every CTA of the launch acts on the same decision.  On "stop" the launch
+// ends with a timeout in the status word and W, the states and the scales as
+// they were (only dX, an output, was written).
+__device__ __forceinline__ bool residency_gate(const GemmParams& p, SharedState* ss) {
+  const uint32_t* started = p.dx_done + p.tiles_n;
+  uint32_t* decision = p.dx_done + p.tiles_n + 1;
+  const uint64_t t0 = ptx::global_timer_ns();
+  while (true) {
+    const uint32_t d = ptx::ld_acquire_gpu(decision);
+    if (d == 1u) return true;
+    if (d == 2u) {
+      *reinterpret_cast<volatile int32_t*>(&ss->abort) = 1;
+      atomicCAS(p.status, 0u, static_cast<uint32_t>(kStatusTimeout));
+      return false;
+    }
+    if (ptx::ld_acquire_gpu(started) >= gridDim.x) {
+      atomicCAS(decision, 0u, 1u);
+    } else if (*reinterpret_cast<volatile int32_t*>(&ss->abort)) {
+      return false;
+    } else if (ptx::global_timer_ns() - t0 > p.wait_limit_ns) {
+      atomicCAS(decision, 0u, 2u);
+    } else {
+      __nanosleep(256);
+    }
+  }
+}
+
 // One dX tile of the one-launch step, by a compute warp: 64 columns
 // (sub*64..) of TMEM lane row r, rounded to bf16 (nearest even) and written
 // to row r of `box`, a 128-row x 64-column bf16 box in shared memory laid out
@@ -1267,6 +1301,7 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
       ++local;
       if (local > first) walk.advance(local - first, p, rank);
       if (io) ok = bounded_wait(&ss->tmem_full[local & 1], (static_cast<uint32_t>(local) >> 1) & 1u, p, ss);
+      if (STEP && io && ok && local == first) ok = residency_gate(p, ss);
       if (STEP && io && ok) ok = bounded_wait_count(p.dx_done + walk.cur_col0 / kTileN, p.dx_target, p, ss);
     }
     if (io && ok) ok = bounded_wait(&ss->epi_full[j & 1], (static_cast<uint32_t>(j) >> 1) & 1u, p, ss);
@@ -1590,6 +1625,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
   __syncthreads();
   ptx::cluster_sync();  // both CTAs' barriers exist before either signals the other's
   ptx::tc_fence_after();
+  if (MODE == kModeStep && threadIdx.x == 0) atomicAdd(p.dx_done + p.tiles_n, 1u);  // residency_gate
 
   if (warp == 0) {
     if (lane == 0) producer_role<MODE, STG, Cfg::kBK>(&mapA, &mapB, &mapDA, &mapDB, p, smA, smB, ss, rank);
