@@ -22,8 +22,9 @@ enum SDtype : int32_t { kSFp32 = 0, kSInt8 = 1, kSBf16 = 2,
                         kSInt8X = 4, kSInt8WX = 5 };
 constexpr int kNumKernelSdt = 6;
 // Longest reduction for which the INT8 epilogue stages the weights: it frees
-// the compute warps from row-strided weight accesses (+40 % at T = 4096) but
-// costs an operand stage, which a long main loop needs (-5 % at T = 16384).
+// the compute warps from row-strided weight accesses (+40 % at T = 4096); over
+// longer reductions the direct form is as fast or faster (block 64 keeps all
+// operand stages either way; the other block widths give one up to staging).
 constexpr int64_t kStageWeightsMaxT = 8192;
 
 // Device-side status codes (values match forge_status_t).
