@@ -178,3 +178,49 @@ def test_llama8b_one_launch_step_with_dx(layer):
         k0 = int(rng.integers(0, K // TILE)) * TILE
         assert_dx_close(dX[t0:t0 + TILE, k0:k0 + TILE].contiguous(), to_bits(dY[t0:t0 + TILE].contiguous()),
                         np.ascontiguousarray(W0b[:, k0:k0 + TILE]), f"dX tile ({t0},{k0})")
+
+
+@pytest.mark.parametrize("layer", ["gate_proj", "k_proj"])
+def test_qwen14b_int8_one_launch_step_with_dx(layer):
+    """The Qwen3-14B configuration's launch: dX and the FORGE step with INT8
+    block-64 AdamW moments of a full-size layer at T = 4096 in one launch (the
+    staged-weights INT8 epilogue).  Same bits as the two-launch form for W, the
+    codes, the scales and dX (k_proj: 80 weight tiles on 76 pairs, so some pairs
+    take two), and sampled dX tiles equal the oracle's dY W from the pre-update
+    weights."""
+    w = inputs.WORKLOADS["qwen14b_int8"]
+    N, K = QWEN[layer]
+    T = w.T
+    seed = 7000 + N % 71
+    X = inputs.normal((T, K), 1.0, inputs.layer_seed(seed, 0, 0, 1), device="cuda")
+    dY = inputs.normal((T, N), w.dy_std, inputs.layer_seed(seed, 0, 0, 2), device="cuda")
+    W0 = inputs.normal((N, K), 0.02, inputs.layer_seed(seed, 0, 0, 3), torch.bfloat16, "cuda")
+    m0 = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    v0 = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+    ms0 = torch.empty((N, K // 64), device="cuda")
+    vs0 = torch.empty((N, K // 64), device="cuda")
+    api.forge_quantize_state(inputs.normal((N, K), 1e-4, inputs.layer_seed(seed, 0, 0, 4), torch.float32, "cuda"),
+                             m0, ms0, True)
+    api.forge_quantize_state(inputs.abs_normal((N, K), 1e-6, inputs.layer_seed(seed, 0, 0, 5), torch.float32, "cuda"),
+                             v0, vs0, False)
+    outs = []
+    for one_launch in (True, False):
+        W, m, v, ms, vs = W0.clone(), m0.clone(), v0.clone(), ms0.clone(), vs0.clone()
+        dX = torch.empty((T, K), dtype=torch.bfloat16, device="cuda")
+        api.forge_set_step_fusion(one_launch)
+        try:
+            api.forge_linear_bwd_step(X, dY, W, "adamw", w.hparams, 1, seed, m, v, ms, vs, dX=dX)
+            api.forge_get_device_status()
+        finally:
+            api.forge_set_step_fusion(True)
+        outs.append((W, m, v, ms, vs, dX))
+    for a, b, name in zip(outs[0], outs[1], ("W", "m codes", "v codes", "m scales", "v scales", "dX")):
+        assert torch.equal(a, b), name
+    dX = outs[0][5]
+    rng = np.random.default_rng(seed)
+    W0b = to_bits(W0)
+    for _ in range(6):
+        t0 = int(rng.integers(0, T // TILE)) * TILE
+        k0 = int(rng.integers(0, K // TILE)) * TILE
+        assert_dx_close(dX[t0:t0 + TILE, k0:k0 + TILE].contiguous(), to_bits(dY[t0:t0 + TILE].contiguous()),
+                        np.ascontiguousarray(W0b[:, k0:k0 + TILE]), f"dX tile ({t0},{k0})")
