@@ -186,7 +186,8 @@ FORGE_API forge_status_t forge_linear_bwd_step_shard(const forge_linear_t* lin,
 /* forge_linear_bwd_step computing the same bits, with the one-launch form's
  * scratch in a fixed, static device array of this library instead of the
  * array that forge_linear_bwd_step uses: the dX-completion counters of the
- * one launch, one 32-bit word per 256-column block of W, 1024 words.  The
+ * one launch, one 32-bit word per 256-column block of W (1024 words), and the
+ * launch's two residency-gate words.  The
  * pages have no counterpart of this entry point; it exists so that a caller
  * can keep such steps off the scratch that forge_linear_bwd_step uses.
  *   - No allocation, ever; the array's device address is looked up once per
