@@ -5,8 +5,9 @@ One step = the backward of the seven linear layers of one decoder layer
 (down, up, gate, o, v, k, q; T = 16384 tokens): for each layer one launch
 computes dX = dY W from the pre-update weights and the fused weight-gradient
 + AdamW step (bf16 weights with stochastic rounding, fp32 moments).  Inputs are seeded synthetic
-tensors resident in HBM; each activation/gradient tensor is >= 134 MB, larger
-than the 129 MB L2, so no L2 flush is needed between steps.
+tensors resident in HBM; one step streams ~10 GB (activations >= 134 MB, the
+k/v output gradients 34 MB, 1.7 GB of states) through the 129 MB L2, so no
+input is still resident when it is read again and no L2 flush is needed.
 
 Printed: one JSON line (rank 0).  ``value`` = (2NKT for dW + 2NKT for dX,
 summed over the layers and ranks) / step time, in TFLOP/s; the timed region of
@@ -636,7 +637,8 @@ def run_ours(args):
                    "hparams": hp, "weights": "bf16, stochastic rounding",
                    "states": "fp32 m, v", "flops_per_step": flops_step,
                    "flops_counted": "2NKT (dW) + 2NKT (dX) per linear",
-                   "l2": "no flush: every X/dY >= 134 MB and the states (1.7 GB) exceed the 129 MB L2",
+                   "l2": "no flush: a step streams ~10 GB (X >= 134 MB, dY 34-470 MB, 1.7 GB of "
+                         "states) through the 129 MB L2 between two reads of any input",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor",
                      "kernel": "one-launch FORGE step (tc_kernel mode 3: dX tiles, then dW tiles "
