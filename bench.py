@@ -5,7 +5,7 @@ One step = the backward of the seven linear layers of one decoder layer
 (down, up, gate, o, v, k, q; T = 16384 tokens): for each layer one launch
 computes dX = dY W from the pre-update weights and the fused weight-gradient
 + AdamW step (bf16 weights with stochastic rounding, fp32 moments).  Inputs are seeded synthetic
-tensors resident in HBM; one step streams ~10 GB (activations >= 134 MB, the
+tensors resident in HBM; one step streams ~8 GB (activations >= 134 MB, the
 k/v output gradients 34 MB, 1.7 GB of states) through the 129 MB L2, so no
 input is still resident when it is read again and no L2 flush is needed.
 
@@ -637,7 +637,7 @@ def run_ours(args):
                    "hparams": hp, "weights": "bf16, stochastic rounding",
                    "states": "fp32 m, v", "flops_per_step": flops_step,
                    "flops_counted": "2NKT (dW) + 2NKT (dX) per linear",
-                   "l2": "no flush: a step streams ~10 GB (X >= 134 MB, dY 34-470 MB, 1.7 GB of "
+                   "l2": "no flush: a step streams ~8 GB (X >= 134 MB, dY 34-470 MB, 1.7 GB of "
                          "states) through the 129 MB L2 between two reads of any input",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor",
