@@ -225,11 +225,23 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// W rounded to its nearest bf16 (ties to even) and widened back, with integer
+// operations: the same value as __float2bfloat16_rn for every finite and
+// infinite W (a NaN stays a NaN).
+__device__ __forceinline__ float round_to_bf16(float x) {
+  uint32_t u = __float_as_uint(x);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return __uint_as_float(u | 0x00400000u);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return __uint_as_float(u & 0xFFFF0000u);
+}
+
 // dX[t, k] = sum_n dY[t, n] * bf16(W[n, k]) with fp32 accumulation; a 64 x 64
 // output tile per block, 4 x 4 per thread, the reduction in slices of 32 n:
 // a 3-deep ring of slices in shared memory filled with asynchronous copies,
 // so two slices are in flight while the block multiplies the third.  Each
-// output sums its products in ascending n (one fused multiply-add each).
+// slice's weights are rounded to bf16 once, in place, when it lands (not once
+// per use: sixteen threads read each).  Each output sums its products in
+// ascending n (one fused multiply-add each).
 constexpr int kDgStages = 3;
 __global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* __restrict__ dY,
                                                           const float* __restrict__ W,
@@ -269,18 +281,25 @@ __global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* _
   for (int64_t sl = 0; sl < slices; ++sl) {
     cp_async_wait<kDgStages - 2>();  // slice sl has landed (this thread's pieces)
     __syncthreads();                 // ... everyone's; and slice sl - 1 is no longer read
-    load(sl + kDgStages - 1, static_cast<int>((sl + kDgStages - 1) % kDgStages));
     const int st = static_cast<int>(sl % kDgStages);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {  // the slice's 32 x 64 weights, each once
+      const int e = tid + u * 256;
+      float& x = sB[st][e >> 6][e & 63];
+      x = round_to_bf16(x);
+    }
+    __syncthreads();
+    load(sl + kDgStages - 1, static_cast<int>((sl + kDgStages - 1) % kDgStages));
 #pragma unroll 4
     for (int nn = 0; nn < 32; ++nn) {
       float a[4], w[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) a[i] = __uint_as_float(static_cast<uint32_t>(sA[st][ty * 4 + i][nn]) << 16);
       const float4 wv = *reinterpret_cast<const float4*>(&sB[st][nn][tx * 4]);
-      w[0] = __bfloat162float(__float2bfloat16_rn(wv.x));
-      w[1] = __bfloat162float(__float2bfloat16_rn(wv.y));
-      w[2] = __bfloat162float(__float2bfloat16_rn(wv.z));
-      w[3] = __bfloat162float(__float2bfloat16_rn(wv.w));
+      w[0] = wv.x;
+      w[1] = wv.y;
+      w[2] = wv.z;
+      w[3] = wv.w;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
