@@ -643,7 +643,10 @@ forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, i
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.skip_loads = g_skip_loads.load();
   CUtensorMap m1 = ma, m2 = ma, mw = ma, mbh = mb;
-  if (state->w_dtype == FORGE_W_BF16_SR) {
+  // the staged epilogue (states through shared memory by TMA): bf16 weights,
+  // or fp32 weights with fp32 states
+  if (state->w_dtype == FORGE_W_BF16_SR ||
+      (state->w_dtype == FORGE_W_FP32 && state->s_dtype == FORGE_STATE_FP32)) {
     if ((st = state_maps(state, opt_kind, lin->N, lin->K, ma, &m1, &m2)) != FORGE_OK ||
         (st = weight_map(state, kernel_sdt(state, lin->T), lin->N, lin->K, ma, &mw)) != FORGE_OK)
       return st;

@@ -94,8 +94,11 @@ constexpr int kPairM = 2 * kTileM;  // rows of a pair tile
 template <int MODE, int WDT, int SDT = kSFp32>
 struct KCfg {
   static constexpr bool kFp8 = (MODE == kModeFusedFp8);
+  // the staged epilogue: every FORGE step with bf16 weights, and the fused
+  // step with fp32 weights and fp32 states
   static constexpr bool kTmaEpi =
-      ((MODE == kModeFusedOpt || MODE == kModeStep || kFp8) && WDT == kWBf16);
+      ((MODE == kModeFusedOpt || MODE == kModeStep || kFp8) && WDT == kWBf16) ||
+      (MODE == kModeFusedOpt && WDT == kWFp32 && SDT == kSFp32);
   static constexpr bool kStageW = kTmaEpi && stages_weights(SDT);
   static constexpr int kBK =
       kFp8 ? kFp8BlockK
@@ -811,6 +814,50 @@ __device__ __forceinline__ void epi_chunk_fp32(uint32_t taddr, uint8_t* buf, int
   }
 }
 
+// fp32 states and fp32 weights: as epi_chunk_fp32, with the thread's 8 fp32
+// weights in registers (`wv`, two 16-byte words) written back unrounded.
+template <int KIND>
+__device__ __forceinline__ void epi_chunk_fp32w(uint32_t taddr, uint8_t* buf, int r, int sub,
+                                                uint4 (&wv)[2], const GemmParams& p) {
+  constexpr int kOffS1 = 0, kOffS2 = 16384;
+  float g[8], w[8], s1[8], s2[8];
+  uint32_t gr[8];
+  ptx::tmem_ld_issue(taddr, gr);  // the gradient arrives while the states are read
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    w[4 * i] = __uint_as_float(wv[i].x); w[4 * i + 1] = __uint_as_float(wv[i].y);
+    w[4 * i + 2] = __uint_as_float(wv[i].z); w[4 * i + 3] = __uint_as_float(wv[i].w);
+    if (uses_s1(KIND)) {
+      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS1 + sw128(r, 2 * sub + i));
+      s1[4 * i] = x.x; s1[4 * i + 1] = x.y; s1[4 * i + 2] = x.z; s1[4 * i + 3] = x.w;
+    } else {
+      s1[4 * i] = s1[4 * i + 1] = s1[4 * i + 2] = s1[4 * i + 3] = 0.f;
+    }
+    if (uses_s2(KIND)) {
+      const float4 x = *reinterpret_cast<const float4*>(buf + kOffS2 + sw128(r, 2 * sub + i));
+      s2[4 * i] = x.x; s2[4 * i + 1] = x.y; s2[4 * i + 2] = x.z; s2[4 * i + 3] = x.w;
+    } else {
+      s2[4 * i] = s2[4 * i + 1] = s2[4 * i + 2] = s2[4 * i + 3] = 0.f;
+    }
+  }
+  ptx::tmem_wait_ld(gr);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) g[j] = __uint_as_float(gr[j]);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) dev::rule<KIND>(w[j], g[j], s1[j], s2[j], p.sc);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    wv[i] = make_uint4(__float_as_uint(w[4 * i]), __float_as_uint(w[4 * i + 1]), __float_as_uint(w[4 * i + 2]),
+                       __float_as_uint(w[4 * i + 3]));
+    if (uses_s1(KIND))
+      *reinterpret_cast<float4*>(buf + kOffS1 + sw128(r, 2 * sub + i)) =
+          make_float4(s1[4 * i], s1[4 * i + 1], s1[4 * i + 2], s1[4 * i + 3]);
+    if (uses_s2(KIND))
+      *reinterpret_cast<float4*>(buf + kOffS2 + sw128(r, 2 * sub + i)) =
+          make_float4(s2[4 * i], s2[4 * i + 1], s2[4 * i + 2], s2[4 * i + 3]);
+  }
+}
+
 // bf16 states: a chunk is 128 rows x 32 columns (m and v 8 KiB each in
 // shared memory, 64-byte rows with the 64-byte swizzle); this thread owns 8
 // columns of row r (16 bytes of each state), starting at element e0.  The
@@ -1347,16 +1394,18 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
   }
 }
 
-// A compute warp of the FORGE epilogue (bf16 weights).  Warp w reads TMEM
-// lanes 32*(w%4).. (its rows) and a quarter of each chunk's columns; its bf16
-// weights (and old INT8 scales) come straight from global memory one chunk
-// ahead, its states from the staged chunk in shared memory.
-template <int KIND, int SDT, int MODE>
+// A compute warp of the FORGE epilogue.  Warp w reads TMEM lanes 32*(w%4)..
+// (its rows) and a quarter of each chunk's columns; its weights (bf16, or fp32
+// with fp32 states) and old INT8 scales come straight from global memory one
+// chunk ahead, its states from the staged chunk in shared memory.
+template <int KIND, int WDT, int SDT, int MODE>
 __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint8_t* epi,
                                       int warp, int lane, uint32_t rank) {
   using G = StagedGeom<KIND, SDT>;
   constexpr bool STEP = MODE == kModeStep, SCALE = MODE == kModeFusedFp8;
+  constexpr bool F32W = WDT == kWFp32;
   constexpr int kCC = G::kCC, kChunks = G::kChunks, kWPerThread = G::kWPerThread;
+  constexpr int kWV = kWPerThread * (F32W ? 4 : 2) / 16;  // 16-byte words of weights per thread and chunk
   const int quarter = warp & 3, sub = (warp - 2) >> 2;  // TMEM lane quarter, column quarter
   const int r = quarter * 32 + lane;
   const int64_t K = p.Ncols;
@@ -1376,17 +1425,17 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   // bytes per element, so they bypass the staging; plain (L1-allocating)
   // loads let the four warps that own the 64 bytes of a row's chunk share one
   // L1 fill instead of four L2 requests.
-  auto prefetch = [&](int j, uint4 (&v)[kWPerThread / 8], float& o1, float& o2) {
+  auto prefetch = [&](int j, uint4 (&v)[kWV], float& o1, float& o2) {
     int row0, col0;
     walk.where(j, kCC, row0, col0);
     const int64_t row = static_cast<int64_t>(row0) + r;
     const int col = col0 + sub * kWPerThread;
     const bool ok = row < p.M && col < K;
-    const uint16_t* q = static_cast<const uint16_t*>(p.W) + row * K + col;
     if (!G::WST) {
+      const uint8_t* q = static_cast<const uint8_t*>(p.W) + (row * K + col) * (F32W ? 4 : 2);
 #pragma unroll
-      for (int h = 0; h < kWPerThread / 8; ++h)
-        v[h] = ok ? *reinterpret_cast<const uint4*>(q + 8 * h) : make_uint4(0, 0, 0, 0);
+      for (int h = 0; h < kWV; ++h)
+        v[h] = ok ? *reinterpret_cast<const uint4*>(q + 16 * h) : make_uint4(0, 0, 0, 0);
     }
     // the old scale of this thread's code block; blocks of 64 or more
     // columns are whole in a quarter's row of the chunk, so after the first
@@ -1399,7 +1448,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
       if (G::U2) o2 = okb ? p.s2_scale[sidx] : 0.f;
     }
   };
-  uint4 wnext[kWPerThread / 8];
+  uint4 wnext[kWV];
   float o1next = 0.f, o2next = 0.f;  // old INT8 scales of the next chunk
   int local = -1;
   if (STEP) {  // the pair's dX tiles: 64 columns per warp into the staging boxes
@@ -1436,7 +1485,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     int row0, col0;
     walk.where(j, kCC, row0, col0);
     const int64_t row = static_cast<int64_t>(row0) + r;
-    uint4 wcur[kWPerThread / 8];
+    uint4 wcur[kWV];
     uint8_t* buf = epi + (j & 1) * G::kBuf;
     float o1 = o1next, o2 = o2next;
     if (G::WST) {  // staged weights; old scales from the quarter that loaded them
@@ -1451,7 +1500,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
       if (j + 1 < total && (sub == 0 || own)) prefetch(j + 1, wnext, o1next, o2next);
     } else {
 #pragma unroll
-      for (int h = 0; h < kWPerThread / 8; ++h) wcur[h] = wnext[h];
+      for (int h = 0; h < kWV; ++h) wcur[h] = wnext[h];
       if (G::I8 && j > 0 && !own) {  // old scales from the quarter that loaded them
         const float* old = reinterpret_cast<const float*>(buf + G::kOffOld);
         o1 = old[r];
@@ -1487,7 +1536,10 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     } else if (G::BF) {
       epi_chunk_bf16s<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     } else {
-      epi_chunk_fp32<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
+      if constexpr (F32W)
+        epi_chunk_fp32w<KIND>(taddr, buf, r, sub, *reinterpret_cast<uint4(*)[2]>(wcur), p);
+      else
+        epi_chunk_fp32<KIND, SCALE>(taddr, buf, r, sub, e0, wcur[0], p);
     }
     if (G::WST) {  // back to the staged chunk (TMA-stored); the next chunk's old scales
 #pragma unroll
@@ -1513,9 +1565,9 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
     // wait for: they are ordered by nothing in this CTA.
     ptx::fence_proxy_async_smem();
     if (!G::WST && row < p.M && col < K) {
-      uint16_t* q = static_cast<uint16_t*>(p.W) + e0;
+      uint8_t* q = static_cast<uint8_t*>(p.W) + e0 * (F32W ? 4 : 2);
 #pragma unroll
-      for (int h = 0; h < kWPerThread / 8; ++h) *reinterpret_cast<uint4*>(q + 8 * h) = wcur[h];
+      for (int h = 0; h < kWV; ++h) *reinterpret_cast<uint4*>(q + 16 * h) = wcur[h];
     }
     // INT8: the thread with the block's last 16 columns stores the block's
     // new absmax; a block wider than a chunk keeps its old one until its last
@@ -1539,7 +1591,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   }
 }
 
-template <int KIND, int SDT, int MODE>
+template <int KIND, int WDT, int SDT, int MODE>
 __device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                                 const CUtensorMap* mDX, const CUtensorMap* mW,
                                                 const GemmParams& p,
@@ -1548,24 +1600,24 @@ __device__ __forceinline__ void epilogue_staged(const CUtensorMap* mS1, const CU
   if (warp == 2 + kNumEpiWarpsStaged)
     epilogue_io_role<KIND, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, lane, rank);
   else
-    epilogue_compute_role<KIND, SDT, MODE>(p, ss, epi, warp, lane, rank);
+    epilogue_compute_role<KIND, WDT, SDT, MODE>(p, ss, epi, warp, lane, rank);
 }
 
-template <int SDT, int MODE>
+template <int WDT, int SDT, int MODE>
 __device__ __forceinline__ void epilogue_tma_dispatch(const CUtensorMap* mS1, const CUtensorMap* mS2,
                                                       const CUtensorMap* mDX, const CUtensorMap* mW,
                                                       const GemmParams& p,
                                                       SharedState* ss, uint8_t* epi, int warp,
                                                       int lane, uint32_t rank) {
   switch (p.sc.kind) {
-    case kAdamW: epilogue_staged<kAdamW, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    case kNAdam: epilogue_staged<kNAdam, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    case kRAdam: epilogue_staged<kRAdam, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    case kLion: epilogue_staged<kLion, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    case kRMSprop: epilogue_staged<kRMSprop, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    case kAdaGrad: epilogue_staged<kAdaGrad, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    case kSGD: epilogue_staged<kSGD, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
-    default: epilogue_staged<kSGDMomentum, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kAdamW: epilogue_staged<kAdamW, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kNAdam: epilogue_staged<kNAdam, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kRAdam: epilogue_staged<kRAdam, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kLion: epilogue_staged<kLion, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kRMSprop: epilogue_staged<kRMSprop, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kAdaGrad: epilogue_staged<kAdaGrad, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    case kSGD: epilogue_staged<kSGD, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
+    default: epilogue_staged<kSGDMomentum, WDT, SDT, MODE>(mS1, mS2, mDX, mW, p, ss, epi, warp, lane, rank); break;
   }
 }
 
@@ -1633,7 +1685,7 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
     if (lane == 0 && rank == 0) mma_role<MODE, STG, Cfg::kBK>(p, smA, smB, ss);
   } else {
     if constexpr (Cfg::kTmaEpi)
-      epilogue_tma_dispatch<SDT, MODE>(&mapS1, &mapS2, &mapDX, &mapW, p, ss, epi, warp, lane, rank);
+      epilogue_tma_dispatch<WDT, SDT, MODE>(&mapS1, &mapS2, &mapDX, &mapW, p, ss, epi, warp, lane, rank);
     else
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
