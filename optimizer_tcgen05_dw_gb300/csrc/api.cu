@@ -462,7 +462,8 @@ forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_
     return FORGE_OK;
   }
   if (w_dtype == FORGE_W_FP32) {
-    if ((e = launch_dgrad_fp32w(lin->dY, static_cast<const float*>(W), lin->dX, T, N, K, s)) != cudaSuccess)
+    if ((e = launch_dgrad_fp32w(lin->dY, static_cast<const float*>(W), lin->dX, T, N, K, d.num_sms, s)) !=
+        cudaSuccess)
       return cuda_fail(e, "dX (fp32 weights) launch");
     return FORGE_OK;
   }
@@ -655,9 +656,11 @@ forge_status_t bwd_step(const forge_linear_t* lin, const forge_state_t* state, i
         (st = mn_major_3d_map(&mbh, lin->X, lin->K, lin->T, bk, 1)) != FORGE_OK)
       return st;
   }
+  // after the fp32-weight dX kernel the step may start at once: its epilogue
+  // waits for dX (which reads the weights it overwrites) before any write
+  const bool after_dx = lin->dX != nullptr && state->w_dtype == FORGE_W_FP32 && lin->N > 0;
   if ((e = launch_tc_fused(state->w_dtype, kernel_sdt(state, lin->T), ma, mb, mbh, m1, m2, mw, p,
-                           grid_for(p, d), s)) !=
-      cudaSuccess)
+                           grid_for(p, d), s, after_dx)) != cudaSuccess)
     return cuda_fail(e, "fused step launch");
   return FORGE_OK;
 }

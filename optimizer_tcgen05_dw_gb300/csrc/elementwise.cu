@@ -235,39 +235,54 @@ __device__ __forceinline__ float round_to_bf16(float x) {
   return __uint_as_float(u & 0xFFFF0000u);
 }
 
-// dX[t, k] = sum_n dY[t, n] * bf16(W[n, k]) with fp32 accumulation; a 64 x 64
-// output tile per block, 4 x 4 per thread, the reduction in slices of 32 n:
-// a 3-deep ring of slices in shared memory filled with asynchronous copies,
-// so two slices are in flight while the block multiplies the third.  Each
-// slice's weights are rounded to bf16 once, in place, when it lands (not once
-// per use: sixteen threads read each).  Each output sums its products in
-// ascending n (one fused multiply-add each).
+// dX[t, k] = sum_n dY[t, n] * bf16(W[n, k]) with fp32 accumulation.  A block
+// of 256 threads owns a TM x TK output tile; SPLIT groups of threads share
+// it, group g taking n = 32 s + g (32 / SPLIT) ... of each 32-n slice s (the
+// groups' sums are added at the end, in group order); a thread keeps 4 x 4
+// outputs (rows ty + (TM / 4) i, columns 4 tx + j).  Slices stream through a
+// 3-deep ring in shared memory filled with asynchronous copies, so two slices
+// are in flight while the block multiplies the third.  Each slice's weights
+// are rounded to bf16 once, in place, when it lands (not once per use).
+// Within a group each output sums its products in ascending n (one fused
+// multiply-add each).  64 x 64 tiles for grids that fill the GPU; 32 x 32
+// tiles split four ways give small layers four times as many blocks.
+//
+// The block lets a dependent grid launch at once (programmatic dependent
+// launch): the FORGE step that follows on the stream starts its main loop
+// while dX runs, and waits for this grid before its first weight write.
 constexpr int kDgStages = 3;
+template <int TM, int TK, int SPLIT>
 __global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* __restrict__ dY,
                                                           const float* __restrict__ W,
                                                           __nv_bfloat16* __restrict__ dX,
                                                           int64_t T, int64_t N, int64_t K) {
-  __shared__ __align__(16) uint16_t sA[kDgStages][64][40];  // [stage][t][n]: dY bits, 80-byte rows
-  __shared__ __align__(16) float sB[kDgStages][32][64];     // [stage][n][k]: W
+  constexpr int kGroup = (TM / 4) * (TK / 4);  // threads per group
+  constexpr int kNPer = 32 / SPLIT;            // n per group and slice
+  static_assert(kGroup * SPLIT == 256, "256 threads per block");
+  static_assert((SPLIT - 1) * TM * TK <= kDgStages * 32 * TK, "the partial sums reuse the weight ring");
+  __shared__ __align__(16) uint16_t sA[kDgStages][TM][40];  // [stage][t][n]: dY bits, 80-byte rows
+  __shared__ __align__(16) float sB[kDgStages][32][TK];     // [stage][n][k]: W
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = static_cast<int>(threadIdx.x);
-  const int tx = tid & 15, ty = tid >> 4;
-  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * 64, k0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const int grp = tid / kGroup, lt = tid % kGroup;
+  const int tx = lt % (TK / 4), ty = lt / (TK / 4);
+  const int64_t t0 = static_cast<int64_t>(blockIdx.y) * TM, k0 = static_cast<int64_t>(blockIdx.x) * TK;
   const int64_t slices = (N + 31) / 32;
   // slice `sl` into stage `st`: dY rows of 32 n (four 16-byte pieces each),
-  // W rows of 64 k (sixteen pieces each); N and K are multiples of 8, so a
+  // W rows of TK k (TK / 4 pieces each); N and K are multiples of 8, so a
   // piece is wholly inside or wholly outside the matrix
   auto load = [&](int64_t sl, int st) {
     if (sl < slices) {
       const int64_t n0 = sl * 32;
-      {
-        const int row = tid >> 2, ch = tid & 3;
+      for (int c = tid; c < TM * 4; c += 256) {
+        const int row = c >> 2, ch = c & 3;
         const int64_t t = t0 + row, n = n0 + ch * 8;
         const bool ok = t < T && n < N;
         cp_async16(&sA[st][row][ch * 8], ok ? static_cast<const void*>(dY + t * N + n) : dY, ok);
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = tid + u * 256, nr = c >> 4, kc = c & 15;
+      for (int c = tid; c < 8 * TK; c += 256) {
+        const int nr = c / (TK / 4), kc = c % (TK / 4);
         const int64_t n = n0 + nr, k = k0 + kc * 4;
         const bool ok = n < N && k < K;
         cp_async16(&sB[st][nr][kc * 4], ok ? static_cast<const void*>(W + n * K + k) : W, ok);
@@ -283,18 +298,19 @@ __global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* _
     __syncthreads();                 // ... everyone's; and slice sl - 1 is no longer read
     const int st = static_cast<int>(sl % kDgStages);
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {  // the slice's 32 x 64 weights, each once
-      const int e = tid + u * 256;
-      float& x = sB[st][e >> 6][e & 63];
+    for (int e = tid; e < 32 * TK; e += 256) {  // the slice's 32 x TK weights, each once
+      float& x = sB[st][e / TK][e % TK];
       x = round_to_bf16(x);
     }
     __syncthreads();
     load(sl + kDgStages - 1, static_cast<int>((sl + kDgStages - 1) % kDgStages));
 #pragma unroll 4
-    for (int nn = 0; nn < 32; ++nn) {
+    for (int q = 0; q < kNPer; ++q) {
+      const int nn = grp * kNPer + q;
       float a[4], w[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = __uint_as_float(static_cast<uint32_t>(sA[st][ty * 4 + i][nn]) << 16);
+      for (int i = 0; i < 4; ++i)
+        a[i] = __uint_as_float(static_cast<uint32_t>(sA[st][ty + (TM / 4) * i][nn]) << 16);
       const float4 wv = *reinterpret_cast<const float4*>(&sB[st][nn][tx * 4]);
       w[0] = wv.x;
       w[1] = wv.y;
@@ -307,15 +323,36 @@ __global__ void __launch_bounds__(256) dgrad_fp32w_kernel(const __nv_bfloat16* _
     }
   }
   cp_async_wait<0>();
+  if constexpr (SPLIT > 1) {  // groups 1.. hand their sums to group 0 through the weight ring
+    __syncthreads();          // every thread is done with the ring
+    float* part = &sB[0][0][0];
+    if (grp > 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          part[((grp - 1) * TM + ty + (TM / 4) * i) * TK + tx * 4 + j] = acc[i][j];
+    }
+    __syncthreads();
+    if (grp > 0) return;
+#pragma unroll
+    for (int g = 1; g < SPLIT; ++g)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] += part[((g - 1) * TM + ty + (TM / 4) * i) * TK + tx * 4 + j];
+  }
+  const int64_t k = k0 + tx * 4;
+  if (k >= K) return;  // K % 8 == 0: columns k .. k + 3 are all inside or all outside
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int64_t t = t0 + ty * 4 + i;
+    const int64_t t = t0 + ty + (TM / 4) * i;
     if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t k = k0 + tx * 4 + j;
-      if (k < K) dX[t * K + k] = __float2bfloat16_rn(acc[i][j]);
-    }
+    const uint32_t lo = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[i][0]))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[i][1]))) << 16);
+    const uint32_t hi = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[i][2]))) |
+                        (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[i][3]))) << 16);
+    *reinterpret_cast<uint2*>(dX + t * K + k) = make_uint2(lo, hi);
   }
 }
 
@@ -356,10 +393,16 @@ cudaError_t launch_dequantize(const ElemParams& p, int num_sms, cudaStream_t s) 
 }
 
 cudaError_t launch_dgrad_fp32w(const void* dY, const float* W, void* dX, int64_t T, int64_t N,
-                               int64_t K, cudaStream_t s) {
-  const dim3 grid(static_cast<unsigned>((K + 63) / 64), static_cast<unsigned>((T + 63) / 64));
-  dgrad_fp32w_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(dY), W,
-                                          static_cast<__nv_bfloat16*>(dX), T, N, K);
+                               int64_t K, int num_sms, cudaStream_t s) {
+  const auto* y = static_cast<const __nv_bfloat16*>(dY);
+  auto* x = static_cast<__nv_bfloat16*>(dX);
+  if (((K + 63) / 64) * ((T + 63) / 64) >= num_sms) {
+    const dim3 grid(static_cast<unsigned>((K + 63) / 64), static_cast<unsigned>((T + 63) / 64));
+    dgrad_fp32w_kernel<64, 64, 1><<<grid, 256, 0, s>>>(y, W, x, T, N, K);
+  } else {
+    const dim3 grid(static_cast<unsigned>((K + 31) / 32), static_cast<unsigned>((T + 31) / 32));
+    dgrad_fp32w_kernel<32, 32, 4><<<grid, 256, 0, s>>>(y, W, x, T, N, K);
+  }
   return cudaGetLastError();
 }
 

@@ -32,9 +32,13 @@ struct ElemParams {
 // (128-byte swizzle), staged when sdt is kSInt8W (else any valid map); bh:
 // the B operand in 64-column boxes for half units (GemmParams::split_from;
 // any valid map when nothing is split).
+// With `after_dx` the launch may start while the fp32-weight dX kernel before
+// it on the stream still runs (programmatic dependent launch); its epilogue
+// waits for that grid before writing weights or states.
 cudaError_t launch_tc_fused(int wdt, int sdt, const CUtensorMap& a, const CUtensorMap& b,
                             const CUtensorMap& bh, const CUtensorMap& s1, const CUtensorMap& s2,
-                            const CUtensorMap& w, const GemmParams& p, int grid, cudaStream_t s);
+                            const CUtensorMap& w, const GemmParams& p, int grid, cudaStream_t s,
+                            bool after_dx = false);
 // tc_step.cu: dX and the FORGE step in one launch (mode kModeStep, bf16
 // weights): a, b the dW operands, da, db the dX operands (dY K-major, W),
 // dx the dX output (bf16, 64-column x 128-row boxes, 128-byte swizzle).
@@ -59,8 +63,9 @@ cudaError_t launch_tc_plain(int mode, const CUtensorMap& a, const CUtensorMap& b
 cudaError_t launch_opt_step(int wdt, int sdt, const ElemParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_quantize(const ElemParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_dequantize(const ElemParams& p, int num_sms, cudaStream_t s);
-// dX = dY * bf16(W) for fp32 master weights (CUDA cores).
+// dX = dY * bf16(W) for fp32 master weights (CUDA cores); its blocks let the
+// next launch on the stream start early (programmatic dependent launch).
 cudaError_t launch_dgrad_fp32w(const void* dY, const float* W, void* dX, int64_t T, int64_t N,
-                               int64_t K, cudaStream_t s);
+                               int64_t K, int num_sms, cudaStream_t s);
 
 }  // namespace forge

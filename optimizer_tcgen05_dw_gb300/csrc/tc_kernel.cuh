@@ -700,6 +700,7 @@ __device__ void epilogue_role(const GemmParams& p, SharedState* ss, int warp, in
     bool ok = true;
     if (warp == 2 && lane == 0) ok = bounded_wait(&ss->tmem_full[acc], aph, p, ss);
     if (ptx::bar_red_or(kEpiBarrier, 32 * kNumEpiWarps, !ok)) break;
+    if (MODE == kModeFusedOpt && local == 0) ptx::grid_dep_wait();  // before the first write
     ptx::tc_fence_after();
     const uint32_t tbase = ss->tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                            static_cast<uint32_t>(acc * kTileN + half * 128);
@@ -1364,6 +1365,7 @@ __device__ void epilogue_io_role(const CUtensorMap* mS1, const CUtensorMap* mS2,
     if (io) {
       issue(0);
       issued = 1;
+      if (MODE == kModeFusedOpt) ptx::grid_dep_wait();  // before the first store
     }
     stop = ptx::bar_red_or(kEpiBarrier, G::kNB, !ready(0));
     if (!stop) consumed = 1;
@@ -1477,6 +1479,7 @@ __device__ void epilogue_compute_role(const GemmParams& p, SharedState* ss, uint
   bool stop = total == 0;
   if (!stop) {
     prefetch(0, wnext, o1next, o2next);
+    if (MODE == kModeFusedOpt) ptx::grid_dep_wait();  // before the first write
     begin(0);
     stop = ptx::bar_red_or(kEpiBarrier, G::kNB, false);  // the I/O warp's verdict
   }
@@ -1702,24 +1705,29 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
 }
 
 // Launch on clusters of two CTAs (the tcgen05 pair); grid is a multiple of 2.
+// `early`: the launch may begin before the previous kernel on the stream ends
+// (programmatic stream serialisation; that kernel lets it in, and the
+// epilogue's grid_dep_wait orders the writes after it).
 template <typename Kernel>
 inline cudaError_t launch_pair(Kernel k, int grid, int threads, int smem, cudaStream_t s,
                                const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& da,
                                const CUtensorMap& db, const CUtensorMap& s1,
                                const CUtensorMap& s2, const CUtensorMap& dx, const CUtensorMap& w,
-                               const GemmParams& p) {
+                               const GemmParams& p, bool early = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = early ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, k, a, b, da, db, s1, s2, dx, w, p);
 }
 

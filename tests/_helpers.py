@@ -150,8 +150,10 @@ class Problem:
               for k, v in self.state0.items()}
         hp = oracle_hparams(self.hp)
         dxs, sens = [], np.zeros((self.N, self.K), dtype=bool)
+        self.w_before = []  # the weights each step starts from (dX reads them)
         for s in range(self.steps):
             Xb, dYb = to_bits(self.X[s]), to_bits(self.dY[s])
+            self.w_before.append(st["W"])
             sens |= self.sensitive(Xb, dYb, st)
             if self.qblock == 64:
                 out = ls.linear_bwd_step(Xb, dYb, st, self.kind, hp, s + 1, self.seed, want_dx=want_dx)

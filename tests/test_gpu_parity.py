@@ -103,6 +103,23 @@ def test_unfused_wgrad_equals_exact_gradient():
     assert_bitexact(dW, ls.weight_gradient(to_bits(prob.X[0]), to_bits(prob.dY[0])), "dW")
 
 
+@pytest.mark.parametrize("shape", [dict(T=200, N=264, K=320), dict(T=1000, N=256, K=640)],
+                         ids=["small_grid", "full_grid"])
+def test_fp32_master_dx_every_step(shape):
+    """fp32 master weights with dX: the dX kernel (32 x 32 tiles split four
+    ways on a small grid, 64 x 64 tiles once the grid fills the GPU) and the
+    step that starts while it runs.  Every step's dX must come from that
+    step's pre-update weights, and the update must still match bit for bit."""
+    prob = Problem(**shape, w_dtype="fp32", s_dtype="fp32", opt_name="adamw", hp=_hp("adamw"),
+                   grid=True, steps=3, seed=17)
+    gpu, gdx = prob.run_gpu(fused=True, want_dx=True)
+    ref, _, _ = prob.run_oracle(want_dx=True)
+    _compare_exact(prob, gpu, ref)
+    for s in range(prob.steps):
+        assert_dx_close(gdx[s], to_bits(prob.dY[s]), ls.weights_for_dx(prob.w_before[s], "fp32"),
+                        f"dX step {s + 1}")
+
+
 # --------------------------------------------------------------- realistic data
 
 def test_single_layer_fp32_master_config():
