@@ -108,6 +108,9 @@ def library_path() -> str:
 def lib() -> ctypes.CDLL:
     """The loaded libforge.  Raises if it has not been built (no fallback)."""
     global _lib
+    L = _lib
+    if L is not None:
+        return L
     with _lock:
         if _lib is None:
             path = library_path()
@@ -130,15 +133,24 @@ def _check(status: int):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
+
+
+# The current stream's handle without building a torch.cuda.Stream object
+# (the call's largest fixed cost otherwise); the public route until CUDA is
+# initialised or where these accessors are missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
 
 
 def _stream(stream):
     if stream is None:
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        if _raw_stream is not None and _cur_device is not None and torch.cuda.is_initialized():
+            return _raw_stream(_cur_device())
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
-        return ctypes.c_void_p(stream.cuda_stream)
-    return ctypes.c_void_p(int(stream))
+        return stream.cuda_stream
+    return int(stream)
 
 
 def _need(t, name, dtype, shape):
@@ -146,7 +158,7 @@ def _need(t, name, dtype, shape):
         raise ValueError(f"{name} is required")
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
-    if tuple(t.shape) != tuple(shape):
+    if t.shape != shape:
         raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
@@ -163,18 +175,48 @@ def hparams(**kw) -> ForgeHparams:
     return ForgeHparams(**{k: float(v) for k, v in h.items()})
 
 
+_hp_cache = {}
+
+
+def _hparams_of(hp: dict) -> ForgeHparams:
+    """hparams(**hp), kept for dicts of plain Python numbers (the library only
+    reads the struct during the call, so calls may share it)."""
+    try:
+        key = tuple(hp.items())
+        h = _hp_cache.get(key)
+    except TypeError:  # an unhashable value
+        return hparams(**hp)
+    if h is None:
+        h = hparams(**hp)
+        if all(type(v) in (float, int) for _, v in key):
+            if len(_hp_cache) >= 256:
+                _hp_cache.clear()
+            _hp_cache[key] = h
+    return h
+
+
 def make_state(W, s1=None, s2=None, s1_scale=None, s2_scale=None) -> ForgeState:
     """A forge_state_t for W (fp32 or bf16) and optional fp32 / INT8 states."""
     N, K = W.shape
-    if W.dtype == torch.float32:
+    wd = W.dtype
+    if wd == torch.float32:
         wdt = W_FP32
-    elif W.dtype == torch.bfloat16:
+    elif wd == torch.bfloat16:
         wdt = W_BF16_SR
     else:
         raise TypeError(f"W must be float32 or bfloat16, got {W.dtype}")
-    _need(W, "W", W.dtype, (N, K))
-    int8 = any(t is not None and t.dtype in (torch.int8, torch.uint8) for t in (s1, s2))
-    bf16 = any(t is not None and t.dtype == torch.bfloat16 for t in (s1, s2))
+    _need(W, "W", wd, (N, K))
+    d1 = None if s1 is None else s1.dtype
+    d2 = None if s2 is None else s2.dtype
+    if d1 in (None, torch.float32) and d2 in (None, torch.float32):  # fp32 or no states
+        if s1 is not None:
+            _need(s1, "s1", torch.float32, (N, K))
+        if s2 is not None:
+            _need(s2, "s2", torch.float32, (N, K))
+        return ForgeState(W.data_ptr(), wdt, STATE_FP32, _ptr(s1), _ptr(s2), _ptr(s1_scale),
+                          _ptr(s2_scale))
+    int8 = d1 in (torch.int8, torch.uint8) or d2 in (torch.int8, torch.uint8)
+    bf16 = d1 == torch.bfloat16 or d2 == torch.bfloat16
     if bf16:
         for t, nm in ((s1, "s1"), (s2, "s2")):
             if t is not None:
@@ -215,7 +257,7 @@ def forge_linear_bwd_step(X, dY, W, opt: str, hp: dict, step: int, seed: int, s1
     st = make_state(W, s1, s2, s1_scale, s2_scale)
     lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), _ptr(dX))
     _check(lib().forge_linear_bwd_step(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
-                                       ctypes.byref(hparams(**hp)), int(step),
+                                       ctypes.byref(_hparams_of(hp)), int(step),
                                        int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
@@ -235,7 +277,7 @@ def forge_linear_bwd_step_shard(X, dY, W, opt: str, hp: dict, step: int, seed: i
     st = make_state(W, s1, s2, s1_scale, s2_scale)
     lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), _ptr(dX))
     _check(lib().forge_linear_bwd_step_shard(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
-                                             ctypes.byref(hparams(**hp)), int(step),
+                                             ctypes.byref(_hparams_of(hp)), int(step),
                                              int(seed) & 0xFFFFFFFFFFFFFFFF, int(row_offset),
                                              _stream(stream)))
 
@@ -253,7 +295,7 @@ def forge_linear_bwd_step_static(X, dY, W, opt: str, hp: dict, step: int, seed: 
     st = make_state(W, s1, s2, s1_scale, s2_scale)
     lin = ForgeLinear(T, N, K, _ptr(X), _ptr(dY), _ptr(dX))
     _check(lib().forge_linear_bwd_step_static(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
-                                              ctypes.byref(hparams(**hp)), int(step),
+                                              ctypes.byref(_hparams_of(hp)), int(step),
                                               int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
@@ -272,7 +314,7 @@ def forge_linear_bwd_step_fp8(Xt, dYt, x_scale: float, dy_scale: float, W, opt: 
     st = make_state(W, s1, s2, s1_scale, s2_scale)
     lin = ForgeLinearFp8(T, N, K, _ptr(Xt), _ptr(dYt), float(x_scale), float(dy_scale))
     _check(lib().forge_linear_bwd_step_fp8(ctypes.byref(lin), ctypes.byref(st), OPT_KINDS[opt],
-                                           ctypes.byref(hparams(**hp)), int(step),
+                                           ctypes.byref(_hparams_of(hp)), int(step),
                                            int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
@@ -304,7 +346,7 @@ def forge_unfused_opt_step(dW, W, opt: str, hp: dict, step: int, seed: int, s1=N
         _need(dW, "dW", torch.float32, (N, K))
     st = make_state(W, s1, s2, s1_scale, s2_scale)
     _check(lib().forge_unfused_opt_step(_ptr(dW), ctypes.byref(st), N, K, OPT_KINDS[opt],
-                                        ctypes.byref(hparams(**hp)), int(step),
+                                        ctypes.byref(_hparams_of(hp)), int(step),
                                         int(seed) & 0xFFFFFFFFFFFFFFFF, _stream(stream)))
 
 
