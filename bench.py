@@ -814,6 +814,9 @@ def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_lay
     results = {}
     per_linear_ms = {}
     s_no = 1
+    # events around each call give the per-linear rates; with one linear the
+    # region's own events give them, and per-call events would only add gaps
+    per_call = len(layers) > 1
     for opt_name in opts:
         hp = inputs.SWEEP_HPARAMS[opt_name] if sweep else w.hparams
         ev = []
@@ -849,7 +852,7 @@ def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_lay
                 end = torch.cuda.Event(enable_timing=True)
                 start.record(stream)
                 for _ in range(steps):
-                    step(s_no, record=True)
+                    step(s_no, record=per_call)
                     s_no += 1
                 end.record(stream)
                 end.synchronize()
@@ -859,9 +862,13 @@ def measure_workload(api, key, steps, warmup, local=0, only_layers=None, num_lay
             total_s = time.perf_counter() - t_start
         api.forge_get_device_status()
         ms = statistics.median(region_ms)
-        kern_ms = sum(a.elapsed_time(b) for _, a, b in ev)
-        for name, a, b in ev:
-            per_linear_ms.setdefault(name, []).append(a.elapsed_time(b))
+        if per_call:
+            kern_ms = sum(a.elapsed_time(b) for _, a, b in ev)
+            for name, a, b in ev:
+                per_linear_ms.setdefault(name, []).append(a.elapsed_time(b))
+        else:  # one linear: its launches are the whole region
+            kern_ms = sum(region_ms) * steps
+            per_linear_ms.setdefault(layers[0][1].name, []).extend(region_ms)
         results[opt_name] = {"ms_per_step": round(ms, 4),
                              "value": round(flops_step / (ms * 1e-3) / 1e12, 2),
                              "kernel_tflops": round(flops_step * steps * len(region_ms) /

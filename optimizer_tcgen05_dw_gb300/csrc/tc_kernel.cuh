@@ -1693,6 +1693,9 @@ __global__ void __launch_bounds__(KCfg<MODE, WDT, SDT>::kThreads, 1)
       epilogue_role<MODE, WDT, SDT>(p, ss, warp, lane, rank);
   }
 
+  // A dependent launch (after the fp32-weight dX kernel) ends only after that
+  // grid, on every path (the epilogue's waits are skipped when a CTA aborts).
+  if (MODE == kModeFusedOpt) ptx::grid_dep_wait();
   __syncwarp();  // the producer's and MMA thread's lanes rejoin their warps first
   ptx::tc_fence_before();
   __syncthreads();
