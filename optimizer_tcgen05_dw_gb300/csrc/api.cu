@@ -435,20 +435,25 @@ void fill_tiles(GemmParams& p, int64_t M, int64_t Ncols, int64_t red, int bk = k
 }
 
 // A last partial wave of pair tiles (R = num_tiles % pairs of them) runs as
-// 2R column halves when they fit one wave, so that it takes half as long.
-// Only for the staged epilogue without dX tiles.
+// 2R column halves when they fit one wave, so that it takes half as long; a
+// layer of at most pairs / 2 tiles (wider than 128 columns) runs every tile as
+// two halves on twice the pairs.  Either way a pair holds at most one half
+// unit, its last.  Only for the staged epilogue without dX tiles.
 void split_tail(GemmParams& p, int pairs) {
   const int F = p.num_tiles, R = F % pairs;
   if (F > pairs && R > 0 && 2 * R <= pairs) {
     p.split_from = F - R;
     p.num_units = F + R;
+  } else if (F > 0 && 2 * F <= pairs && p.Ncols > kTileN / 2) {
+    p.split_from = 0;
+    p.num_units = 2 * F;
   }
 }
 
-// Clusters of two CTAs, at most one CTA per SM.
+// Clusters of two CTAs, at most one CTA per SM, at most one pair per unit.
 int grid_for(const GemmParams& p, const DeviceInfo& d) {
   const int pairs = d.num_sms / 2;
-  return 2 * (p.num_tiles < pairs ? p.num_tiles : pairs);
+  return 2 * (p.num_units < pairs ? p.num_units : pairs);
 }
 
 forge_status_t launch_dgrad(const forge_linear_t* lin, const void* W, int32_t w_dtype, cudaStream_t s,

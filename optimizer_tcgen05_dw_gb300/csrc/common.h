@@ -108,7 +108,9 @@ struct GemmParams {
   // Work units of the weight tiles: tiles 0 .. split_from-1 whole, then each
   // remaining tile as two 128-column halves (units split_from ..
   // num_units-1), so that a last partial wave of pair tiles becomes half as
-  // long.  split_from == num_tiles == num_units when nothing is split.
+  // long, or (split_from == 0) a small layer's tiles spread over twice the
+  // pairs.  A pair holds at most one half unit, its last.  split_from ==
+  // num_tiles == num_units when nothing is split.
   int32_t num_units, split_from;
   void* out;                 // wgrad store: fp32 [M x Ncols]; dgrad: bf16 [M x Ncols]
   void* W;                   // fused: [M x Ncols] fp32 or bf16

@@ -448,15 +448,31 @@ def test_nonfinite_activations_match_oracle(opt_name, s_dtype):
 
 @pytest.mark.parametrize("shape", [dict(T=208, N=2560, K=2048), dict(T=144, N=2568, K=2048)],
                          ids=["aligned", "ragged_rows"])
-@pytest.mark.parametrize("opt_name,s_dtype", [("adamw", "fp32"), ("adamw", "int8"), ("lion", "bf16"),
-                                              ("sgd_momentum", "fp32")])
-def test_split_last_wave_bitexact(shape, opt_name, s_dtype):
+@pytest.mark.parametrize("w_dtype,opt_name,s_dtype", [("bf16", "adamw", "fp32"), ("bf16", "adamw", "int8"),
+                                                      ("bf16", "lion", "bf16"), ("bf16", "sgd_momentum", "fp32"),
+                                                      ("fp32", "adamw", "fp32"), ("fp32", "sgd_momentum", "fp32")])
+def test_split_last_wave_bitexact(shape, w_dtype, opt_name, s_dtype):
     """More pair tiles than CTA pairs with a short last wave (80 or 88 tiles
     on 76 pairs): the last partial wave runs as 128-column half tiles (N = 128
     MMAs, half-width operand boxes).  Every element still matches the oracle
     bit for bit, in the split tiles as elsewhere."""
-    prob = Problem(**shape, w_dtype="bf16", s_dtype=s_dtype, opt_name=opt_name, hp=_hp(opt_name),
+    prob = Problem(**shape, w_dtype=w_dtype, s_dtype=s_dtype, opt_name=opt_name, hp=_hp(opt_name),
                    grid=True, steps=2, seed=47)
+    gpu, _ = prob.run_gpu(fused=True)
+    ref, _, _ = prob.run_oracle()
+    _compare_exact(prob, gpu, ref)
+
+
+@pytest.mark.parametrize("shape", [dict(T=300, N=256, K=256), dict(T=136, N=1288, K=1408),
+                                   dict(T=64, N=512, K=4864)],
+                         ids=["one_tile", "ragged_36_tiles", "38_tiles"])
+@pytest.mark.parametrize("w_dtype,s_dtype", [("bf16", "fp32"), ("bf16", "int8"), ("fp32", "fp32")])
+def test_small_layer_half_units_bitexact(shape, w_dtype, s_dtype):
+    """A layer of at most 38 pair tiles (half the 76 pairs) runs every tile as
+    two 128-column halves on twice the pairs; the result is the oracle's bit
+    for bit, ragged edges included."""
+    prob = Problem(**shape, w_dtype=w_dtype, s_dtype=s_dtype, opt_name="adamw", hp=_hp("adamw"),
+                   grid=True, steps=2, seed=53)
     gpu, _ = prob.run_gpu(fused=True)
     ref, _, _ = prob.run_oracle()
     _compare_exact(prob, gpu, ref)
