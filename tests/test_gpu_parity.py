@@ -103,13 +103,15 @@ def test_unfused_wgrad_equals_exact_gradient():
     assert_bitexact(dW, ls.weight_gradient(to_bits(prob.X[0]), to_bits(prob.dY[0])), "dW")
 
 
-@pytest.mark.parametrize("shape", [dict(T=200, N=264, K=320), dict(T=1000, N=256, K=648)],
-                         ids=["small_grid", "full_grid"])
+@pytest.mark.parametrize("shape", [dict(T=200, N=264, K=320), dict(T=1000, N=256, K=648),
+                                   dict(T=4096, N=1024, K=1024)],
+                         ids=["small_grid", "full_grid", "long_dx"])
 def test_fp32_master_dx_every_step(shape):
     """fp32 master weights with dX: the dX kernel (32 x 32 tiles split four
-    ways on a small grid, 64 x 64 tiles once the grid fills the GPU) and the
-    step that starts while it runs.  Every step's dX must come from that
-    step's pre-update weights, and the update must still match bit for bit."""
+    ways on a small grid, 64 x 64 tiles once the grid fills the GPU, several
+    waves of them in `long_dx`) and the step that starts while it runs.  Every
+    step's dX must come from that step's pre-update weights, and the update
+    must still match bit for bit."""
     prob = Problem(**shape, w_dtype="fp32", s_dtype="fp32", opt_name="adamw", hp=_hp("adamw"),
                    grid=True, steps=3, seed=17)
     gpu, gdx = prob.run_gpu(fused=True, want_dx=True)
