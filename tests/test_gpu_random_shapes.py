@@ -1,7 +1,7 @@
 """Seeded random layers against the oracle, bit for bit.
 
 Twenty configurations drawn from one seed: T in 1..1200, N and K multiples of 8
-(half of them of 64) in 8..640, one of the eight rules, one of the weight/state dtypes (and for INT8
+(half of them of 64) in 8..640 (and twelve with T up to 300, N and K up to 2560), one of the eight rules, one of the weight/state dtypes (and for INT8
 states with bf16 weights one of the four block widths that divide K), with or
 without dX.  Integer-grid inputs keep every FP32 sum exact, so W, the states and
 the INT8 scales must equal the oracle's bit for bit, and dX must lie within its
@@ -24,12 +24,12 @@ RULES = ["adamw", "nadam", "radam", "lion", "rmsprop", "adagrad", "sgd", "sgd_mo
 DTYPES = [("fp32", "fp32"), ("bf16", "fp32"), ("bf16", "int8"), ("bf16", "bf16"), ("fp32", "int8")]
 
 
-def _draw(i):
+def _draw(i, t_max=1200, nk_max=640):
     rng = np.random.default_rng(9000 + i)
-    T = int(rng.integers(1, 1201))
+    T = int(rng.integers(1, t_max + 1))
     align = 64 if rng.integers(0, 2) else 8  # half the draws take the one-launch form's alignment
-    N = align * int(rng.integers(1, 640 // align + 1))
-    K = align * int(rng.integers(1, 640 // align + 1))
+    N = align * int(rng.integers(1, nk_max // align + 1))
+    K = align * int(rng.integers(1, nk_max // align + 1))
     w_dtype, s_dtype = DTYPES[int(rng.integers(0, len(DTYPES)))]
     qblock = 64
     if s_dtype == "int8":
@@ -58,7 +58,18 @@ def _library(cuda_device):
 
 @pytest.mark.parametrize("i", range(20))
 def test_random_layer_bitexact_on_integer_grid(i):
-    c = _draw(i)
+    _check_draw(i, _draw(i))
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_mid_layer_bitexact_on_integer_grid(i):
+    """Wider layers (N, K up to 2560, T up to 300): up to 100 pair tiles, so the
+    draws fall on all three tile schedules: every tile as two column halves
+    (at most 38 tiles), whole tiles in one partial wave, and a split last wave."""
+    _check_draw(100 + i, _draw(100 + i, t_max=300, nk_max=2560))
+
+
+def _check_draw(i, c):
     hp = dict(inputs.SWEEP_HPARAMS[c["rule"]])
     hp.setdefault("weight_decay", 0.01)
     prob = Problem(T=c["T"], N=c["N"], K=c["K"], w_dtype=c["w_dtype"], s_dtype=c["s_dtype"],
